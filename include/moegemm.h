@@ -1,0 +1,243 @@
+/*
+ * moegemm.h -- C ABI of libmoegemm.so: the MoE grouped GEMM on one GB300.
+ *
+ * In an MoE layer every expert has the same weight shape, so N and K are
+ * fixed and only the token dimension varies per expert ("flops/deepgemm-
+ * grouped-masked-moe-gemm", "Arithmetic intensity").  The library provides the
+ * planning step ("MoE GroupGEMM padding under expert skew", "Calculate padded
+ * token columns" and "Summarize skew without losing the histogram") and the
+ * three grouped GEMM forms ("flops/deepgemm-grouped-masked-moe-gemm",
+ * "Workarounds"): M-grouped contiguous, masked, and K-grouped weight
+ * gradient.  Every GEMM is a CUDA kernel for sm_103a.
+ *
+ * Conventions used by every call:
+ *   - Tokens are rows.  Expert weights are B[e] of shape [N, K] with K
+ *     contiguous (the nn.Linear layout); each expert computes
+ *     D_e = A_e * B[e]^T, D_e row-major [rows, N].
+ *   - "d_" pointers are device pointers (cudaMalloc / torch CUDA memory);
+ *     all other pointers are host pointers.  The caller allocates and owns
+ *     every buffer; the library allocates no device memory and keeps no
+ *     per-call state.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Device calls only enqueue work on it: they never synchronise
+ *     and never read device memory from the host, so they can be captured in
+ *     a CUDA graph.
+ *   - Errors the host can see (null pointers, bad sizes, bad alignment) are
+ *     returned at once and nothing is launched.  Errors only the device can
+ *     see (a negative count, a count beyond a buffer, a timed-out wait) are
+ *     written to *d_status (int32, device) with the first error winning; the
+ *     caller reads it when it chooses.  d_status may be NULL, in which case
+ *     device-side errors are dropped.  Nothing aborts, traps or throws.
+ *   - Every wait inside a kernel is bounded (see mg_set_wait_limit_ns): a
+ *     kernel that cannot make progress writes MG_ERR_TIMEOUT to *d_status,
+ *     drains its own in-flight copies, frees its tensor memory and returns.
+ *   - Global base addresses must be 16-byte aligned; N and K must be
+ *     multiples of 128.
+ */
+#ifndef MOEGEMM_H
+#define MOEGEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MG_OK = 0,
+  MG_ERR_INVALID_ARG = 1,  /* null pointer, non-positive size, bad value      */
+  MG_ERR_UNSUPPORTED = 2,  /* valid request this build does not handle        */
+  MG_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed               */
+  MG_ERR_CAPACITY = 4,     /* output or tile list too small for the counts     */
+  MG_ERR_TIMEOUT = 5,      /* a device wait ran past the wait limit            */
+  MG_ERR_DEVICE_ARG = 6    /* device-resident argument invalid (count < 0, ...) */
+} mg_status;
+
+typedef enum {
+  MG_BF16 = 0,             /* bf16 operands, fp32 accumulate                   */
+  MG_FP8_E4M3_UE8M0 = 1    /* E4M3 operands with UE8M0 per-128 block scales    */
+} mg_dtype;
+
+/* Padding accounting of one histogram at one token tile q ("MoE GroupGEMM
+ * padding under expert skew", "Calculate padded token columns", "Summarize
+ * skew without losing the histogram").  48 bytes, naturally aligned. */
+typedef struct {
+  int64_t P;           /* padded token rows  sum_e q*ceil(t_e/q)             */
+  int64_t U;           /* useful token rows  sum_e t_e                        */
+  int64_t sumsq;       /* sum_e t_e^2                                         */
+  int32_t active;      /* experts with t_e > 0                                */
+  int32_t num_tiles;   /* sum_e ceil(t_e/q)                                   */
+  double pad_frac;     /* (double)(P-U) / (double)P; 0.0 when P == 0          */
+  double eff_experts;  /* ((double)U*(double)U) / (double)sumsq; 0.0 if none   */
+} mg_plan_stats;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* mg_status_str(mg_status s);
+
+/* ------------------------------------------------------------------------
+ * Planning.  Defined by "MoE GroupGEMM padding under expert skew",
+ * "Calculate padded token columns": with t_e tokens for expert e and token
+ * tile q, expert e executes q*ceil(t_e/q) rows; P sums them, U sums t_e, the
+ * padding fraction is (P-U)/P; effective experts is U^2 / sum t_e^2
+ * ("Summarize skew without losing the histogram").  The offsets are the
+ * M-grouped contiguous layout: expert segments concatenated in expert order,
+ * each starting on a multiple of q ("flops/deepgemm-grouped-masked-moe-gemm",
+ * "Arithmetic intensity").
+ *
+ *   counts / d_counts  int32 [E], t_e >= 0.
+ *   offsets            int64 [E+1]: offsets[e] = sum_{e'<e} q*ceil(t_e'/q),
+ *                      offsets[E] = P.  Expert e's rows: [offsets[e],
+ *                      offsets[e] + t_e).
+ *   tiles              int32 [3*max_tiles] or NULL: triples (e, first_row,
+ *                      rows) for e ascending and j ascending over
+ *                      0..ceil(t_e/q)-1: (e, offsets[e] + j*q,
+ *                      min(q, t_e - j*q)).  Experts with t_e = 0 get none.
+ *   max_tiles          capacity of `tiles` in triples.
+ *   stats              the accounting above.
+ *
+ * If there are more than max_tiles tiles, the first max_tiles are written,
+ * offsets and stats are complete, and the call reports MG_ERR_CAPACITY.
+ * Tile rows are int32: when a tile list is requested and P exceeds 2^31-1,
+ * only tiles whose first row fits are written and the call reports
+ * MG_ERR_UNSUPPORTED (offsets and stats stay complete).
+ * A negative count is MG_ERR_INVALID_ARG (host) / MG_ERR_DEVICE_ARG (device,
+ * that expert counted as 0).  P, U and sumsq are exact in int64 for
+ * E <= 2^20 and t_e < 2^31; the two doubles are correctly rounded IEEE
+ * operations in the order written above, identical on host and device.
+ * ------------------------------------------------------------------------ */
+
+/* Host, synchronous, touches no GPU. */
+mg_status moe_plan_host(const int32_t* counts, int32_t E, int32_t q,
+                        int64_t* offsets, int32_t* tiles, int32_t max_tiles,
+                        mg_plan_stats* stats);
+
+/* Device, stream-ordered; all pointers are device pointers (d_tiles may be
+ * NULL).  One small kernel; the host never reads the counts. */
+mg_status moe_plan(const int32_t* d_counts, int32_t E, int32_t q,
+                   int64_t* d_offsets, int32_t* d_tiles, int32_t max_tiles,
+                   mg_plan_stats* d_stats, int32_t* d_status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Token-tile selection.  The tile along the token dimension is chosen from
+ * the count histogram, on the GPU, with no host round trip ("MoE GroupGEMM
+ * padding under expert skew", "Adapt kernels without adding a CPU stall").
+ * Candidates are priced by padded MMA work, weight/activation traffic and
+ * per-tile scheduling cost ("Padding is not the whole cost model"); the
+ * constants were measured on GB300.  This is the choice mgemm_contiguous
+ * makes when called with tile_q = 0.
+ *
+ *   dt, N, K      as for mgemm_contiguous.
+ *   d_counts      int32 [E] (device) / counts (host).
+ *   d_tile_q      int32 (device): the chosen token tile, one of 32, 64, 128,
+ *                 256 (bf16) or 32, 64, 128, 240 (fp8).
+ *   num_sms       (host variant) SM count to price waves against; <= 0 uses
+ *                 152.
+ * ------------------------------------------------------------------------ */
+mg_status moe_select_tile(mg_dtype dt, const int32_t* d_counts, int32_t E,
+                          int32_t N, int32_t K, int32_t* d_tile_q,
+                          int32_t* d_status, void* stream);
+mg_status moe_select_tile_host(mg_dtype dt, const int32_t* counts, int32_t E,
+                               int32_t N, int32_t K, int32_t num_sms,
+                               int32_t* tile_q);
+
+/* ------------------------------------------------------------------------
+ * M-grouped contiguous grouped GEMM ("flops/deepgemm-grouped-masked-moe-
+ * gemm", "Workarounds": contiguous layout for prefill/training; "Arithmetic
+ * intensity": segments aligned to the M block; "MoE GroupGEMM padding under
+ * expert skew", "Grouped execution does not require padded experts": tiles
+ * are built from each expert's actual count, zero-sized experts load no
+ * weights, tail rows are excluded).
+ *
+ * For every expert e with t_e = d_counts[e] > 0 and every r < t_e:
+ *     D[off_e + r, :] = A[off_e + r, :] * B[e]^T
+ * where off_e = sum_{e'<e} align_q*ceil(t_e'/align_q) (moe_plan at q =
+ * align_q).  No other row of D is written: padding rows keep whatever the
+ * caller left there.
+ *
+ *   A     [rows_cap, K]   bf16, or E4M3 bytes (dt = MG_FP8_E4M3_UE8M0).
+ *   SFA   uint8 [K/128, rows_cap]: UE8M0 scale of (row, 128-wide K block),
+ *         K-block major so one block's scales for consecutive rows are
+ *         contiguous.  fp8 only; NULL for bf16.
+ *   B     [E, N, K]       bf16 or E4M3 bytes.
+ *   SFB   uint8 [E, K/128, N/128]: UE8M0 scale of each 128x128 weight block.
+ *         fp8 only; NULL for bf16.
+ *   D     [rows_cap, N]   bf16 (fp32 accumulation, one final rounding).
+ *   align_q  layout alignment of expert segments (>= 1; a multiple of 16
+ *            for fp8).  rows_cap must be < 2^31.
+ *   tile_q   token tile of the kernel: 0 = chosen on the device from the
+ *            counts (moe_select_tile); otherwise a multiple of 16 in
+ *            [16, 256] (fp8: [16, 240] or 256).  The result does not depend
+ *            on it.
+ *
+ * Value of an E4M3 element: e4m3(x) * 2^(s-127) with s its block's scale
+ * byte.  Device errors: t_e < 0 -> MG_ERR_DEVICE_ARG (expert skipped);
+ * aligned segments beyond rows_cap -> MG_ERR_CAPACITY (experts that do not
+ * fit are skipped).
+ * ------------------------------------------------------------------------ */
+mg_status mgemm_contiguous(mg_dtype dt, const void* A, const uint8_t* SFA,
+                           const void* B, const uint8_t* SFB, void* D,
+                           const int32_t* d_counts, int32_t E,
+                           int64_t rows_cap, int32_t N, int32_t K,
+                           int32_t align_q, int32_t tile_q,
+                           int32_t* d_status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Masked grouped GEMM ("flops/deepgemm-grouped-masked-moe-gemm",
+ * "Workarounds": masked grouped GEMM for decode under CUDA graphs;
+ * "Arithmetic intensity": the kernel takes a mask and computes only the
+ * valid portions, so no CPU sync sits on the critical path).
+ *
+ * For every e and every r < v_e = d_valid_m[e]:
+ *     D[e, r, :] = A[e, r, :] * B[e]^T
+ * Rows r >= v_e are not written; experts with v_e = 0 load nothing.
+ *
+ *   A     [E, M_max, K]    bf16 or E4M3 bytes.
+ *   SFA   uint8 [E, K/128, M_max] (fp8 only; M_max a multiple of 16).
+ *   B, SFB  as for mgemm_contiguous.
+ *   D     [E, M_max, N]    bf16.
+ *   E*M_max must be < 2^31.
+ * Device errors: v_e < 0 or v_e > M_max -> MG_ERR_DEVICE_ARG (expert
+ * skipped).
+ * ------------------------------------------------------------------------ */
+mg_status mgemm_masked(mg_dtype dt, const void* A, const uint8_t* SFA,
+                       const void* B, const uint8_t* SFB, void* D,
+                       const int32_t* d_valid_m, int32_t E, int32_t M_max,
+                       int32_t N, int32_t K, int32_t* d_status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * K-grouped weight-gradient GEMM ("flops/deepgemm-grouped-masked-moe-gemm",
+ * "Workarounds": K-grouped GEMM for MoE weight backward, M and N fixed and
+ * the contraction length varying per expert).
+ *
+ * With tok_e = sum_{e'<e} t_e' (tokens packed by expert, no alignment):
+ *     dW[e] = sum_{t in [tok_e, tok_e + t_e)} dY[t, :]^T X[t, :]   ([N, K])
+ * dW is overwritten; experts with t_e = 0 get dW[e] = 0 with no loads.
+ *
+ *   dY    bf16 [T_cap, N];  X  bf16 [T_cap, K];  dW  fp32 [E, N, K].
+ *   T_cap < 2^31.
+ * Device errors: t_e < 0 -> MG_ERR_DEVICE_ARG; sum t_e > T_cap ->
+ * MG_ERR_CAPACITY; dW[e] of an expert that does not fit is not written.
+ * ------------------------------------------------------------------------ */
+mg_status kgemm_grouped(const void* dY, const void* X, float* dW,
+                        const int32_t* d_counts, int32_t E, int64_t T_cap,
+                        int32_t N, int32_t K, int32_t* d_status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Bounded waits.  Every kernel spin-wait gives up after this many
+ * nanoseconds of wall time measured from the CTA's start (default 2e9),
+ * writing MG_ERR_TIMEOUT.  Process-wide; not thread-safe against concurrent
+ * launches.  ns <= 0 restores the default.
+ * ------------------------------------------------------------------------ */
+mg_status mg_set_wait_limit_ns(int64_t ns);
+int64_t mg_get_wait_limit_ns(void);
+
+/* Self-test of the bounded wait: one CTA waits on a shared-memory barrier
+ * that nothing will ever complete, with a limit of limit_ns, and must write
+ * MG_ERR_TIMEOUT to *d_status and return.  Faults nothing. */
+mg_status mg_wait_selftest(int32_t* d_status, int64_t limit_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOEGEMM_H */

@@ -1,0 +1,203 @@
+"""Thin ctypes binding of libmoegemm.so (C ABI in include/moegemm.h).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels.  Torch tensors supply device memory and the current stream; nothing
+here computes the method, and every call raises if the library is missing or
+returns an error.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+MG_OK = 0
+STATUS_NAMES = {
+    0: "MG_OK", 1: "MG_ERR_INVALID_ARG", 2: "MG_ERR_UNSUPPORTED", 3: "MG_ERR_CUDA",
+    4: "MG_ERR_CAPACITY", 5: "MG_ERR_TIMEOUT", 6: "MG_ERR_DEVICE_ARG",
+}
+MG_BF16, MG_FP8_E4M3_UE8M0 = 0, 1
+
+# Every function the header declares, with its ctypes signature.
+_c_i32p = ctypes.POINTER(ctypes.c_int32)
+_c_i64p = ctypes.POINTER(ctypes.c_int64)
+_vp = ctypes.c_void_p
+_i32 = ctypes.c_int32
+_i64 = ctypes.c_int64
+
+
+class PlanStats(ctypes.Structure):
+    _fields_ = [("P", ctypes.c_int64), ("U", ctypes.c_int64), ("sumsq", ctypes.c_int64),
+                ("active", ctypes.c_int32), ("num_tiles", ctypes.c_int32),
+                ("pad_frac", ctypes.c_double), ("eff_experts", ctypes.c_double)]
+
+
+SIGNATURES = {
+    "mg_status_str": (ctypes.c_char_p, [_i32]),
+    "moe_plan_host": (_i32, [_c_i32p, _i32, _i32, _c_i64p, _c_i32p, _i32, ctypes.POINTER(PlanStats)]),
+    "moe_plan": (_i32, [_vp, _i32, _i32, _vp, _vp, _i32, _vp, _vp, _vp]),
+    "moe_select_tile": (_i32, [_i32, _vp, _i32, _i32, _i32, _vp, _vp, _vp]),
+    "moe_select_tile_host": (_i32, [_i32, _c_i32p, _i32, _i32, _i32, _i32, _c_i32p]),
+    "mgemm_contiguous": (_i32, [_i32, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32, _i32, _vp, _vp]),
+    "mgemm_masked": (_i32, [_i32, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp]),
+    "kgemm_grouped": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _vp, _vp]),
+    "mg_set_wait_limit_ns": (_i32, [_i64]),
+    "mg_get_wait_limit_ns": (_i64, []),
+    "mg_wait_selftest": (_i32, [_vp, _i64, _vp]),
+}
+
+_LIB = None
+
+
+class MoeGemmError(RuntimeError):
+    def __init__(self, fn, code):
+        super().__init__(f"{fn} failed: {STATUS_NAMES.get(code, code)}")
+        self.code = code
+
+
+def load(path: str = None) -> ctypes.CDLL:
+    """Loads the library (once).  Raises if it has not been built."""
+    global _LIB
+    if _LIB is not None and path is None:
+        return _LIB
+    p = path or _build.LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"{p} is missing: build it with __graft_entry__.build()")
+    lib = ctypes.CDLL(p)
+    for name, (res, args) in SIGNATURES.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    if path is None:
+        _LIB = lib
+    return lib
+
+
+def _check(fn, code):
+    if code != MG_OK:
+        raise MoeGemmError(fn, code)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype_of(A):
+    import torch
+    if A.dtype == torch.bfloat16:
+        return MG_BF16
+    if A.dtype in (torch.uint8, torch.float8_e4m3fn):
+        return MG_FP8_E4M3_UE8M0
+    raise TypeError(f"unsupported operand dtype {A.dtype}")
+
+
+def status_str(code: int) -> str:
+    return load().mg_status_str(code).decode()
+
+
+# ------------------------------------------------------------------ host plan
+def plan_host(counts, q: int, max_tiles: int = None):
+    """moe_plan_host: returns (offsets int64 [E+1], tiles int32 [T,3], PlanStats, status)."""
+    lib = load()
+    c = np.ascontiguousarray(np.asarray(counts, dtype=np.int32))
+    E = len(c)
+    offsets = np.zeros(E + 1, dtype=np.int64)
+    if max_tiles is None:
+        max_tiles = int(sum(-(-int(t) // q) for t in c if t > 0)) if q > 0 else 0
+    tiles = np.zeros((max(max_tiles, 1), 3), dtype=np.int32)
+    st = PlanStats()
+    code = lib.moe_plan_host(c.ctypes.data_as(_c_i32p), E, q, offsets.ctypes.data_as(_c_i64p),
+                             tiles.ctypes.data_as(_c_i32p) if max_tiles > 0 else None,
+                             max_tiles, ctypes.byref(st))
+    return offsets, tiles[:max_tiles], st, code
+
+
+def select_tile_host(dtype: int, counts, N: int, K: int, num_sms: int = 0) -> int:
+    lib = load()
+    c = np.ascontiguousarray(np.asarray(counts, dtype=np.int32))
+    out = ctypes.c_int32(0)
+    _check("moe_select_tile_host",
+           lib.moe_select_tile_host(dtype, c.ctypes.data_as(_c_i32p), len(c), N, K, num_sms, ctypes.byref(out)))
+    return out.value
+
+
+# ---------------------------------------------------------------- device calls
+STATS_DTYPE = np.dtype([("P", "<i8"), ("U", "<i8"), ("sumsq", "<i8"), ("active", "<i4"),
+                        ("num_tiles", "<i4"), ("pad_frac", "<f8"), ("eff_experts", "<f8")])
+
+
+def decode_stats(buf) -> dict:
+    """48-byte mg_plan_stats (a uint8 tensor) -> dict."""
+    a = np.frombuffer(buf.cpu().numpy().tobytes(), dtype=STATS_DTYPE)[0]
+    return {k: a[k].item() for k in STATS_DTYPE.names}
+
+
+def plan(d_counts, q: int, max_tiles: int, status=None, stream=None):
+    """moe_plan on device tensors; returns (offsets, tiles, stats_bytes)."""
+    import torch
+    lib = load()
+    dev = d_counts.device
+    E = d_counts.numel()
+    offsets = torch.empty(E + 1, dtype=torch.int64, device=dev)
+    tiles = torch.empty((max(max_tiles, 1), 3), dtype=torch.int32, device=dev)
+    stats = torch.zeros(48, dtype=torch.uint8, device=dev)
+    _check("moe_plan", lib.moe_plan(_ptr(d_counts), E, q, _ptr(offsets),
+                                    _ptr(tiles) if max_tiles > 0 else None, max_tiles,
+                                    _ptr(stats), _ptr(status), _stream(stream)))
+    return offsets, tiles[:max_tiles], stats
+
+
+def select_tile(dtype: int, d_counts, N: int, K: int, status=None, stream=None):
+    import torch
+    lib = load()
+    out = torch.zeros(1, dtype=torch.int32, device=d_counts.device)
+    _check("moe_select_tile", lib.moe_select_tile(dtype, _ptr(d_counts), d_counts.numel(), N, K,
+                                                  _ptr(out), _ptr(status), _stream(stream)))
+    return out
+
+
+def mgemm_contiguous(A, B, D, d_counts, align_q: int, SFA=None, SFB=None, tile_q: int = 0,
+                     status=None, stream=None):
+    lib = load()
+    rows_cap, K = A.shape
+    E, N, _ = B.shape
+    _check("mgemm_contiguous", lib.mgemm_contiguous(
+        _dtype_of(A), _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(D), _ptr(d_counts), E,
+        rows_cap, N, K, align_q, tile_q, _ptr(status), _stream(stream)))
+
+
+def mgemm_masked(A, B, D, d_valid_m, SFA=None, SFB=None, status=None, stream=None):
+    lib = load()
+    E, M_max, K = A.shape
+    N = B.shape[1]
+    _check("mgemm_masked", lib.mgemm_masked(
+        _dtype_of(A), _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(D), _ptr(d_valid_m), E,
+        M_max, N, K, _ptr(status), _stream(stream)))
+
+
+def kgemm_grouped(dY, X, dW, d_counts, status=None, stream=None):
+    lib = load()
+    T_cap, N = dY.shape
+    K = X.shape[1]
+    E = dW.shape[0]
+    _check("kgemm_grouped", lib.kgemm_grouped(_ptr(dY), _ptr(X), _ptr(dW), _ptr(d_counts), E,
+                                              T_cap, N, K, _ptr(status), _stream(stream)))
+
+
+def set_wait_limit_ns(ns: int):
+    load().mg_set_wait_limit_ns(int(ns))
+
+
+def get_wait_limit_ns() -> int:
+    return load().mg_get_wait_limit_ns()
+
+
+def wait_selftest(status, limit_ns: int, stream=None):
+    _check("mg_wait_selftest", load().mg_wait_selftest(_ptr(status), int(limit_ns), _stream(stream)))

@@ -1,0 +1,449 @@
+// Contiguous and masked MoE grouped GEMM for sm_103a (bf16, and E4M3 with
+// UE8M0 per-128 block scales).
+//
+// "flops/deepgemm-grouped-masked-moe-gemm", "Arithmetic intensity" and
+// "Workarounds": N and K are shared by all experts; the contiguous form
+// concatenates each expert's token rows on M-block boundaries, the masked
+// form keeps fixed per-expert buffers and computes only the first valid_m[e]
+// rows.  "MoE GroupGEMM padding under expert skew", "Grouped execution does
+// not require padded experts": a persistent kernel builds its tiles from the
+// actual counts, experts with no tokens produce no tiles (so their weights are
+// never loaded) and tail rows are not written.
+//
+// Tile shape.  Tokens sit on the MMA N axis and 128 weight rows on the MMA M
+// axis, so a tile is 128 output columns x q_n token rows with q_n any
+// multiple of 16 up to 256, chosen per tile at run time: full tiles use the
+// selected token tile q, an expert's last tile is trimmed to round_up(rows,
+// 16).  The instruction descriptor and the TMA box count are runtime values,
+// so a single launch serves every tile size with no host round trip
+// ("Adapt kernels without adding a CPU stall").
+//
+// CTA = 6 warps: warp 0 issues TMA, warp 1 owns TMEM and issues tcgen05.mma
+// (and stages the fp8 block scales into TMEM), warps 2-5 drain the fp32
+// accumulator from TMEM and store bf16 rows.  Operands stream through a
+// shared-memory ring of up to 16 stages; two TMEM accumulators let the
+// epilogue of one tile overlap the main loop of the next.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "mg_internal.h"
+#include "sched.cuh"
+
+namespace mg {
+namespace fwd {
+
+constexpr int kThreads = 192;
+constexpr int kMaxStages = 16;
+constexpr int kWRows = 128;                      // weight rows per tile (MMA M)
+constexpr int kRowBytes = 128;                   // K bytes per stage and row
+constexpr int kWTileBytes = kWRows * kRowBytes;  // 16 KB
+constexpr int kMaxQ = 256;
+constexpr int kSfRaw = 256;                      // token scale bytes per stage
+constexpr int kSfStage = 256 + 512 + 1024;       // raw + weight words + token words
+constexpr int kGroupTiles = 8;                   // token tiles per raster group
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccStride = 256;             // TMEM columns between accumulators
+constexpr uint32_t kSfaCol = 496, kSfbCol = 500;  // fp8 scale columns
+constexpr int kSmemBytes = 227 * 1024;
+constexpr uint64_t kDrainNs = 200ull * 1000 * 1000;
+
+struct Params {
+  const int32_t* counts;
+  const uint8_t* sfb;
+  __nv_bfloat16* D;
+  int32_t* status;
+  int64_t wait_ns;
+  int32_t E, N, K;
+  int32_t masked, fp8;
+  int32_t rows_total, M_max, align_q, tile_q;
+};
+
+struct Shared {
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int32_t abort_flag;
+  int32_t q;         // token tile of full tiles
+  int32_t qn_max;    // widest tile of this launch
+  int32_t total;     // tiles of this launch
+};
+
+struct Tile {
+  int32_t e, nb, row0, rows, qn, sf_x, sf_z;
+};
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64_t deadline,
+                                          volatile int32_t* abort_flag, int32_t* status) {
+  const bool ok = wait_bounded(bar, parity, deadline, abort_flag, status);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Tile t of the launch.  Experts in order; inside an expert, groups of
+// kGroupTiles token tiles sweep all 128-column weight blocks before moving
+// on, so CTAs working at the same time share weight and activation tiles in
+// L2.
+__device__ __forceinline__ Tile decode_tile(int32_t t, const int32_t* tpre, const int32_t* cnt,
+                                            const int32_t* rowbase, int32_t E, int32_t NB,
+                                            int32_t q, int32_t masked) {
+  int32_t lo = 0, hi = E;  // tpre[lo] <= t < tpre[hi]
+  while (hi - lo > 1) {
+    const int32_t mid = (lo + hi) >> 1;
+    if (tpre[mid] <= t) lo = mid; else hi = mid;
+  }
+  Tile tl;
+  tl.e = lo;
+  const int32_t mt = (tpre[lo + 1] - tpre[lo]) / NB;
+  const int32_t l = t - tpre[lo];
+  const int32_t g = l / (kGroupTiles * NB);
+  const int32_t gbase = g * kGroupTiles;
+  const int32_t gsz = min(kGroupTiles, mt - gbase);
+  const int32_t r = l - g * kGroupTiles * NB;
+  tl.nb = r / gsz;
+  const int32_t j = gbase + r % gsz;
+  const int32_t in_e = j * q;
+  tl.rows = min(q, cnt[lo] - in_e);
+  tl.qn = round_up16(tl.rows);
+  tl.row0 = rowbase[lo] + in_e;
+  tl.sf_x = masked ? in_e : tl.row0;
+  tl.sf_z = masked ? lo : 0;
+  return tl;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA64,
+               const __grid_constant__ CUtensorMap tmA16, const __grid_constant__ CUtensorMap tmSF,
+               const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  Shared& sh = *reinterpret_cast<Shared*>(smem);
+  const int32_t E = p.E;
+  int32_t* cnt = reinterpret_cast<int32_t*>(smem + ((sizeof(Shared) + 15) & ~size_t(15)));
+  int32_t* rowbase = cnt + E;
+  int32_t* tpre = rowbase + E;
+  const uintptr_t sched_end = reinterpret_cast<uintptr_t>(tpre + E + 1);
+  uint8_t* sf_area = reinterpret_cast<uint8_t*>((sched_end + 1023) & ~uintptr_t(1023));
+
+  const uint32_t warp = warp_id(), lane = lane_id();
+  const uint64_t deadline = globaltimer_ns() + (uint64_t)p.wait_ns;
+  const int32_t NB = p.N / kWRows;
+  const int32_t KB = p.K / (p.fp8 ? 128 : 64);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kMaxStages; ++i) {
+      mbar_init(&sh.full[i], 1);
+      mbar_init(&sh.empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sh.acc_full[i], 1);
+      mbar_init(&sh.acc_empty[i], 4 * 32);
+    }
+    mbar_init(&sh.drain, 1);
+    sh.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(&sh.tmem_base, kTmemCols);
+
+  // ---- validated counts
+  for (int32_t e = threadIdx.x; e < E; e += kThreads) {
+    int32_t c = __ldg(p.counts + e);
+    if (c < 0 || (p.masked && c > p.M_max)) {
+      set_status(p.status, MG_ERR_DEVICE_ARG);
+      c = 0;
+    }
+    cnt[e] = c;
+  }
+  __syncthreads();
+
+  // ---- schedule (warp 0): row bases, token tile, tile prefix
+  if (warp == 0) {
+    // row base of each expert
+    if (p.masked) {
+      for (int32_t e = lane; e < E; e += 32) rowbase[e] = e * p.M_max;
+    } else {
+      int64_t carry = 0;
+      for (int32_t b = 0; b < E; b += 32) {
+        const int32_t e = b + lane;
+        const int64_t own = e < E ? (int64_t)p.align_q * cdiv64(cnt[e], p.align_q) : 0;
+        int64_t v = own;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int64_t n = __shfl_up_sync(0xffffffffu, v, o);
+          if ((int)lane >= o) v += n;
+        }
+        if (e < E) {
+          const int64_t start = carry + v - own;
+          if (start + cnt[e] > p.rows_total) {
+            cnt[e] = 0;  // segment does not fit: skip the expert
+            rowbase[e] = 0;
+          } else {
+            rowbase[e] = (int32_t)start;
+          }
+        }
+        carry += __shfl_sync(0xffffffffu, v, 31);
+      }
+      if (lane == 0 && carry > p.rows_total) set_status(p.status, MG_ERR_CAPACITY);
+    }
+    __syncwarp();
+    // token tile
+    int32_t q = p.tile_q;
+    if (p.masked) {
+      q = kMaxQ;
+    } else if (q == 0) {
+      int64_t tiles[kNumTileCand];
+#pragma unroll
+      for (int i = 0; i < kNumTileCand; ++i) {
+        int64_t s = 0;
+        for (int32_t e = lane; e < E; e += 32) s += cdiv64(cnt[e], tile_candidate(p.fp8, i));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        tiles[i] = s;
+      }
+      q = pick_tile(p.fp8 != 0, tiles, NB, sel_kblocks(p.fp8 != 0, p.K), (int)gridDim.x);
+    }
+    // tile prefix (NB weight blocks per token tile) and the widest tile
+    int32_t carry = 0, qmax = 0;
+    for (int32_t b = 0; b < E; b += 32) {
+      const int32_t e = b + lane;
+      const int32_t c = e < E ? cnt[e] : 0;
+      const int32_t own = (int32_t)cdiv64(c, q) * NB;
+      if (c > 0) qmax = max(qmax, min(q, round_up16(c)));
+      int32_t v = own;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int32_t n = __shfl_up_sync(0xffffffffu, v, o);
+        if ((int)lane >= o) v += n;
+      }
+      if (e < E) tpre[e] = carry + v - own;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) qmax = max(qmax, __shfl_xor_sync(0xffffffffu, qmax, o));
+    if (lane == 0) {
+      tpre[E] = carry;
+      sh.total = carry;
+      sh.q = q;
+      sh.qn_max = max(qmax, 16);
+    }
+  }
+  __syncthreads();
+  tc_fence_after();
+
+  // ---- ring layout, identical in every CTA
+  const int32_t q = sh.q;
+  const int32_t total = sh.total;
+  const int32_t stage_bytes = kWTileBytes + sh.qn_max * kRowBytes;
+  const int32_t sf_bytes = p.fp8 ? kSfStage : 0;
+  const int32_t avail = kSmemBytes - 1024 - (int32_t)(reinterpret_cast<uintptr_t>(sf_area) -
+                                                     reinterpret_cast<uintptr_t>(smem)) - 1024;
+  int32_t S = avail / (stage_bytes + sf_bytes);
+  S = min(S, kMaxStages);
+  uint8_t* ring = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(sf_area) + (uintptr_t)S * sf_bytes + 1023) & ~uintptr_t(1023));
+  const uint32_t n_acc = (!p.fp8 || sh.qn_max <= 240) ? 2u : 1u;
+  const uint32_t tmem = sh.tmem_base;
+
+  if (warp == 0) {
+    // ================================================= TMA producer
+    if (lane == 0 && S > 0) {
+      tma_prefetch_desc(&tmW);
+      tma_prefetch_desc(&tmA64);
+      tma_prefetch_desc(&tmA16);
+      if (p.fp8) tma_prefetch_desc(&tmSF);
+      uint32_t stage = 0, phase = 0;
+      int64_t issued = 0;
+      bool ok = true;
+      for (int32_t t = blockIdx.x; ok && t < total; t += gridDim.x) {
+        const Tile tl = decode_tile(t, tpre, cnt, rowbase, E, NB, q, p.masked);
+        const int32_t wy = tl.e * p.N + tl.nb * kWRows;
+        const uint32_t bytes = kWTileBytes + tl.qn * kRowBytes + (p.fp8 ? kSfRaw : 0);
+        for (int32_t kb = 0; kb < KB; ++kb) {
+          if (!wait_bounded(&sh.empty[stage], phase ^ 1u, deadline, &sh.abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sw = ring + (size_t)stage * stage_bytes;
+          uint8_t* sa = sw + kWTileBytes;
+          mbar_arrive_expect_tx(&sh.full[stage], bytes);
+          const int32_t kx = kb * (p.fp8 ? 128 : 64);
+          tma_load_2d(sw, &tmW, &sh.full[stage], kx, wy);
+          for (int32_t r = 0; r < tl.qn;) {
+            if (tl.qn - r >= 64) {
+              tma_load_2d(sa + r * kRowBytes, &tmA64, &sh.full[stage], kx, tl.row0 + r);
+              r += 64;
+            } else {
+              tma_load_2d(sa + r * kRowBytes, &tmA16, &sh.full[stage], kx, tl.row0 + r);
+              r += 16;
+            }
+          }
+          if (p.fp8) tma_load_3d(sf_area + (size_t)stage * kSfStage, &tmSF, &sh.full[stage], tl.sf_x, kb, tl.sf_z);
+          ++issued;
+          if (++stage == (uint32_t)S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // every issued copy lands before the CTA can exit
+      const uint64_t dl = globaltimer_ns() + kDrainNs;
+      for (int64_t i = issued > S ? issued - S : 0; i < issued; ++i)
+        wait_drain(&sh.full[i % S], (uint32_t)((i / S) & 1), dl);
+    }
+  } else if (warp == 1) {
+    // ================================================= MMA issuer
+    if (S > 0) {
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      for (int32_t t = blockIdx.x; ok && t < total; t += gridDim.x) {
+        const Tile tl = decode_tile(t, tpre, cnt, rowbase, E, NB, q, p.masked);
+        uint32_t wsf[4] = {127u, 127u, 127u, 127u};
+        if (p.fp8) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int32_t kb = (int32_t)lane + 32 * i;
+            if (kb < KB) wsf[i] = __ldg(p.sfb + ((int64_t)tl.e * KB + kb) * NB + tl.nb);
+          }
+        }
+        if (!warp_wait(&sh.acc_empty[acc], acc_phase ^ 1u, deadline, &sh.abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + acc * kAccStride;
+        const uint32_t idesc = p.fp8 ? idesc_mxf8(kWRows, tl.qn) : idesc_bf16(kWRows, tl.qn, 0, 0);
+        for (int32_t kb = 0; kb < KB; ++kb) {
+          if (!warp_wait(&sh.full[stage], phase, deadline, &sh.abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          uint8_t* sw = ring + (size_t)stage * stage_bytes;
+          uint8_t* sa = sw + kWTileBytes;
+          uint8_t* sfs = sf_area + (size_t)stage * kSfStage;
+          if (p.fp8) {
+            // TMEM scale words: lane l, column c holds the scale of row
+            // c*32 + l; every byte of a word carries the same UE8M0 value.
+            const uint32_t wb = __shfl_sync(0xffffffffu, wsf[kb >> 5], kb & 31) & 0xFFu;
+            const uint32_t ww = wb * 0x01010101u;
+            *reinterpret_cast<uint4*>(sfs + kSfRaw + lane * 16) = make_uint4(ww, ww, ww, ww);
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+              uint32_t v[4];
+#pragma unroll
+              for (int c = 0; c < 4; ++c) v[c] = (uint32_t)sfs[g * 128 + c * 32 + lane] * 0x01010101u;
+              *reinterpret_cast<uint4*>(sfs + kSfRaw + 512 + g * 512 + lane * 16) =
+                  make_uint4(v[0], v[1], v[2], v[3]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
+          if (lane == 0) {
+            if (p.fp8) {
+              tmem_cp_32x128b_x4(tmem + kSfaCol, desc_sf_32x16(smem_u32(sfs + kSfRaw)));
+              tmem_cp_32x128b_x4(tmem + kSfbCol, desc_sf_32x16(smem_u32(sfs + kSfRaw + 512)));
+              if (tl.qn > 128)
+                tmem_cp_32x128b_x4(tmem + kSfbCol + 4, desc_sf_32x16(smem_u32(sfs + kSfRaw + 1024)));
+            }
+            const uint32_t a0 = smem_u32(sw), b0 = smem_u32(sa);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+              const uint64_t ad = desc_kmajor_sw128(a0 + ks * 32);
+              const uint64_t bd = desc_kmajor_sw128(b0 + ks * 32);
+              const uint32_t accum = (kb | ks) != 0 ? 1u : 0u;
+              if (p.fp8)
+                mma_mxf8(d_tmem, ad, bd, idesc, tmem + kSfaCol, tmem + kSfbCol, accum);
+              else
+                mma_f16(d_tmem, ad, bd, idesc, accum);
+            }
+            mma_commit(&sh.empty[stage]);
+          }
+          __syncwarp();
+          if (++stage == (uint32_t)S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        if (lane == 0) mma_commit(&sh.acc_full[acc]);
+        __syncwarp();
+        if (++acc == n_acc) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+    }
+    // all tcgen05 work of this CTA completes before TMEM is released
+    if (lane == 0) {
+      mma_commit(&sh.drain);
+      wait_drain(&sh.drain, 0, globaltimer_ns() + kDrainNs);
+    }
+    __syncwarp();
+  } else {
+    // ================================================= epilogue
+    const uint32_t quad = warp & 3u;  // TMEM lanes this warp may access
+    uint32_t acc = 0, acc_phase = 0;
+    for (int32_t t = blockIdx.x; S > 0 && t < total; t += gridDim.x) {
+      const Tile tl = decode_tile(t, tpre, cnt, rowbase, E, NB, q, p.masked);
+      if (!warp_wait(&sh.acc_full[acc], acc_phase, deadline, &sh.abort_flag, p.status)) break;
+      tc_fence_after();
+      const int32_t n = tl.nb * kWRows + (int32_t)(quad * 32 + lane);
+      const uint32_t taddr = tmem + ((quad * 32u) << 16) + acc * kAccStride;
+      __nv_bfloat16* dcol = p.D + (int64_t)tl.row0 * p.N + n;
+      for (int32_t c0 = 0; c0 < tl.qn; c0 += 16) {
+        uint32_t r[16];
+        tmem_ld16(taddr + (uint32_t)c0, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (c0 + i < tl.rows) dcol[(int64_t)(c0 + i) * p.N] = __float2bfloat16_rn(__uint_as_float(r[i]));
+      }
+      tc_fence_before();
+      mbar_arrive(&sh.acc_empty[acc]);
+      if (++acc == n_acc) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace fwd
+
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s) {
+  static bool attr_done[64] = {};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 64 && !attr_done[dev]) {
+    err = cudaFuncSetAttribute(fwd::fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               fwd::kSmemBytes);
+    if (err != cudaSuccess) return err;
+    attr_done[dev] = true;
+  }
+  fwd::Params p;
+  p.counts = a.counts;
+  p.sfb = a.sfb;
+  p.D = static_cast<__nv_bfloat16*>(a.D);
+  p.status = a.status;
+  p.wait_ns = a.wait_ns;
+  p.E = a.E;
+  p.N = a.N;
+  p.K = a.K;
+  p.masked = a.masked ? 1 : 0;
+  p.fp8 = a.fp8 ? 1 : 0;
+  p.rows_total = a.rows_total;
+  p.M_max = a.M_max;
+  p.align_q = a.align_q;
+  p.tile_q = a.tile_q;
+  const int grid = num_sms_current_device();
+  fwd::fwd_kernel<<<grid, fwd::kThreads, fwd::kSmemBytes, s>>>(a.tmW, a.tmA64, a.tmA16, a.tmSF, p);
+  return cudaGetLastError();
+}
+
+}  // namespace mg

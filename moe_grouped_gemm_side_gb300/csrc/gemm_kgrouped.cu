@@ -1,0 +1,368 @@
+// K-grouped MoE weight-gradient GEMM for sm_103a ("flops/deepgemm-grouped-
+// masked-moe-gemm", "Workarounds": K-grouped GEMM for MoE weight backward, M
+// and N fixed while the contraction length -- the expert's token count --
+// varies).
+//
+//   dW[e] = sum over expert e's tokens t of dY[t, :]^T X[t, :]    ([N, K], fp32)
+//
+// Tokens are packed by expert with no alignment, so both operands arrive
+// MN-major: a TMA box is 64 tokens x 64 contiguous columns of dY or X, and
+// the MMA reads them through transposed (MN-major) descriptors.  A tile is a
+// 128 x 256 block of dW; its main loop walks the expert's tokens 64 at a
+// time.  The last, partial block of an expert may hold the next expert's
+// tokens: the MMA warp zeroes those rows of the staged operands in shared
+// memory and issues only the 16-token MMA steps that still hold valid tokens.
+//
+// Tiles of all experts are ordered by descending token count and dealt to
+// the persistent CTAs in a snake order, so every CTA receives a similar mix
+// of long and short tiles.  Experts with no tokens produce zero tiles that
+// the epilogue writes without any load or MMA.
+#include "common.cuh"
+#include "mg_internal.h"
+#include "sched.cuh"
+
+namespace mg {
+namespace kg {
+
+constexpr int kThreads = 192;
+constexpr int kMaxStages = 6;
+constexpr int kBlockT = 64;          // tokens per stage
+constexpr int kBoxBytes = kBlockT * 128;  // one 64 x 64 bf16 box
+constexpr int kTileM = 128;          // dW rows per tile
+constexpr int kTileN = 256;          // dW columns per tile (max)
+constexpr int kStageBytes = (kTileM / 64 + kTileN / 64) * kBoxBytes;  // 48 KB
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccStride = 256;
+constexpr int kSmemBytes = 227 * 1024;
+constexpr uint64_t kDrainNs = 200ull * 1000 * 1000;
+
+struct Params {
+  const int32_t* counts;
+  float* dW;
+  int32_t* status;
+  int64_t wait_ns;
+  int32_t E, N, K, T_cap;
+};
+
+struct Shared {
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int32_t abort_flag;
+  int32_t n_valid;
+};
+
+struct Tile {
+  int32_t e, mb, nb, w, cnt, tok0;
+};
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64_t deadline,
+                                          volatile int32_t* abort_flag, int32_t* status) {
+  const bool ok = wait_bounded(bar, parity, deadline, abort_flag, status);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Position `pos` of the CTA's snake walk -> tile.
+__device__ __forceinline__ Tile decode_tile(int32_t pos, const int32_t* order, const int32_t* cnt,
+                                            const int32_t* tokoff, int32_t NBk, int32_t NT,
+                                            int32_t K) {
+  Tile tl;
+  const int32_t pe = pos / NT, l = pos - pe * NT;
+  tl.e = order[pe];
+  tl.mb = l / NBk;
+  tl.nb = l - tl.mb * NBk;
+  tl.w = min(kTileN, K - tl.nb * kTileN);
+  tl.cnt = cnt[tl.e];
+  tl.tok0 = tokoff[tl.e];
+  return tl;
+}
+
+// Position of the CTA's r-th tile: rounds of gridDim.x tiles, alternating
+// direction.  Returns -1 past the end of the list.
+__device__ __forceinline__ int32_t snake_pos(int32_t r, int32_t total) {
+  const int64_t base = (int64_t)r * gridDim.x;
+  if (base >= total) return -1;
+  const int64_t pos = base + ((r & 1) ? (int64_t)(gridDim.x - 1 - blockIdx.x) : (int64_t)blockIdx.x);
+  return pos < total ? (int32_t)pos : -2;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    kg_kernel(const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmX,
+              const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  Shared& sh = *reinterpret_cast<Shared*>(smem);
+  const int32_t E = p.E;
+  int32_t* cnt = reinterpret_cast<int32_t*>(smem + ((sizeof(Shared) + 15) & ~size_t(15)));
+  int32_t* tokoff = cnt + E;
+  int32_t* order = tokoff + E;
+  uint8_t* ring = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(order + E) + 1023) & ~uintptr_t(1023));
+
+  const uint32_t warp = warp_id(), lane = lane_id();
+  const uint64_t deadline = globaltimer_ns() + (uint64_t)p.wait_ns;
+  const int32_t NBk = (p.K + kTileN - 1) / kTileN;
+  const int32_t NT = (p.N / kTileM) * NBk;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kMaxStages; ++i) {
+      mbar_init(&sh.full[i], 1);
+      mbar_init(&sh.empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sh.acc_full[i], 1);
+      mbar_init(&sh.acc_empty[i], 4 * 32);
+    }
+    mbar_init(&sh.drain, 1);
+    sh.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(&sh.tmem_base, kTmemCols);
+
+  // ---- counts (-1 marks an expert that is skipped)
+  for (int32_t e = threadIdx.x; e < E; e += kThreads) {
+    int32_t c = __ldg(p.counts + e);
+    if (c < 0) {
+      set_status(p.status, MG_ERR_DEVICE_ARG);
+      c = -1;
+    }
+    cnt[e] = c;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int64_t carry = 0;
+    for (int32_t b = 0; b < E; b += 32) {
+      const int32_t e = b + lane;
+      const int64_t own = (e < E && cnt[e] > 0) ? cnt[e] : 0;
+      int64_t v = own;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int64_t n = __shfl_up_sync(0xffffffffu, v, o);
+        if ((int)lane >= o) v += n;
+      }
+      if (e < E) {
+        const int64_t start = carry + v - own;
+        if (start + own > p.T_cap) {
+          set_status(p.status, MG_ERR_CAPACITY);
+          cnt[e] = -1;
+          tokoff[e] = 0;
+        } else {
+          tokoff[e] = (int32_t)start;
+        }
+      }
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+  }
+  __syncthreads();
+  // ---- experts by descending count (ties: lower index first), skipped last
+  for (int32_t e = threadIdx.x; e < E; e += kThreads) {
+    const int32_t c = cnt[e];
+    if (c < 0) continue;
+    int32_t rank = 0;
+    for (int32_t f = 0; f < E; ++f) {
+      const int32_t d = cnt[f];
+      rank += (d > c) || (d == c && f < e);
+    }
+    order[rank] = e;
+  }
+  if (threadIdx.x == 0) {
+    int32_t nv = 0;
+    for (int32_t e = 0; e < E; ++e) nv += cnt[e] >= 0;
+    sh.n_valid = nv;
+  }
+  __syncthreads();
+  tc_fence_after();
+
+  const int32_t total = sh.n_valid * NT;
+  const int32_t avail = kSmemBytes - 1024 - (int32_t)(reinterpret_cast<uintptr_t>(ring) -
+                                                     reinterpret_cast<uintptr_t>(smem));
+  const int32_t S = min(kMaxStages, avail / kStageBytes);
+  const uint32_t tmem = sh.tmem_base;
+
+  if (warp == 0) {
+    // ================================================= TMA producer
+    if (lane == 0 && S > 0) {
+      tma_prefetch_desc(&tmY);
+      tma_prefetch_desc(&tmX);
+      uint32_t stage = 0, phase = 0;
+      int64_t issued = 0;
+      bool ok = true;
+      for (int32_t r = 0; ok; ++r) {
+        const int32_t pos = snake_pos(r, total);
+        if (pos == -1) break;
+        if (pos < 0) continue;
+        const Tile tl = decode_tile(pos, order, cnt, tokoff, NBk, NT, p.K);
+        if (tl.cnt == 0) continue;
+        const int32_t nkb = (tl.cnt + kBlockT - 1) / kBlockT;
+        const uint32_t bytes = (uint32_t)(2 + tl.w / 64) * kBoxBytes;
+        for (int32_t kb = 0; kb < nkb; ++kb) {
+          if (!wait_bounded(&sh.empty[stage], phase ^ 1u, deadline, &sh.abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = ring + (size_t)stage * kStageBytes;
+          uint8_t* sb = sa + 2 * kBoxBytes;
+          mbar_arrive_expect_tx(&sh.full[stage], bytes);
+          const int32_t y = tl.tok0 + kb * kBlockT;
+#pragma unroll
+          for (int i = 0; i < 2; ++i)
+            tma_load_2d(sa + i * kBoxBytes, &tmY, &sh.full[stage], tl.mb * kTileM + i * 64, y);
+          for (int i = 0; i < tl.w / 64; ++i)
+            tma_load_2d(sb + i * kBoxBytes, &tmX, &sh.full[stage], tl.nb * kTileN + i * 64, y);
+          ++issued;
+          if (++stage == (uint32_t)S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      const uint64_t dl = globaltimer_ns() + kDrainNs;
+      for (int64_t i = issued > S ? issued - S : 0; i < issued; ++i)
+        wait_drain(&sh.full[i % S], (uint32_t)((i / S) & 1), dl);
+    }
+  } else if (warp == 1) {
+    // ================================================= MMA issuer
+    if (S > 0) {
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      for (int32_t r = 0; ok; ++r) {
+        const int32_t pos = snake_pos(r, total);
+        if (pos == -1) break;
+        if (pos < 0) continue;
+        const Tile tl = decode_tile(pos, order, cnt, tokoff, NBk, NT, p.K);
+        if (tl.cnt == 0) continue;
+        const int32_t nkb = (tl.cnt + kBlockT - 1) / kBlockT;
+        if (!warp_wait(&sh.acc_empty[acc], acc_phase ^ 1u, deadline, &sh.abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + acc * kAccStride;
+        const uint32_t idesc = idesc_bf16(kTileM, (uint32_t)tl.w, 1, 1);
+        const int32_t nbox = 2 + tl.w / 64;
+        for (int32_t kb = 0; kb < nkb; ++kb) {
+          if (!warp_wait(&sh.full[stage], phase, deadline, &sh.abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          uint8_t* sa = ring + (size_t)stage * kStageBytes;
+          uint8_t* sb = sa + 2 * kBoxBytes;
+          const int32_t rem = tl.cnt - kb * kBlockT;
+          int32_t nks = 4;
+          if (rem < kBlockT) {
+            nks = (rem + 15) >> 4;
+            const int32_t z0 = rem, z1 = nks * 16;  // rows [z0, z1) belong to no token of e
+            if (z1 > z0) {
+              const int32_t per_box = (z1 - z0) * 8;  // 16-byte chunks
+              for (int32_t i = lane; i < per_box * nbox; i += 32) {
+                const int32_t box = i / per_box, c = i - box * per_box;
+                *reinterpret_cast<uint4*>(sa + box * kBoxBytes + z0 * 128 + c * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
+              }
+              fence_proxy_async_smem();
+            }
+            __syncwarp();
+          }
+          if (lane == 0) {
+            const uint32_t a0 = smem_u32(sa), b0 = smem_u32(sb);
+            for (int ks = 0; ks < nks; ++ks) {
+              const uint64_t ad = desc_mnmajor_sw128(a0 + ks * 2048, kBoxBytes);
+              const uint64_t bd = desc_mnmajor_sw128(b0 + ks * 2048, kBoxBytes);
+              mma_f16(d_tmem, ad, bd, idesc, (kb | ks) != 0 ? 1u : 0u);
+            }
+            mma_commit(&sh.empty[stage]);
+          }
+          __syncwarp();
+          if (++stage == (uint32_t)S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        if (lane == 0) mma_commit(&sh.acc_full[acc]);
+        __syncwarp();
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+    }
+    if (lane == 0) {
+      mma_commit(&sh.drain);
+      wait_drain(&sh.drain, 0, globaltimer_ns() + kDrainNs);
+    }
+    __syncwarp();
+  } else {
+    // ================================================= epilogue
+    const uint32_t quad = warp & 3u;
+    uint32_t acc = 0, acc_phase = 0;
+    for (int32_t r = 0; S > 0; ++r) {
+      const int32_t pos = snake_pos(r, total);
+      if (pos == -1) break;
+      if (pos < 0) continue;
+      const Tile tl = decode_tile(pos, order, cnt, tokoff, NBk, NT, p.K);
+      const int32_t row = tl.mb * kTileM + (int32_t)(quad * 32 + lane);
+      float* dst = p.dW + ((int64_t)tl.e * p.N + row) * p.K + tl.nb * kTileN;
+      if (tl.cnt == 0) {
+        for (int32_t c = 0; c < tl.w; c += 4)
+          *reinterpret_cast<float4*>(dst + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+        continue;
+      }
+      if (!warp_wait(&sh.acc_full[acc], acc_phase, deadline, &sh.abort_flag, p.status)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem + ((quad * 32u) << 16) + acc * kAccStride;
+      for (int32_t c0 = 0; c0 < tl.w; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(taddr + (uint32_t)c0, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; i += 4)
+          *reinterpret_cast<float4*>(dst + c0 + i) =
+              make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+                          __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+      }
+      tc_fence_before();
+      mbar_arrive(&sh.acc_empty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace kg
+
+cudaError_t launch_kgrouped(const KgArgs& a, cudaStream_t s) {
+  static bool attr_done[64] = {};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 64 && !attr_done[dev]) {
+    err = cudaFuncSetAttribute(kg::kg_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kg::kSmemBytes);
+    if (err != cudaSuccess) return err;
+    attr_done[dev] = true;
+  }
+  kg::Params p;
+  p.counts = a.counts;
+  p.dW = a.dW;
+  p.status = a.status;
+  p.wait_ns = a.wait_ns;
+  p.E = a.E;
+  p.N = a.N;
+  p.K = a.K;
+  p.T_cap = a.T_cap;
+  kg::kg_kernel<<<num_sms_current_device(), kg::kThreads, kg::kSmemBytes, s>>>(a.tmY, a.tmX, p);
+  return cudaGetLastError();
+}
+
+}  // namespace mg

@@ -1,0 +1,54 @@
+// Internal host-side interface between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "moegemm.h"
+
+namespace mg {
+
+// Contiguous and masked forms share one kernel: both place an expert's
+// token rows at a known row base of a 2-D [rows_total, K] activation view and
+// compute only its first t_e rows.
+struct FwdArgs {
+  bool fp8 = false;
+  bool masked = false;
+  const int32_t* counts = nullptr;  // t_e (contiguous) or valid_m (masked)
+  int32_t E = 0, N = 0, K = 0;
+  int32_t rows_total = 0;           // contiguous: rows_cap; masked: E*M_max
+  int32_t M_max = 0;                // masked only
+  int32_t align_q = 1;              // contiguous only
+  int32_t tile_q = 0;               // 0: choose on the device
+  const uint8_t* sfb = nullptr;     // fp8 weight scales [E, K/128, N/128]
+  void* D = nullptr;
+  int32_t* status = nullptr;
+  int64_t wait_ns = 0;
+  CUtensorMap tmW{}, tmA64{}, tmA16{}, tmSF{};
+};
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s);
+
+struct KgArgs {
+  const int32_t* counts = nullptr;
+  int32_t E = 0, N = 0, K = 0;
+  int32_t T_cap = 0;
+  float* dW = nullptr;
+  int32_t* status = nullptr;
+  int64_t wait_ns = 0;
+  CUtensorMap tmY{}, tmX{};
+};
+cudaError_t launch_kgrouped(const KgArgs& a, cudaStream_t s);
+
+cudaError_t launch_plan(const int32_t* counts, int32_t E, int32_t q, int64_t* offsets,
+                        int32_t* tiles, int32_t max_tiles, mg_plan_stats* stats,
+                        int32_t* status, cudaStream_t s);
+cudaError_t launch_select(bool fp8, const int32_t* counts, int32_t E, int32_t N, int32_t K,
+                          int32_t* tile_q, int32_t* status, cudaStream_t s);
+cudaError_t launch_wait_selftest(int32_t* status, int64_t limit_ns, cudaStream_t s);
+
+int num_sms_current_device();
+
+constexpr int kMaxExperts = 1024;
+
+}  // namespace mg

@@ -1,0 +1,173 @@
+"""C ABI checks that need no GPU: the library loads, exports every function
+the header declares, the host planner matches the oracle bit for bit, and
+bad arguments come back as error codes before anything is launched."""
+import ctypes
+import os
+import random
+import re
+
+import numpy as np
+import pytest
+
+from moe_grouped_gemm_side_gb300 import binding as mb
+from oracle import plan as op
+from tests.conftest import ROOT
+
+pytestmark = pytest.mark.cpu
+
+HEADER = os.path.join(ROOT, "include", "moegemm.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z_][a-z0-9_]*)\s*\(", src, re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for f in ("moe_plan", "moe_plan_host", "mgemm_contiguous", "mgemm_masked", "kgemm_grouped",
+              "moe_select_tile", "mg_status_str"):
+        assert f in names
+    assert set(names) == set(mb.SIGNATURES), "binding and header disagree"
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code, name in mb.STATUS_NAMES.items():
+        assert mb.status_str(code) == name
+    assert mb.status_str(99) == "MG_ERR_UNKNOWN"
+
+
+def _check_plan(counts, q):
+    offs, tiles, st, code = mb.plan_host(counts, q)
+    ref = op.plan(counts, q)
+    assert code == 0
+    assert offs.tolist() == ref.offsets
+    assert [tuple(t) for t in tiles.tolist()] == ref.tiles
+    assert (st.P, st.U, st.sumsq, st.active, st.num_tiles) == (ref.P, ref.U, ref.sumsq, ref.active, ref.num_tiles)
+    # the two ratios are bit-identical doubles
+    assert st.pad_frac.hex() == ref.pad_frac.hex()
+    assert st.eff_experts.hex() == ref.eff_experts.hex()
+
+
+def test_host_plan_worked_examples(lib):
+    for counts in ([17, 17, 17, 17, 16, 16, 16, 16], [100, 32, 0, 0, 0, 0, 0, 0]):
+        for q in (8, 16, 32):
+            _check_plan(counts, q)
+
+
+def test_host_plan_random_bit_exact(lib):
+    rng = random.Random(21)
+    for _ in range(3000):
+        E = rng.randint(1, 70)
+        zero = rng.random()
+        c = [0 if rng.random() < zero else rng.randint(1, rng.choice([3, 40, 500, 20000])) for _ in range(E)]
+        _check_plan(c, rng.choice([1, 2, 5, 8, 16, 32, 64, 128, 256]))
+
+
+def test_host_plan_edges(lib):
+    _check_plan([0], 8)
+    _check_plan([0] * 300, 128)
+    _check_plan([1], 1)
+    _check_plan(list(range(1024)), 7)
+    # P beyond int32: offsets and stats stay exact, the int32 tile list is refused
+    huge = [2 ** 31 - 1, 2 ** 31 - 1]
+    offs, tiles, st, code = mb.plan_host(huge, 1 << 20)
+    ref = op.plan(huge, 1 << 20)
+    assert code == 2 and offs.tolist() == ref.offsets and st.P == ref.P
+    assert st.eff_experts.hex() == ref.eff_experts.hex()
+    fits = [t for t in ref.tiles if t[1] <= 2 ** 31 - 1]
+    assert [tuple(t) for t in tiles.tolist()][:len(fits)] == fits
+    offs, _, st, code = mb.plan_host(huge, 1 << 20, max_tiles=0)
+    assert code == 0 and offs.tolist() == ref.offsets
+    _check_plan(list(range(1024)), 7)
+
+
+def test_host_plan_capacity_and_errors(lib):
+    offs, tiles, st, code = mb.plan_host([17] * 8, 8, max_tiles=5)
+    assert code == 4 and st.P == 192 and st.num_tiles == 24 and offs[-1] == 192
+    assert [tuple(t) for t in tiles.tolist()] == op.plan([17] * 8, 8).tiles[:5]
+    _, _, _, code = mb.plan_host([3, -1], 8)
+    assert code == 1
+    _, _, _, code = mb.plan_host([3], 0)
+    assert code == 1
+    st = mb.PlanStats()
+    off = np.zeros(2, np.int64)
+    assert lib.moe_plan_host(None, 1, 8, off.ctypes.data_as(mb._c_i64p), None, 0, ctypes.byref(st)) == 1
+
+
+def test_select_tile_host(lib):
+    # many tokens per expert: the largest tile; bf16 and fp8 candidates differ
+    big = [4096] * 64
+    assert mb.select_tile_host(mb.MG_BF16, big, 4096, 7168) == 256
+    assert mb.select_tile_host(mb.MG_FP8_E4M3_UE8M0, big, 4096, 7168) == 240
+    for seed in range(50):
+        c = [random.Random(seed).randint(0, 300) for _ in range(32)]
+        q = mb.select_tile_host(mb.MG_BF16, c, 4096, 2048)
+        assert q in (32, 64, 128, 256)
+    assert mb.select_tile_host(mb.MG_BF16, [0] * 8, 256, 256) == 256
+
+
+FAKE = ctypes.c_void_p(1 << 20)       # aligned, never dereferenced
+MISALIGNED = ctypes.c_void_p((1 << 20) + 8)
+
+
+def test_device_calls_reject_bad_arguments_before_launch(lib):
+    L = lib
+    # contiguous
+    args = [mb.MG_BF16, FAKE, None, FAKE, None, FAKE, FAKE, 8, 1024, 256, 256, 16, 0, None, None]
+
+    def contig(kw):
+        a = list(args)
+        for k, v in kw.items():
+            a[k] = v
+        return L.mgemm_contiguous(*a)
+    assert contig({1: None}) == 1            # A NULL
+    assert contig({0: 7}) == 1               # bad dtype
+    assert contig({7: 0}) == 1               # E <= 0
+    assert contig({9: 200}) == 2             # N not a multiple of 128
+    assert contig({10: 192}) == 2            # K not a multiple of 128
+    assert contig({11: 0}) == 1              # align_q
+    assert contig({12: 24}) == 1             # tile_q not a multiple of 16
+    assert contig({12: 512}) == 1            # tile_q too large
+    assert contig({8: 0}) == 1               # rows_cap
+    assert contig({1: MISALIGNED}) == 1      # alignment
+    assert contig({7: 5000}) == 2            # too many experts
+    assert contig({0: 1}) == 1               # fp8 without scales
+    assert contig({0: 1, 2: FAKE, 4: FAKE, 11: 8}) == 2     # fp8 align_q % 16
+    assert contig({0: 1, 2: FAKE, 4: FAKE, 12: 248}) == 1   # fp8 tile 248
+    # masked
+    m = [mb.MG_BF16, FAKE, None, FAKE, None, FAKE, FAKE, 8, 256, 256, 256, None, None]
+    assert L.mgemm_masked(*[None if i == 6 else v for i, v in enumerate(m)]) == 1
+    assert L.mgemm_masked(*[0 if i == 8 else v for i, v in enumerate(m)]) == 1
+    assert L.mgemm_masked(*[1 if i == 0 else v for i, v in enumerate(m)]) == 1
+    mm = list(m)
+    mm[0], mm[2], mm[4], mm[8] = 1, FAKE, FAKE, 40
+    assert L.mgemm_masked(*mm) == 2            # fp8 M_max % 16
+    # k-grouped
+    k = [FAKE, FAKE, FAKE, FAKE, 4, 4096, 256, 256, None, None]
+    assert L.kgemm_grouped(*[None if i == 2 else v for i, v in enumerate(k)]) == 1
+    assert L.kgemm_grouped(*[0 if i == 5 else v for i, v in enumerate(k)]) == 1
+    assert L.kgemm_grouped(*[320 if i == 6 else v for i, v in enumerate(k)]) == 2
+    # plan / select / self-test
+    assert L.moe_plan(FAKE, 4, 0, FAKE, None, 0, FAKE, None, None) == 1
+    assert L.moe_plan(FAKE, 4, 8, FAKE, None, 5, FAKE, None, None) == 1
+    assert L.moe_select_tile(3, FAKE, 4, 256, 256, FAKE, None, None) == 1
+    assert L.moe_select_tile(0, FAKE, 4, 250, 256, FAKE, None, None) == 2
+    assert L.mg_wait_selftest(None, 1000, None) == 1
+
+
+def test_wait_limit_setting(lib):
+    old = lib.mg_get_wait_limit_ns()
+    try:
+        lib.mg_set_wait_limit_ns(12345)
+        assert lib.mg_get_wait_limit_ns() == 12345
+        lib.mg_set_wait_limit_ns(0)
+        assert lib.mg_get_wait_limit_ns() == 2_000_000_000
+    finally:
+        lib.mg_set_wait_limit_ns(old)
