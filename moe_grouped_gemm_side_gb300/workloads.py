@@ -266,6 +266,9 @@ WORKLOADS: Dict[str, dict] = {
         form="contiguous", dtype="bf16", E=64, N=4096, K=7168, align_q=128, seed=1004,
         a_std=7168 ** -0.5, b_std=7168 ** -0.5, counts=counts_zipf_prefill,
         second=dict(N=7168, K=2048)),
+    "prefill_fp8_e16_t8192_n4096_k7168": dict(
+        form="contiguous", dtype="fp8", E=16, N=4096, K=7168, align_q=128, seed=1006,
+        a_std=1.0, b_std=1.0, counts=lambda: counts_zipf_prefill(seed=1006, E=16, total=8192)),
     "kgrouped_bf16_e32_t65536_n4096_k2048": dict(
         form="kgrouped", dtype="bf16", E=32, N=4096, K=2048, T=65536, seed=1005,
         counts=counts_dirichlet),
