@@ -231,6 +231,16 @@ mg_status kgemm_grouped(const void* dY, const void* X, float* dW,
 mg_status mg_set_wait_limit_ns(int64_t ns);
 int64_t mg_get_wait_limit_ns(void);
 
+/* ------------------------------------------------------------------------
+ * Kernel family for the contiguous and masked forms.  0 (default): the
+ * CTA-pair kernel (two SMs share each MMA, 256 weight rows per tile) when
+ * N % 256 == 0, else the single-CTA kernel; 1: always the single-CTA kernel;
+ * 2: same as 0.  Results are identical up to fp32 summation order.
+ * Process-wide.  Returns MG_ERR_INVALID_ARG for other values.
+ * ------------------------------------------------------------------------ */
+mg_status mg_set_kernel_policy(int32_t policy);
+int32_t mg_get_kernel_policy(void);
+
 /* Self-test of the bounded wait: one CTA waits on a shared-memory barrier
  * that nothing will ever complete, with a limit of limit_ns, and must write
  * MG_ERR_TIMEOUT to *d_status and return.  Faults nothing. */

@@ -45,7 +45,11 @@ SIGNATURES = {
     "mg_set_wait_limit_ns": (_i32, [_i64]),
     "mg_get_wait_limit_ns": (_i64, []),
     "mg_wait_selftest": (_i32, [_vp, _i64, _vp]),
+    "mg_set_kernel_policy": (_i32, [_i32]),
+    "mg_get_kernel_policy": (_i32, []),
 }
+
+POLICY_AUTO, POLICY_SINGLE_CTA, POLICY_CTA_PAIR = 0, 1, 2
 
 _LIB = None
 
@@ -201,3 +205,11 @@ def get_wait_limit_ns() -> int:
 
 def wait_selftest(status, limit_ns: int, stream=None):
     _check("mg_wait_selftest", load().mg_wait_selftest(_ptr(status), int(limit_ns), _stream(stream)))
+
+
+def set_kernel_policy(policy: int):
+    _check("mg_set_kernel_policy", load().mg_set_kernel_policy(int(policy)))
+
+
+def get_kernel_policy() -> int:
+    return load().mg_get_kernel_policy()

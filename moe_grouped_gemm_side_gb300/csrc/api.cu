@@ -19,6 +19,15 @@ namespace {
 
 constexpr int64_t kDefaultWaitNs = 2000000000LL;
 std::atomic<int64_t> g_wait_ns{kDefaultWaitNs};
+std::atomic<int32_t> g_policy{0};
+
+// The CTA-pair kernel needs 256-row weight blocks; policy 1 forces the
+// single-CTA kernel everywhere.
+bool use_pair(int32_t N) {
+  const int32_t pol = g_policy.load();
+  if (N % 256 != 0 || pol == 1) return false;
+  return true;
+}
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -57,14 +66,14 @@ mg_status encode_2d(CUtensorMap* m, CUtensorMapDataType dt, uint32_t elem, const
 }
 
 // Tensor map over uint8 block scales [d2, d1, d0] (d0 contiguous), box
-// {box0, 1, 1}.
+// {box0, box1, 1}.
 mg_status encode_sf_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
-                       uint32_t box0) {
+                       uint32_t box0, uint32_t box1) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return MG_ERR_CUDA;
   cuuint64_t dims[3] = {d0, d1, d2};
   cuuint64_t strides[2] = {d0, d0 * d1};
-  cuuint32_t box[3] = {box0, 1, 1};
+  cuuint32_t box[3] = {box0, box1, 1};
   cuuint32_t es[3] = {1, 1, 1};
   const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims,
                         strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -96,8 +105,11 @@ mg_status check_fwd_common(mg_dtype dt, const void* A, const uint8_t* SFA, const
   return MG_OK;
 }
 
+// sf_kblocks: K-blocks of token scales per TMA box (1 for the single-CTA
+// kernel, 4 for the CTA-pair kernel, which packs four K-blocks per word).
 mg_status encode_operands(FwdArgs& a, const void* A, const uint8_t* SFA, const void* B,
-                          int64_t rows_total, int64_t sf_rows, int64_t sf_groups) {
+                          int64_t rows_total, int64_t sf_rows, int64_t sf_groups,
+                          uint32_t sf_kblocks) {
   const CUtensorMapDataType dt = a.fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const uint32_t elem = a.fp8 ? 1 : 2;
   const uint32_t box_k = 128 / elem;  // one 128-byte swizzle row
@@ -111,8 +123,12 @@ mg_status encode_operands(FwdArgs& a, const void* A, const uint8_t* SFA, const v
   st = encode_2d(&a.tmA16, dt, elem, A, (uint64_t)a.K, (uint64_t)rows_total, box_k, 16,
                  CU_TENSOR_MAP_SWIZZLE_128B);
   if (st != MG_OK) return st;
+  st = encode_2d(&a.tmA8, dt, elem, A, (uint64_t)a.K, (uint64_t)rows_total, box_k, 8,
+                 CU_TENSOR_MAP_SWIZZLE_128B);
+  if (st != MG_OK) return st;
   if (a.fp8) {
-    st = encode_sf_3d(&a.tmSF, SFA, (uint64_t)sf_rows, (uint64_t)a.K / 128, (uint64_t)sf_groups, 256);
+    st = encode_sf_3d(&a.tmSF, SFA, (uint64_t)sf_rows, (uint64_t)a.K / 128, (uint64_t)sf_groups, 256,
+                      sf_kblocks);
     if (st != MG_OK) return st;
   } else {
     std::memset(&a.tmSF, 0, sizeof(a.tmSF));
@@ -191,8 +207,8 @@ mg_status moe_select_tile(mg_dtype dt, const int32_t* d_counts, int32_t E, int32
   if (!valid_dtype(dt) || d_counts == nullptr || d_tile_q == nullptr) return MG_ERR_INVALID_ARG;
   if (E <= 0 || N <= 0 || K <= 0) return MG_ERR_INVALID_ARG;
   if (N % 128 != 0 || K % 128 != 0) return MG_ERR_UNSUPPORTED;
-  return from_cuda(launch_select(dt == MG_FP8_E4M3_UE8M0, d_counts, E, N, K, d_tile_q, d_status,
-                                 static_cast<cudaStream_t>(stream)));
+  return from_cuda(launch_select(dt == MG_FP8_E4M3_UE8M0, use_pair(N), d_counts, E, N, K,
+                                 d_tile_q, d_status, static_cast<cudaStream_t>(stream)));
 }
 
 mg_status moe_select_tile_host(mg_dtype dt, const int32_t* counts, int32_t E, int32_t N, int32_t K,
@@ -204,7 +220,9 @@ mg_status moe_select_tile_host(mg_dtype dt, const int32_t* counts, int32_t E, in
   int64_t tiles[kNumTileCand] = {};
   for (int i = 0; i < kNumTileCand; ++i)
     for (int32_t e = 0; e < E; ++e) tiles[i] += cdiv64(counts[e] > 0 ? counts[e] : 0, tile_candidate(fp8, i));
-  *tile_q = pick_tile(fp8, tiles, N / 128, sel_kblocks(fp8, K), num_sms > 0 ? num_sms : 152);
+  const int sms = num_sms > 0 ? num_sms : 152;
+  *tile_q = use_pair(N) ? pick_tile_pair(fp8, tiles, N / 256, sel_kblocks(fp8, K), sms / 2)
+                        : pick_tile(fp8, tiles, N / 128, sel_kblocks(fp8, K), sms);
   return MG_OK;
 }
 
@@ -235,9 +253,10 @@ mg_status mgemm_contiguous(mg_dtype dt, const void* A, const uint8_t* SFA, const
   a.D = D;
   a.status = d_status;
   a.wait_ns = g_wait_ns.load();
-  st = encode_operands(a, A, SFA, B, rows_cap, rows_cap, 1);
+  st = encode_operands(a, A, SFA, B, rows_cap, rows_cap, 1, use_pair(N) ? 4u : 1u);
   if (st != MG_OK) return st;
-  return from_cuda(launch_fwd(a, static_cast<cudaStream_t>(stream)));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return from_cuda(use_pair(N) ? launch_fwd2(a, s) : launch_fwd(a, s));
 }
 
 mg_status mgemm_masked(mg_dtype dt, const void* A, const uint8_t* SFA, const void* B,
@@ -261,9 +280,10 @@ mg_status mgemm_masked(mg_dtype dt, const void* A, const uint8_t* SFA, const voi
   a.D = D;
   a.status = d_status;
   a.wait_ns = g_wait_ns.load();
-  st = encode_operands(a, A, SFA, B, (int64_t)E * M_max, M_max, E);
+  st = encode_operands(a, A, SFA, B, (int64_t)E * M_max, M_max, E, use_pair(N) ? 4u : 1u);
   if (st != MG_OK) return st;
-  return from_cuda(launch_fwd(a, static_cast<cudaStream_t>(stream)));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return from_cuda(use_pair(N) ? launch_fwd2(a, s) : launch_fwd(a, s));
 }
 
 mg_status kgemm_grouped(const void* dY, const void* X, float* dW, const int32_t* d_counts,
@@ -298,6 +318,14 @@ mg_status mg_set_wait_limit_ns(int64_t ns) {
 }
 
 int64_t mg_get_wait_limit_ns(void) { return g_wait_ns.load(); }
+
+mg_status mg_set_kernel_policy(int32_t policy) {
+  if (policy < 0 || policy > 2) return MG_ERR_INVALID_ARG;
+  g_policy.store(policy);
+  return MG_OK;
+}
+
+int32_t mg_get_kernel_policy(void) { return g_policy.load(); }
 
 mg_status mg_wait_selftest(int32_t* d_status, int64_t limit_ns, void* stream) {
   if (d_status == nullptr || limit_ns <= 0 || limit_ns > 10000000000LL) return MG_ERR_INVALID_ARG;

@@ -99,8 +99,8 @@ __global__ void __launch_bounds__(kPlanThreads)
 }
 
 __global__ void select_kernel(const int32_t* __restrict__ counts, int32_t E, int32_t fp8,
-                              int32_t NB, int32_t KB, int32_t num_sms, int32_t* tile_q,
-                              int32_t* status) {
+                              int32_t pair, int32_t N, int32_t KB, int32_t num_sms,
+                              int32_t* tile_q, int32_t* status) {
   const int lane = threadIdx.x;
   int64_t tiles[kNumTileCand];
 #pragma unroll
@@ -118,7 +118,9 @@ __global__ void select_kernel(const int32_t* __restrict__ counts, int32_t E, int
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
     tiles[i] = s;
   }
-  if (lane == 0) *tile_q = pick_tile(fp8 != 0, tiles, NB, KB, num_sms);
+  if (lane == 0)
+    *tile_q = pair ? pick_tile_pair(fp8 != 0, tiles, N / 256, KB, num_sms / 2)
+                   : pick_tile(fp8 != 0, tiles, N / 128, KB, num_sms);
 }
 
 __global__ void wait_selftest_kernel(int32_t* status, int64_t limit_ns) {
@@ -156,10 +158,11 @@ cudaError_t launch_plan(const int32_t* counts, int32_t E, int32_t q, int64_t* of
   return cudaGetLastError();
 }
 
-cudaError_t launch_select(bool fp8, const int32_t* counts, int32_t E, int32_t N, int32_t K,
-                          int32_t* tile_q, int32_t* status, cudaStream_t s) {
-  select_kernel<<<1, 32, 0, s>>>(counts, E, fp8 ? 1 : 0, N / 128, (int32_t)sel_kblocks(fp8, K),
-                                 num_sms_current_device(), tile_q, status);
+cudaError_t launch_select(bool fp8, bool pair, const int32_t* counts, int32_t E, int32_t N,
+                          int32_t K, int32_t* tile_q, int32_t* status, cudaStream_t s) {
+  select_kernel<<<1, 32, 0, s>>>(counts, E, fp8 ? 1 : 0, pair ? 1 : 0, N,
+                                 (int32_t)sel_kblocks(fp8, K), num_sms_current_device(), tile_q,
+                                 status);
   return cudaGetLastError();
 }
 

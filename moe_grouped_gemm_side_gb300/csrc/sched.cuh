@@ -72,9 +72,9 @@ constexpr int64_t kSelMmaCyclesPerTok = 2;        // per K-block, per token colu
 constexpr int64_t kSelLoadNum = 8, kSelLoadDen = 5;  // cycles per 128-byte row (1.6)
 constexpr int64_t kSelTileOverhead = 2500;        // per tile
 
-MG_HD int64_t tile_cost_cycles(int q, int64_t KB) {
+MG_HD int64_t tile_cost_cycles(int q, int64_t KB, int b_rows_per_sm) {
   const int64_t mma = kSelMmaCyclesPerTok * q;
-  const int64_t load = (128 + q) * kSelLoadNum / kSelLoadDen;
+  const int64_t load = (128 + b_rows_per_sm) * kSelLoadNum / kSelLoadDen;
   return KB * max64(mma, load) + kSelTileOverhead;
 }
 
@@ -93,7 +93,27 @@ MG_HD int pick_tile(bool fp8, const int64_t (&token_tiles)[kNumTileCand], int64_
     const int q = tile_candidate(fp8, i);
     const int64_t T = token_tiles[i] * NB;
     const int64_t waves = cdiv64(T, num_sms);
-    const int64_t cost = waves * tile_cost_cycles(q, KB);
+    const int64_t cost = waves * tile_cost_cycles(q, KB, q);
+    if (best < 0 || cost <= best) {
+      best = cost;
+      best_q = q;
+    }
+  }
+  return best_q;
+}
+
+// Same choice for the CTA-pair kernel: a pair tile covers 256 weight rows
+// (NB_pair = N/256 per token tile), each SM stages q/2 token rows, and the
+// pairs are the workers.
+MG_HD int pick_tile_pair(bool fp8, const int64_t (&token_tiles)[kNumTileCand], int64_t NB_pair,
+                         int64_t KB, int num_pairs) {
+  int best_q = tile_candidate(fp8, kNumTileCand - 1);
+  int64_t best = -1;
+  for (int i = 0; i < kNumTileCand; ++i) {
+    const int q = tile_candidate(fp8, i);
+    const int64_t T = token_tiles[i] * NB_pair;
+    const int64_t waves = cdiv64(T, num_pairs);
+    const int64_t cost = waves * tile_cost_cycles(q, KB, q / 2);
     if (best < 0 || cost <= best) {
       best = cost;
       best_q = q;

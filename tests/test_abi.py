@@ -171,3 +171,13 @@ def test_wait_limit_setting(lib):
         assert lib.mg_get_wait_limit_ns() == 2_000_000_000
     finally:
         lib.mg_set_wait_limit_ns(old)
+
+
+def test_kernel_policy_setting(lib):
+    assert lib.mg_get_kernel_policy() == 0
+    try:
+        for v in (1, 2, 0):
+            assert lib.mg_set_kernel_policy(v) == 0 and lib.mg_get_kernel_policy() == v
+        assert lib.mg_set_kernel_policy(3) == 1 and lib.mg_get_kernel_policy() == 0
+    finally:
+        lib.mg_set_kernel_policy(0)

@@ -12,6 +12,15 @@ from tests import gpu_util as gu
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(autouse=True, params=["single_cta", "cta_pair"])
+def kernel_policy(request, lib):
+    """Run every case on both kernel families (the pair kernel needs N % 256 == 0;
+    other shapes fall back to the single-CTA kernel)."""
+    mb.set_kernel_policy(mb.POLICY_SINGLE_CTA if request.param == "single_cta" else mb.POLICY_CTA_PAIR)
+    yield request.param
+    mb.set_kernel_policy(mb.POLICY_AUTO)
+
+
 def run_contiguous(counts, N, K, dtype, align_q, tile_q=0, seed=1, integer=False, rows_extra=37,
                    a_std=1.0, b_std=1.0, dev="cuda"):
     """Builds operands with poisoned padding, runs the GPU, returns
