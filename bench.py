@@ -474,6 +474,8 @@ def run_ours(args):
     ws, rank, local = dist_setup()
     dev = torch.device("cuda", local)
     lib = mb.load()
+    mb.set_kernel_policy({"auto": mb.POLICY_AUTO, "single": mb.POLICY_SINGLE_CTA,
+                          "pair": mb.POLICY_CTA_PAIR}[args.kernel_policy])
     w = make_workload(args.workload, dev)
     stream = torch.cuda.current_stream()
     peaks = load_peaks()
@@ -549,7 +551,7 @@ def run_ours(args):
         "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_max / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3" if w.fp8 else "bf16", "data": "synthetic",
-        "config": w.config(),
+        "config": dict(w.config(), kernel_policy=args.kernel_policy),
         "per_gemm_ms": per_gemm,
         "roofline": roof,
         "cpu_baseline": cpu,
@@ -600,6 +602,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--kernel-policy", choices=["auto", "single", "pair"], default="auto",
+                    help="grouped GEMM kernel family (auto: CTA pairs when N %% 256 == 0)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
