@@ -603,7 +603,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--kernel-policy", choices=["auto", "single", "pair"], default="auto",
-                    help="grouped GEMM kernel family (auto: CTA pairs when N %% 256 == 0)")
+                    help="grouped GEMM kernel family (auto: single-CTA kernel)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

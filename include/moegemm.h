@@ -232,10 +232,11 @@ mg_status mg_set_wait_limit_ns(int64_t ns);
 int64_t mg_get_wait_limit_ns(void);
 
 /* ------------------------------------------------------------------------
- * Kernel family for the contiguous and masked forms.  0 (default): the
- * CTA-pair kernel (two SMs share each MMA, 256 weight rows per tile) when
- * N % 256 == 0, else the single-CTA kernel; 1: always the single-CTA kernel;
- * 2: same as 0.  Results are identical up to fp32 summation order.
+ * Kernel family for the contiguous and masked forms.  0 (default) and 1:
+ * the single-CTA kernel (128 weight rows per tile); 2: the CTA-pair kernel
+ * (two SMs of a cluster share each MMA, 256 weight rows per tile) when
+ * N % 256 == 0, else the single-CTA kernel.  Results are identical up to
+ * fp32 summation order.
  * Process-wide.  Returns MG_ERR_INVALID_ARG for other values.
  * ------------------------------------------------------------------------ */
 mg_status mg_set_kernel_policy(int32_t policy);

@@ -21,12 +21,11 @@ constexpr int64_t kDefaultWaitNs = 2000000000LL;
 std::atomic<int64_t> g_wait_ns{kDefaultWaitNs};
 std::atomic<int32_t> g_policy{0};
 
-// The CTA-pair kernel needs 256-row weight blocks; policy 1 forces the
-// single-CTA kernel everywhere.
+// Policy 0 (default) and 1 run the single-CTA kernel, which measured faster
+// on every workload here; policy 2 runs the CTA-pair kernel where it applies
+// (256-row weight blocks, so N % 256 == 0).
 bool use_pair(int32_t N) {
-  const int32_t pol = g_policy.load();
-  if (N % 256 != 0 || pol == 1) return false;
-  return true;
+  return g_policy.load() == 2 && N % 256 == 0;
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -105,8 +104,8 @@ mg_status check_fwd_common(mg_dtype dt, const void* A, const uint8_t* SFA, const
   return MG_OK;
 }
 
-// sf_kblocks: K-blocks of token scales per TMA box (1 for the single-CTA
-// kernel, 4 for the CTA-pair kernel, which packs four K-blocks per word).
+// sf_kblocks: K-blocks of token scales per TMA box (both kernels pack four
+// K-blocks per scale word and load their scales four K-blocks at a time).
 mg_status encode_operands(FwdArgs& a, const void* A, const uint8_t* SFA, const void* B,
                           int64_t rows_total, int64_t sf_rows, int64_t sf_groups,
                           uint32_t sf_kblocks) {
@@ -253,7 +252,7 @@ mg_status mgemm_contiguous(mg_dtype dt, const void* A, const uint8_t* SFA, const
   a.D = D;
   a.status = d_status;
   a.wait_ns = g_wait_ns.load();
-  st = encode_operands(a, A, SFA, B, rows_cap, rows_cap, 1, use_pair(N) ? 4u : 1u);
+  st = encode_operands(a, A, SFA, B, rows_cap, rows_cap, 1, 4u);
   if (st != MG_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   return from_cuda(use_pair(N) ? launch_fwd2(a, s) : launch_fwd(a, s));
@@ -280,7 +279,7 @@ mg_status mgemm_masked(mg_dtype dt, const void* A, const uint8_t* SFA, const voi
   a.D = D;
   a.status = d_status;
   a.wait_ns = g_wait_ns.load();
-  st = encode_operands(a, A, SFA, B, (int64_t)E * M_max, M_max, E, use_pair(N) ? 4u : 1u);
+  st = encode_operands(a, A, SFA, B, (int64_t)E * M_max, M_max, E, 4u);
   if (st != MG_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   return from_cuda(use_pair(N) ? launch_fwd2(a, s) : launch_fwd(a, s));

@@ -60,15 +60,48 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait that lets the hardware suspend the thread until the phase
+// completes or `hint_ns` elapses.  A suspended thread issues nothing, so
+// warps that wait for long stretches (the epilogue during a main loop, the
+// producer on a full ring) leave the scheduler to the MMA-issuing warp that
+// shares their SM sub-partition.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+constexpr uint32_t kWaitHintNs = 20000;
+
+// Non-blocking probe of a phase; much cheaper than try_wait when the phase
+// has already completed (the common case for a well-fed pipeline).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase of `bar` with the given parity to complete.  Gives up
 // when another role has raised `abort_flag` or when the absolute deadline
 // passes, in which case it raises the flag and records MG_ERR_TIMEOUT.
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, uint64_t deadline,
                                              volatile int32_t* abort_flag, int32_t* status) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_test_wait(bar, parity)) return true;
   while (true) {
     if (*abort_flag) return false;
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, kWaitHintNs)) return true;
     if (globaltimer_ns() > deadline) {
       *abort_flag = 1;
       set_status(status, MG_ERR_TIMEOUT);
@@ -79,7 +112,7 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, uin
 
 // Drain wait used on the way out: ignores the abort flag, still bounded.
 __device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity, uint64_t deadline) {
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_sleep(bar, parity, kWaitHintNs)) {
     if (globaltimer_ns() > deadline) return false;
   }
   return true;
@@ -314,6 +347,57 @@ __device__ __forceinline__ void mma_commit_pair(uint64_t* bar, uint16_t mask) {
 __device__ __forceinline__ void tmem_cp_32x128b_x4_pair(uint32_t taddr, uint64_t sdesc) {
   asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
                : "memory");
+}
+
+// ------------------------------------------------ packed FP8 block scales
+// One 32-bit TMEM scale word per row carries the UE8M0 scales of four
+// consecutive 128-wide K-blocks (byte i = K-block kb0 + i); the MMA picks
+// the byte with the scale ids of its instruction descriptor, so scales are
+// copied into TMEM once per four K-blocks.
+constexpr int kSfGroup = 4;
+constexpr int kSfRawBytes = kSfGroup * 256;               // [4][256] token scale bytes
+constexpr int kSfStageBytes = kSfRawBytes + 512 + 1024;   // raw + weight words + token words
+
+// Weight scale bytes of K-blocks kb..kb+3 packed into one word (127 past
+// the end).  `wsf` holds a tile's scales, lane l owning K-blocks l, l+32,
+// l+64, l+96.  Warp-collective.
+__device__ __forceinline__ uint32_t sf_weight_word(const uint32_t (&wsf)[4], int32_t kb,
+                                                   int32_t KB) {
+  uint32_t w = 0;
+#pragma unroll
+  for (int i = 0; i < kSfGroup; ++i) {
+    const int32_t k2 = kb + i;
+    uint32_t v = __shfl_sync(0xffffffffu, wsf[0], k2 & 31);
+    const uint32_t v1 = __shfl_sync(0xffffffffu, wsf[1], k2 & 31);
+    const uint32_t v2 = __shfl_sync(0xffffffffu, wsf[2], k2 & 31);
+    const uint32_t v3 = __shfl_sync(0xffffffffu, wsf[3], k2 & 31);
+    const int32_t sel = (k2 >> 5) & 3;
+    v = sel == 1 ? v1 : sel == 2 ? v2 : sel == 3 ? v3 : v;
+    w |= (k2 < KB ? (v & 0xFFu) : 127u) << (8 * i);
+  }
+  return w;
+}
+
+// Scale words of one 4-K-block group, from the raw token scales at `sfs`
+// ([4][256] bytes): weight words (every row the same four bytes) at
+// sfs + 1024 and token words (row t: its scales in the four K-blocks) at
+// sfs + 1536 (tokens 0-127) and sfs + 2048 (tokens 128-255), each a 32-row x
+// 16-byte matrix for tcgen05.cp 32x128b (row l, word c = token c*32 + l).
+// Lane l writes row l of each matrix.
+__device__ __forceinline__ void sf_build_words(uint8_t* sfs, uint32_t wword, uint32_t lane) {
+  *reinterpret_cast<uint4*>(sfs + kSfRawBytes + lane * 16) = make_uint4(wword, wword, wword, wword);
+#pragma unroll
+  for (int g = 0; g < 2; ++g) {
+    uint32_t v[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int t = g * 128 + c * 32 + (int)lane;
+      v[c] = (uint32_t)sfs[t] | ((uint32_t)sfs[256 + t] << 8) | ((uint32_t)sfs[512 + t] << 16) |
+             ((uint32_t)sfs[768 + t] << 24);
+    }
+    *reinterpret_cast<uint4*>(sfs + kSfRawBytes + 512 + g * 512 + lane * 16) =
+        make_uint4(v[0], v[1], v[2], v[3]);
+  }
 }
 
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }

@@ -19,10 +19,11 @@
 // ("Adapt kernels without adding a CPU stall").
 //
 // CTA = 6 warps: warp 0 issues TMA, warp 1 owns TMEM and issues tcgen05.mma
-// (and stages the fp8 block scales into TMEM), warps 2-5 drain the fp32
-// accumulator from TMEM and store bf16 rows.  Operands stream through a
-// shared-memory ring of up to 16 stages; two TMEM accumulators let the
-// epilogue of one tile overlap the main loop of the next.
+// (and stages the fp8 block scales into TMEM, four K-blocks per copy),
+// warps 2-5 drain the fp32 accumulators from TMEM and store bf16 rows.
+// Operands stream through a shared-memory ring of up to 16 stages; two TMEM
+// accumulators (columns 0 and 256) let the epilogue of one tile overlap the
+// main loop of the next.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -38,8 +39,8 @@ constexpr int kWRows = 128;                      // weight rows per tile (MMA M)
 constexpr int kRowBytes = 128;                   // K bytes per stage and row
 constexpr int kWTileBytes = kWRows * kRowBytes;  // 16 KB
 constexpr int kMaxQ = 256;
-constexpr int kSfRaw = 256;                      // token scale bytes per stage
-constexpr int kSfStage = 256 + 512 + 1024;       // raw + weight words + token words
+constexpr int kSfRaw = kSfRawBytes;              // [4][256] token scale bytes
+constexpr int kSfStage = kSfStageBytes;          // raw + weight words + token words
 constexpr int kGroupTiles = 8;                   // token tiles per raster group
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccStride = 256;             // TMEM columns between accumulators
@@ -243,6 +244,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   S = min(S, kMaxStages);
   uint8_t* ring = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(sf_area) + (uintptr_t)S * sf_bytes + 1023) & ~uintptr_t(1023));
+  // fp8 scale words sit at columns 496-507, so a second accumulator at column
+  // 256 needs N <= 240 there.
   const uint32_t n_acc = (!p.fp8 || sh.qn_max <= 240) ? 2u : 1u;
   const uint32_t tmem = sh.tmem_base;
 
@@ -259,15 +262,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int32_t t = blockIdx.x; ok && t < total; t += gridDim.x) {
         const Tile tl = decode_tile(t, tpre, cnt, rowbase, E, NB, q, p.masked);
         const int32_t wy = tl.e * p.N + tl.nb * kWRows;
-        const uint32_t bytes = kWTileBytes + tl.qn * kRowBytes + (p.fp8 ? kSfRaw : 0);
+        const uint32_t bytes = kWTileBytes + tl.qn * kRowBytes;
         for (int32_t kb = 0; kb < KB; ++kb) {
+          const bool group = p.fp8 && (kb % kSfGroup) == 0;
           if (!wait_bounded(&sh.empty[stage], phase ^ 1u, deadline, &sh.abort_flag, p.status)) {
             ok = false;
             break;
           }
           uint8_t* sw = ring + (size_t)stage * stage_bytes;
           uint8_t* sa = sw + kWTileBytes;
-          mbar_arrive_expect_tx(&sh.full[stage], bytes);
+          mbar_arrive_expect_tx(&sh.full[stage], bytes + (group ? (uint32_t)kSfRaw : 0u));
           const int32_t kx = kb * (p.fp8 ? 128 : 64);
           tma_load_2d(sw, &tmW, &sh.full[stage], kx, wy);
           for (int32_t r = 0; r < tl.qn;) {
@@ -279,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               r += 16;
             }
           }
-          if (p.fp8) tma_load_3d(sf_area + (size_t)stage * kSfStage, &tmSF, &sh.full[stage], tl.sf_x, kb, tl.sf_z);
+          if (group) tma_load_3d(sf_area + (size_t)stage * kSfStage, &tmSF, &sh.full[stage], tl.sf_x, kb, tl.sf_z);
           ++issued;
           if (++stage == (uint32_t)S) {
             stage = 0;
@@ -310,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!warp_wait(&sh.acc_empty[acc], acc_phase ^ 1u, deadline, &sh.abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + acc * kAccStride;
-        const uint32_t idesc = p.fp8 ? idesc_mxf8(kWRows, tl.qn) : idesc_bf16(kWRows, tl.qn, 0, 0);
+        const uint32_t idesc0 = p.fp8 ? idesc_mxf8(kWRows, tl.qn) : idesc_bf16(kWRows, tl.qn, 0, 0);
         for (int32_t kb = 0; kb < KB; ++kb) {
           if (!warp_wait(&sh.full[stage], phase, deadline, &sh.abort_flag, p.status)) {
             ok = false;
@@ -320,31 +324,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* sw = ring + (size_t)stage * stage_bytes;
           uint8_t* sa = sw + kWTileBytes;
           uint8_t* sfs = sf_area + (size_t)stage * kSfStage;
-          if (p.fp8) {
-            // TMEM scale words: lane l, column c holds the scale of row
-            // c*32 + l; every byte of a word carries the same UE8M0 value.
-            const uint32_t wb = __shfl_sync(0xffffffffu, wsf[kb >> 5], kb & 31) & 0xFFu;
-            const uint32_t ww = wb * 0x01010101u;
-            *reinterpret_cast<uint4*>(sfs + kSfRaw + lane * 16) = make_uint4(ww, ww, ww, ww);
-#pragma unroll
-            for (int g = 0; g < 2; ++g) {
-              uint32_t v[4];
-#pragma unroll
-              for (int c = 0; c < 4; ++c) v[c] = (uint32_t)sfs[g * 128 + c * 32 + lane] * 0x01010101u;
-              *reinterpret_cast<uint4*>(sfs + kSfRaw + 512 + g * 512 + lane * 16) =
-                  make_uint4(v[0], v[1], v[2], v[3]);
-            }
+          const bool group = p.fp8 && (kb % kSfGroup) == 0;
+          if (group) {
+            // TMEM scale words for K-blocks kb..kb+3: lane l, column c holds
+            // the word of row c*32 + l.
+            sf_build_words(sfs, sf_weight_word(wsf, kb, KB), lane);
             fence_proxy_async_smem();
             __syncwarp();
           }
           if (lane == 0) {
-            if (p.fp8) {
+            if (group) {
               tmem_cp_32x128b_x4(tmem + kSfaCol, desc_sf_32x16(smem_u32(sfs + kSfRaw)));
               tmem_cp_32x128b_x4(tmem + kSfbCol, desc_sf_32x16(smem_u32(sfs + kSfRaw + 512)));
               if (tl.qn > 128)
                 tmem_cp_32x128b_x4(tmem + kSfbCol + 4, desc_sf_32x16(smem_u32(sfs + kSfRaw + 1024)));
             }
             const uint32_t a0 = smem_u32(sw), b0 = smem_u32(sa);
+            const uint32_t sid = (uint32_t)(kb & 3);
+            const uint32_t idesc = p.fp8 ? (idesc0 | (sid << 4) | (sid << 29)) : idesc0;
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
               const uint64_t ad = desc_kmajor_sw128(a0 + ks * 32);

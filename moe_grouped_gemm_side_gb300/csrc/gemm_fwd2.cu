@@ -14,6 +14,7 @@
 //     commits are multicast to both CTAs' stage and accumulator barriers;
 //   * each CTA's epilogue drains its own TMEM (its own 128 weight rows) and
 //     releases the accumulator on the leader's barrier.
+
 //
 // FP8 block scales are packed four K-blocks per 32-bit TMEM word: one
 // tcgen05.cp per four K-blocks, the MMA selecting the byte with the scale
@@ -36,9 +37,8 @@ constexpr int kPairRows = 256;                   // weight rows per pair tile (M
 constexpr int kRowBytes = 128;
 constexpr int kWTileBytes = kWRows * kRowBytes;  // 16 KB
 constexpr int kMaxQ = 256;
-constexpr int kSfGroup = 4;                      // K-blocks per scale word
-constexpr int kSfRaw = kSfGroup * 256;           // [4][256] token scale bytes
-constexpr int kSfStage = kSfRaw + 512 + 1024;    // raw + weight words + token words
+constexpr int kSfRaw = kSfRawBytes;
+constexpr int kSfStage = kSfStageBytes;
 constexpr int kGroupTiles = 8;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccStride = 256;
@@ -107,44 +107,6 @@ __device__ __forceinline__ Tile decode_tile(int32_t t, const int32_t* tpre, cons
   tl.sf_x = masked ? in_e : tl.row0;
   tl.sf_z = masked ? lo : 0;
   return tl;
-}
-
-// Weight scale bytes of K-blocks kb..kb+3 of this CTA's 128-row block packed
-// into one word (byte i = K-block kb+i; 127 past the end).  `wsf` holds the
-// tile's scales, lane l owning K-blocks l, l+32, l+64, l+96.
-__device__ __forceinline__ uint32_t weight_word(const uint32_t (&wsf)[4], int32_t kb, int32_t KB) {
-  uint32_t w = 0;
-#pragma unroll
-  for (int i = 0; i < kSfGroup; ++i) {
-    const int32_t k2 = kb + i;
-    uint32_t v = __shfl_sync(0xffffffffu, wsf[0], k2 & 31);
-    const uint32_t v1 = __shfl_sync(0xffffffffu, wsf[1], k2 & 31);
-    const uint32_t v2 = __shfl_sync(0xffffffffu, wsf[2], k2 & 31);
-    const uint32_t v3 = __shfl_sync(0xffffffffu, wsf[3], k2 & 31);
-    const int32_t sel = (k2 >> 5) & 3;
-    v = sel == 1 ? v1 : sel == 2 ? v2 : sel == 3 ? v3 : v;
-    w |= (k2 < KB ? (v & 0xFFu) : 127u) << (8 * i);
-  }
-  return w;
-}
-
-// Scale words of one 4-K-block group: weight words (all rows of this CTA
-// carry the same four bytes) and token words (byte i of token t's word is
-// its scale in K-block kb0 + i).  Lane l writes row l of each 32x128b matrix.
-__device__ __forceinline__ void build_scale_words(uint8_t* sfs, uint32_t wword, uint32_t lane) {
-  *reinterpret_cast<uint4*>(sfs + kSfRaw + lane * 16) = make_uint4(wword, wword, wword, wword);
-#pragma unroll
-  for (int g = 0; g < 2; ++g) {
-    uint32_t v[4];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int t = g * 128 + c * 32 + (int)lane;
-      v[c] = (uint32_t)sfs[t] | ((uint32_t)sfs[256 + t] << 8) | ((uint32_t)sfs[512 + t] << 16) |
-             ((uint32_t)sfs[768 + t] << 24);
-    }
-    *reinterpret_cast<uint4*>(sfs + kSfRaw + 512 + g * 512 + lane * 16) =
-        make_uint4(v[0], v[1], v[2], v[3]);
-  }
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -280,6 +242,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   S = min(S, kMaxStages);
   uint8_t* ring = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(sf_area) + (uintptr_t)S * sf_bytes + 1023) & ~uintptr_t(1023));
+  // fp8 scale words sit at columns 496-507, so a second accumulator at column
+  // 256 needs N <= 240 there.
   const uint32_t n_acc = (!p.fp8 || sh.qn_max <= 240) ? 2u : 1u;
   const uint32_t tmem = sh.tmem_base;
 
@@ -381,7 +345,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               break;
             }
             if (group) {
-              build_scale_words(sfs, weight_word(wsf, kb, KB), lane);
+              sf_build_words(sfs, sf_weight_word(wsf, kb, KB), lane);
               fence_proxy_async_smem();
             }
             __syncwarp();
@@ -393,7 +357,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               break;
             }
             if (group) {
-              build_scale_words(sfs, weight_word(wsf, kb, KB), lane);
+              sf_build_words(sfs, sf_weight_word(wsf, kb, KB), lane);
               fence_proxy_async_smem();
               __syncwarp();
             }
