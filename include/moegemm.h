@@ -232,11 +232,13 @@ mg_status mg_set_wait_limit_ns(int64_t ns);
 int64_t mg_get_wait_limit_ns(void);
 
 /* ------------------------------------------------------------------------
- * Kernel family for the contiguous and masked forms.  0 (default) and 1:
- * the single-CTA kernel (128 weight rows per tile); 2: the CTA-pair kernel
- * (two SMs of a cluster share each MMA, 256 weight rows per tile) when
- * N % 256 == 0, else the single-CTA kernel.  Results are identical up to
- * fp32 summation order.
+ * Kernel family for the contiguous and masked forms.  0 (default): when
+ * N % 256 == 0 each CTA computes two adjacent 128-row weight blocks against
+ * one token tile (more multiply-adds per byte brought into shared memory),
+ * one block otherwise; 1: one 128-row weight block per CTA always; 2: the
+ * CTA-pair kernel (two SMs of a cluster share each MMA, 256 weight rows per
+ * tile) when N % 256 == 0, one block per CTA otherwise.
+ * Results are identical up to fp32 summation order.
  * Process-wide.  Returns MG_ERR_INVALID_ARG for other values.
  * ------------------------------------------------------------------------ */
 mg_status mg_set_kernel_policy(int32_t policy);

@@ -49,7 +49,7 @@ SIGNATURES = {
     "mg_get_kernel_policy": (_i32, []),
 }
 
-POLICY_AUTO, POLICY_SINGLE_CTA, POLICY_CTA_PAIR = 0, 1, 2
+POLICY_AUTO, POLICY_SINGLE_CTA, POLICY_CTA_PAIR = 0, 1, 2   # AUTO: two weight blocks per CTA
 
 _LIB = None
 

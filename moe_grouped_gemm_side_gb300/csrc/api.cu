@@ -21,11 +21,18 @@ constexpr int64_t kDefaultWaitNs = 2000000000LL;
 std::atomic<int64_t> g_wait_ns{kDefaultWaitNs};
 std::atomic<int32_t> g_policy{0};
 
-// Policy 0 (default) and 1 run the single-CTA kernel, which measured faster
-// on every workload here; policy 2 runs the CTA-pair kernel where it applies
-// (256-row weight blocks, so N % 256 == 0).
-bool use_pair(int32_t N) {
-  return g_policy.load() == 2 && N % 256 == 0;
+// Policy 0 (default): one CTA computes two 128-row weight blocks per tile
+// when N % 256 == 0, one block otherwise; 1: one block per CTA always;
+// 2: the CTA-pair kernel (cta_group::2) when N % 256 == 0.
+int fwd_variant(int32_t N) {
+  const int32_t pol = g_policy.load();
+  if (N % 256 != 0 || pol == 1) return kFwdSingle;
+  return pol == 2 ? kFwdPair : kFwdDual;
+}
+
+cudaError_t launch_fwd_any(const FwdArgs& a, cudaStream_t s) {
+  const int v = fwd_variant(a.N);
+  return v == kFwdPair ? launch_fwd2(a, s) : launch_fwd(a, s, v == kFwdDual);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -206,7 +213,7 @@ mg_status moe_select_tile(mg_dtype dt, const int32_t* d_counts, int32_t E, int32
   if (!valid_dtype(dt) || d_counts == nullptr || d_tile_q == nullptr) return MG_ERR_INVALID_ARG;
   if (E <= 0 || N <= 0 || K <= 0) return MG_ERR_INVALID_ARG;
   if (N % 128 != 0 || K % 128 != 0) return MG_ERR_UNSUPPORTED;
-  return from_cuda(launch_select(dt == MG_FP8_E4M3_UE8M0, use_pair(N), d_counts, E, N, K,
+  return from_cuda(launch_select(dt == MG_FP8_E4M3_UE8M0, fwd_variant(N), d_counts, E, N, K,
                                  d_tile_q, d_status, static_cast<cudaStream_t>(stream)));
 }
 
@@ -220,8 +227,7 @@ mg_status moe_select_tile_host(mg_dtype dt, const int32_t* counts, int32_t E, in
   for (int i = 0; i < kNumTileCand; ++i)
     for (int32_t e = 0; e < E; ++e) tiles[i] += cdiv64(counts[e] > 0 ? counts[e] : 0, tile_candidate(fp8, i));
   const int sms = num_sms > 0 ? num_sms : 152;
-  *tile_q = use_pair(N) ? pick_tile_pair(fp8, tiles, N / 256, sel_kblocks(fp8, K), sms / 2)
-                        : pick_tile(fp8, tiles, N / 128, sel_kblocks(fp8, K), sms);
+  *tile_q = pick_tile(fp8, tiles, fwd_variant(N), N, sel_kblocks(fp8, K), sms);
   return MG_OK;
 }
 
@@ -255,7 +261,7 @@ mg_status mgemm_contiguous(mg_dtype dt, const void* A, const uint8_t* SFA, const
   st = encode_operands(a, A, SFA, B, rows_cap, rows_cap, 1, 4u);
   if (st != MG_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return from_cuda(use_pair(N) ? launch_fwd2(a, s) : launch_fwd(a, s));
+  return from_cuda(launch_fwd_any(a, s));
 }
 
 mg_status mgemm_masked(mg_dtype dt, const void* A, const uint8_t* SFA, const void* B,
@@ -282,7 +288,7 @@ mg_status mgemm_masked(mg_dtype dt, const void* A, const uint8_t* SFA, const voi
   st = encode_operands(a, A, SFA, B, (int64_t)E * M_max, M_max, E, 4u);
   if (st != MG_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return from_cuda(use_pair(N) ? launch_fwd2(a, s) : launch_fwd(a, s));
+  return from_cuda(launch_fwd_any(a, s));
 }
 
 mg_status kgemm_grouped(const void* dY, const void* X, float* dW, const int32_t* d_counts,

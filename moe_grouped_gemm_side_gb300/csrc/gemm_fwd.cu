@@ -10,20 +10,27 @@
 // actual counts, experts with no tokens produce no tiles (so their weights are
 // never loaded) and tail rows are not written.
 //
-// Tile shape.  Tokens sit on the MMA N axis and 128 weight rows on the MMA M
-// axis, so a tile is 128 output columns x q_n token rows with q_n any
-// multiple of 16 up to 256, chosen per tile at run time: full tiles use the
-// selected token tile q, an expert's last tile is trimmed to round_up(rows,
-// 16).  The instruction descriptor and the TMA box count are runtime values,
-// so a single launch serves every tile size with no host round trip
-// ("Adapt kernels without adding a CPU stall").
+// Tile shape.  Tokens sit on the MMA N axis and 128-row weight blocks on the
+// MMA M axis.  A tile is kBlocks weight blocks (128 or 256 output columns)
+// x q_n token rows, q_n any multiple of 16 up to 256 chosen per tile at run
+// time: full tiles use the selected token tile q, an expert's last tile is
+// trimmed to round_up(rows, 16).  The instruction descriptor and the TMA box
+// count are runtime values, so one launch serves every tile size with no
+// host round trip ("Adapt kernels without adding a CPU stall").
+//
+// Why two weight blocks.  A K-block stage must arrive in shared memory
+// before its MMAs run, and on GB300 an SM takes in about 46 bytes per cycle
+// however the copies are issued; with one 128-row block and 256 tokens a
+// stage carries 48 KB for 2.1 M multiply-adds and the SM waits on data.  Two
+// weight blocks against the same token tile carry 64 KB for twice the
+// multiply-adds (1.5x the work per byte).  Their two 256-column fp32
+// accumulators fill TMEM, so that tile shape runs one tile at a time (the
+// epilogue is not overlapped); the one-block shape keeps two accumulators
+// and overlaps the epilogue of a tile with the next main loop.
 //
 // CTA = 6 warps: warp 0 issues TMA, warp 1 owns TMEM and issues tcgen05.mma
 // (and stages the fp8 block scales into TMEM, four K-blocks per copy),
 // warps 2-5 drain the fp32 accumulators from TMEM and store bf16 rows.
-// Operands stream through a shared-memory ring of up to 16 stages; two TMEM
-// accumulators (columns 0 and 256) let the epilogue of one tile overlap the
-// main loop of the next.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -35,16 +42,17 @@ namespace fwd {
 
 constexpr int kThreads = 192;
 constexpr int kMaxStages = 16;
-constexpr int kWRows = 128;                      // weight rows per tile (MMA M)
+constexpr int kWRows = 128;                      // rows of one weight block (MMA M)
 constexpr int kRowBytes = 128;                   // K bytes per stage and row
 constexpr int kWTileBytes = kWRows * kRowBytes;  // 16 KB
-constexpr int kMaxQ = 256;
 constexpr int kSfRaw = kSfRawBytes;              // [4][256] token scale bytes
-constexpr int kSfStage = kSfStageBytes;          // raw + weight words + token words
+// per-stage scale area: raw bytes, weight words of block 0, token words,
+// weight words of block 1
+constexpr int kSfStage = kSfStageBytes + 512;
+constexpr int kSfW1 = kSfStageBytes;             // offset of block-1 weight words
 constexpr int kGroupTiles = 8;                   // token tiles per raster group
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccStride = 256;             // TMEM columns between accumulators
-constexpr uint32_t kSfaCol = 496, kSfbCol = 500;  // fp8 scale columns
 constexpr int kSmemBytes = 227 * 1024;
 constexpr uint64_t kDrainNs = 200ull * 1000 * 1000;
 
@@ -83,9 +91,8 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64
 }
 
 // Tile t of the launch.  Experts in order; inside an expert, groups of
-// kGroupTiles token tiles sweep all 128-column weight blocks before moving
-// on, so CTAs working at the same time share weight and activation tiles in
-// L2.
+// kGroupTiles token tiles sweep all weight blocks before moving on, so CTAs
+// working at the same time share weight and activation tiles in L2.
 __device__ __forceinline__ Tile decode_tile(int32_t t, const int32_t* tpre, const int32_t* cnt,
                                             const int32_t* rowbase, int32_t E, int32_t NB,
                                             int32_t q, int32_t masked) {
@@ -113,10 +120,12 @@ __device__ __forceinline__ Tile decode_tile(int32_t t, const int32_t* tpre, cons
   return tl;
 }
 
+template <int kBlocks>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA64,
                const __grid_constant__ CUtensorMap tmA16, const __grid_constant__ CUtensorMap tmSF,
                const Params p) {
+  static_assert(kBlocks == 1 || kBlocks == 2, "one or two weight blocks per tile");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -130,8 +139,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const uint32_t warp = warp_id(), lane = lane_id();
   const uint64_t deadline = globaltimer_ns() + (uint64_t)p.wait_ns;
-  const int32_t NB = p.N / kWRows;
+  const int32_t NB = p.N / (kBlocks * kWRows);   // tiles per token tile
+  const int32_t NB128 = p.N / kWRows;
   const int32_t KB = p.K / (p.fp8 ? 128 : 64);
+  // TMEM: accumulator(s) at columns 0 and 256; fp8 scale words after the
+  // last accumulator: weight words of each block (4 columns each), then the
+  // token words (8 columns).
+  const uint32_t sfa_col = 496u;
+  const uint32_t sfb_col = kBlocks == 2 ? 504u : 500u;
+  // widest token tile: 256, but 240 where two fp8 accumulators must leave
+  // room for the scale words
+  const int32_t q_cap = (kBlocks == 2 && p.fp8) ? 240 : 256;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kMaxStages; ++i) {
@@ -161,7 +179,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- schedule (warp 0): row bases, token tile, tile prefix
   if (warp == 0) {
-    // row base of each expert
     if (p.masked) {
       for (int32_t e = lane; e < E; e += 32) rowbase[e] = e * p.M_max;
     } else {
@@ -189,10 +206,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0 && carry > p.rows_total) set_status(p.status, MG_ERR_CAPACITY);
     }
     __syncwarp();
-    // token tile
     int32_t q = p.tile_q;
     if (p.masked) {
-      q = kMaxQ;
+      q = q_cap;
     } else if (q == 0) {
       int64_t tiles[kNumTileCand];
 #pragma unroll
@@ -203,9 +219,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
         tiles[i] = s;
       }
-      q = pick_tile(p.fp8 != 0, tiles, NB, sel_kblocks(p.fp8 != 0, p.K), (int)gridDim.x);
+      q = pick_tile(p.fp8 != 0, tiles, kBlocks == 2 ? kFwdDual : kFwdSingle, p.N,
+                    sel_kblocks(p.fp8 != 0, p.K), (int)gridDim.x);
     }
-    // tile prefix (NB weight blocks per token tile) and the widest tile
+    q = min(q, q_cap);
     int32_t carry = 0, qmax = 0;
     for (int32_t b = 0; b < E; b += 32) {
       const int32_t e = b + lane;
@@ -236,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- ring layout, identical in every CTA
   const int32_t q = sh.q;
   const int32_t total = sh.total;
-  const int32_t stage_bytes = kWTileBytes + sh.qn_max * kRowBytes;
+  const int32_t stage_bytes = kBlocks * kWTileBytes + sh.qn_max * kRowBytes;
   const int32_t sf_bytes = p.fp8 ? kSfStage : 0;
   const int32_t avail = kSmemBytes - 1024 - (int32_t)(reinterpret_cast<uintptr_t>(sf_area) -
                                                      reinterpret_cast<uintptr_t>(smem)) - 1024;
@@ -244,9 +261,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   S = min(S, kMaxStages);
   uint8_t* ring = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(sf_area) + (uintptr_t)S * sf_bytes + 1023) & ~uintptr_t(1023));
-  // fp8 scale words sit at columns 496-507, so a second accumulator at column
-  // 256 needs N <= 240 there.
-  const uint32_t n_acc = (!p.fp8 || sh.qn_max <= 240) ? 2u : 1u;
+  // accumulator sets: two (double buffered) with one block, unless fp8 scale
+  // words need the columns; one with two blocks
+  const uint32_t n_acc = (kBlocks == 1 && (!p.fp8 || sh.qn_max <= 240)) ? 2u : 1u;
   const uint32_t tmem = sh.tmem_base;
 
   if (warp == 0) {
@@ -261,8 +278,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int32_t t = blockIdx.x; ok && t < total; t += gridDim.x) {
         const Tile tl = decode_tile(t, tpre, cnt, rowbase, E, NB, q, p.masked);
-        const int32_t wy = tl.e * p.N + tl.nb * kWRows;
-        const uint32_t bytes = kWTileBytes + tl.qn * kRowBytes;
+        const int32_t wy = tl.e * p.N + tl.nb * kBlocks * kWRows;
+        const uint32_t bytes = kBlocks * kWTileBytes + tl.qn * kRowBytes;
         for (int32_t kb = 0; kb < KB; ++kb) {
           const bool group = p.fp8 && (kb % kSfGroup) == 0;
           if (!wait_bounded(&sh.empty[stage], phase ^ 1u, deadline, &sh.abort_flag, p.status)) {
@@ -270,10 +287,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           uint8_t* sw = ring + (size_t)stage * stage_bytes;
-          uint8_t* sa = sw + kWTileBytes;
+          uint8_t* sa = sw + kBlocks * kWTileBytes;
           mbar_arrive_expect_tx(&sh.full[stage], bytes + (group ? (uint32_t)kSfRaw : 0u));
           const int32_t kx = kb * (p.fp8 ? 128 : 64);
-          tma_load_2d(sw, &tmW, &sh.full[stage], kx, wy);
+#pragma unroll
+          for (int b = 0; b < kBlocks; ++b)
+            tma_load_2d(sw + b * kWTileBytes, &tmW, &sh.full[stage], kx, wy + b * kWRows);
           for (int32_t r = 0; r < tl.qn;) {
             if (tl.qn - r >= 64) {
               tma_load_2d(sa + r * kRowBytes, &tmA64, &sh.full[stage], kx, tl.row0 + r);
@@ -303,62 +322,89 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int32_t t = blockIdx.x; ok && t < total; t += gridDim.x) {
         const Tile tl = decode_tile(t, tpre, cnt, rowbase, E, NB, q, p.masked);
-        uint32_t wsf[4] = {127u, 127u, 127u, 127u};
-        if (p.fp8) {
+        // weight scales of the tile's blocks: lane l holds K-blocks l + 32 i
+        uint32_t wsf[kBlocks][4];
+#pragma unroll
+        for (int b = 0; b < kBlocks; ++b)
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int32_t kb = (int32_t)lane + 32 * i;
-            if (kb < KB) wsf[i] = __ldg(p.sfb + ((int64_t)tl.e * KB + kb) * NB + tl.nb);
+            wsf[b][i] = (p.fp8 && kb < KB)
+                            ? __ldg(p.sfb + ((int64_t)tl.e * KB + kb) * NB128 + tl.nb * kBlocks + b)
+                            : 127u;
           }
-        }
         if (!warp_wait(&sh.acc_empty[acc], acc_phase ^ 1u, deadline, &sh.abort_flag, p.status)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem + acc * kAccStride;
+        const uint32_t d0 = tmem + acc * kAccStride;   // block b accumulates at d0 + b * 256
         const uint32_t idesc0 = p.fp8 ? idesc_mxf8(kWRows, tl.qn) : idesc_bf16(kWRows, tl.qn, 0, 0);
+        // The wait for stage kb+1 sits between the third and the fourth
+        // K-step of stage kb, so the tensor pipe still holds queued work
+        // while the warp waits; waiting after the whole stage left the pipe
+        // idle at every stage boundary.
+        if (!warp_wait(&sh.full[stage], phase, deadline, &sh.abort_flag, p.status)) break;
+        tc_fence_after();
         for (int32_t kb = 0; kb < KB; ++kb) {
-          if (!warp_wait(&sh.full[stage], phase, deadline, &sh.abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
           uint8_t* sw = ring + (size_t)stage * stage_bytes;
-          uint8_t* sa = sw + kWTileBytes;
           uint8_t* sfs = sf_area + (size_t)stage * kSfStage;
           const bool group = p.fp8 && (kb % kSfGroup) == 0;
           if (group) {
             // TMEM scale words for K-blocks kb..kb+3: lane l, column c holds
             // the word of row c*32 + l.
-            sf_build_words(sfs, sf_weight_word(wsf, kb, KB), lane);
+            sf_build_words(sfs, sf_weight_word(wsf[0], kb, KB), lane);
+            if (kBlocks == 2) {
+              const uint32_t w1 = sf_weight_word(wsf[kBlocks - 1], kb, KB);
+              *reinterpret_cast<uint4*>(sfs + kSfW1 + lane * 16) = make_uint4(w1, w1, w1, w1);
+            }
             fence_proxy_async_smem();
             __syncwarp();
           }
+          const uint32_t a0 = smem_u32(sw), b0 = smem_u32(sw + kBlocks * kWTileBytes);
+          const uint32_t sid = (uint32_t)(kb & 3);
+          const uint32_t idesc = p.fp8 ? (idesc0 | (sid << 4) | (sid << 29)) : idesc0;
           if (lane == 0) {
             if (group) {
-              tmem_cp_32x128b_x4(tmem + kSfaCol, desc_sf_32x16(smem_u32(sfs + kSfRaw)));
-              tmem_cp_32x128b_x4(tmem + kSfbCol, desc_sf_32x16(smem_u32(sfs + kSfRaw + 512)));
+              tmem_cp_32x128b_x4(tmem + sfa_col, desc_sf_32x16(smem_u32(sfs + kSfRaw)));
+              if (kBlocks == 2)
+                tmem_cp_32x128b_x4(tmem + sfa_col + 4, desc_sf_32x16(smem_u32(sfs + kSfW1)));
+              tmem_cp_32x128b_x4(tmem + sfb_col, desc_sf_32x16(smem_u32(sfs + kSfRaw + 512)));
               if (tl.qn > 128)
-                tmem_cp_32x128b_x4(tmem + kSfbCol + 4, desc_sf_32x16(smem_u32(sfs + kSfRaw + 1024)));
+                tmem_cp_32x128b_x4(tmem + sfb_col + 4, desc_sf_32x16(smem_u32(sfs + kSfRaw + 1024)));
             }
-            const uint32_t a0 = smem_u32(sw), b0 = smem_u32(sa);
-            const uint32_t sid = (uint32_t)(kb & 3);
-            const uint32_t idesc = p.fp8 ? (idesc0 | (sid << 4) | (sid << 29)) : idesc0;
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-              const uint64_t ad = desc_kmajor_sw128(a0 + ks * 32);
+            for (int ks = 0; ks < 3; ++ks) {
               const uint64_t bd = desc_kmajor_sw128(b0 + ks * 32);
               const uint32_t accum = (kb | ks) != 0 ? 1u : 0u;
+#pragma unroll
+              for (int b = 0; b < kBlocks; ++b) {
+                const uint64_t ad = desc_kmajor_sw128(a0 + b * kWTileBytes + ks * 32);
+                if (p.fp8)
+                  mma_mxf8(d0 + b * kAccStride, ad, bd, idesc, tmem + sfa_col + 4 * b, tmem + sfb_col, accum);
+                else
+                  mma_f16(d0 + b * kAccStride, ad, bd, idesc, accum);
+              }
+            }
+          }
+          const uint32_t nstage = stage + 1 == (uint32_t)S ? 0u : stage + 1;
+          const uint32_t nphase = stage + 1 == (uint32_t)S ? phase ^ 1u : phase;
+          if (kb + 1 < KB && !warp_wait(&sh.full[nstage], nphase, deadline, &sh.abort_flag, p.status))
+            ok = false;
+          tc_fence_after();
+          if (lane == 0) {
+            const uint64_t bd = desc_kmajor_sw128(b0 + 96);
+#pragma unroll
+            for (int b = 0; b < kBlocks; ++b) {
+              const uint64_t ad = desc_kmajor_sw128(a0 + b * kWTileBytes + 96);
               if (p.fp8)
-                mma_mxf8(d_tmem, ad, bd, idesc, tmem + kSfaCol, tmem + kSfbCol, accum);
+                mma_mxf8(d0 + b * kAccStride, ad, bd, idesc, tmem + sfa_col + 4 * b, tmem + sfb_col, 1u);
               else
-                mma_f16(d_tmem, ad, bd, idesc, accum);
+                mma_f16(d0 + b * kAccStride, ad, bd, idesc, 1u);
             }
             mma_commit(&sh.empty[stage]);
           }
           __syncwarp();
-          if (++stage == (uint32_t)S) {
-            stage = 0;
-            phase ^= 1u;
-          }
+          stage = nstage;
+          phase = nphase;
+          if (!ok) break;
         }
         if (!ok) break;
         if (lane == 0) mma_commit(&sh.acc_full[acc]);
@@ -383,16 +429,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Tile tl = decode_tile(t, tpre, cnt, rowbase, E, NB, q, p.masked);
       if (!warp_wait(&sh.acc_full[acc], acc_phase, deadline, &sh.abort_flag, p.status)) break;
       tc_fence_after();
-      const int32_t n = tl.nb * kWRows + (int32_t)(quad * 32 + lane);
+      const int32_t n = tl.nb * kBlocks * kWRows + (int32_t)(quad * 32 + lane);
       const uint32_t taddr = tmem + ((quad * 32u) << 16) + acc * kAccStride;
       __nv_bfloat16* dcol = p.D + (int64_t)tl.row0 * p.N + n;
       for (int32_t c0 = 0; c0 < tl.qn; c0 += 16) {
-        uint32_t r[16];
-        tmem_ld16(taddr + (uint32_t)c0, r);
+        uint32_t r[kBlocks][16];
+#pragma unroll
+        for (int b = 0; b < kBlocks; ++b) tmem_ld16(taddr + b * kAccStride + (uint32_t)c0, r[b]);
         tmem_ld_wait();
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-          if (c0 + i < tl.rows) dcol[(int64_t)(c0 + i) * p.N] = __float2bfloat16_rn(__uint_as_float(r[i]));
+          if (c0 + i < tl.rows) {
+#pragma unroll
+            for (int b = 0; b < kBlocks; ++b)
+              dcol[(int64_t)(c0 + i) * p.N + b * kWRows] = __float2bfloat16_rn(__uint_as_float(r[b][i]));
+          }
       }
       tc_fence_before();
       mbar_arrive(&sh.acc_empty[acc]);
@@ -412,16 +463,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace fwd
 
-cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s) {
-  static bool attr_done[64] = {};
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s, bool two_blocks) {
+  static bool attr_done[2][64] = {};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
-  if (dev < 64 && !attr_done[dev]) {
-    err = cudaFuncSetAttribute(fwd::fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               fwd::kSmemBytes);
+  auto kernel = two_blocks ? fwd::fwd_kernel<2> : fwd::fwd_kernel<1>;
+  if (dev < 64 && !attr_done[two_blocks][dev]) {
+    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, fwd::kSmemBytes);
     if (err != cudaSuccess) return err;
-    attr_done[dev] = true;
+    attr_done[two_blocks][dev] = true;
   }
   fwd::Params p;
   p.counts = a.counts;
@@ -438,8 +489,8 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s) {
   p.M_max = a.M_max;
   p.align_q = a.align_q;
   p.tile_q = a.tile_q;
-  const int grid = num_sms_current_device();
-  fwd::fwd_kernel<<<grid, fwd::kThreads, fwd::kSmemBytes, s>>>(a.tmW, a.tmA64, a.tmA16, a.tmSF, p);
+  kernel<<<num_sms_current_device(), fwd::kThreads, fwd::kSmemBytes, s>>>(a.tmW, a.tmA64, a.tmA16,
+                                                                          a.tmSF, p);
   return cudaGetLastError();
 }
 

@@ -201,7 +201,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
         tiles[i] = s;
       }
-      q = pick_tile_pair(p.fp8 != 0, tiles, NB, sel_kblocks(p.fp8 != 0, p.K), n_pairs);
+      q = pick_tile(p.fp8 != 0, tiles, kFwdPair, p.N, sel_kblocks(p.fp8 != 0, p.K), 2 * n_pairs);
     }
     int32_t carry = 0, qmax = 0;
     for (int32_t b = 0; b < E; b += 32) {
@@ -335,37 +335,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           d_tmem = tmem + acc * kAccStride;
           idesc0 = p.fp8 ? idesc_mxf8(kPairRows, tl.qn) : idesc_bf16(kPairRows, tl.qn, 0, 0);
         }
-        for (int32_t kb = 0; kb < KB; ++kb) {
-          uint8_t* sfs = sf_area + (size_t)stage * kSfStage;
-          const bool group = p.fp8 && (kb % kSfGroup) == 0;
-          if (!leader) {
-            // peer: scale words of this stage's group, then tell the leader
+        if (!leader) {
+          // peer: scale words of each group, then tell the leader
+          for (int32_t kb = 0; kb < KB; ++kb) {
+            uint8_t* sfs = sf_area + (size_t)stage * kSfStage;
             if (!warp_wait(&sh.sf_full[stage], phase, deadline, &sh.abort_flag, p.status)) {
               ok = false;
               break;
             }
-            if (group) {
+            if (kb % kSfGroup == 0) {
               sf_build_words(sfs, sf_weight_word(wsf, kb, KB), lane);
               fence_proxy_async_smem();
             }
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(sf_ready_leader + (uint32_t)(stage * sizeof(uint64_t)));
             __syncwarp();
-          } else {
-            if (!warp_wait(&sh.full[stage], phase, deadline, &sh.abort_flag, p.status)) {
-              ok = false;
-              break;
+            if (++stage == (uint32_t)S) {
+              stage = 0;
+              phase ^= 1u;
             }
+          }
+        } else {
+          // leader: the wait for stage kb+1 (operands of both CTAs and, for
+          // fp8, the peer's scale words) sits between the third and fourth
+          // K-step MMA of stage kb, so the tensor pipe holds queued work while
+          // the warp waits.
+          ok = warp_wait(&sh.full[stage], phase, deadline, &sh.abort_flag, p.status) &&
+               (!p.fp8 || warp_wait(&sh.sf_ready[stage], phase, deadline, &sh.abort_flag, p.status));
+          tc_fence_after();
+          for (int32_t kb = 0; ok && kb < KB; ++kb) {
+            uint8_t* sfs = sf_area + (size_t)stage * kSfStage;
+            const bool group = p.fp8 && (kb % kSfGroup) == 0;
             if (group) {
               sf_build_words(sfs, sf_weight_word(wsf, kb, KB), lane);
               fence_proxy_async_smem();
               __syncwarp();
             }
-            if (p.fp8 && !warp_wait(&sh.sf_ready[stage], phase, deadline, &sh.abort_flag, p.status)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
+            uint8_t* sw = ring + (size_t)stage * stage_bytes;
+            const uint32_t a0 = smem_u32(sw), b0 = smem_u32(sw + kWTileBytes);
+            const uint32_t sid = (uint32_t)(kb & 3);
+            const uint32_t idesc = p.fp8 ? (idesc0 | (sid << 4) | (sid << 29)) : idesc0;
             if (lane == 0) {
               if (group) {
                 tmem_cp_32x128b_x4_pair(tmem + kSfaCol, desc_sf_32x16(smem_u32(sfs + kSfRaw)));
@@ -373,12 +382,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (tl.qn > 128)
                   tmem_cp_32x128b_x4_pair(tmem + kSfbCol + 4, desc_sf_32x16(smem_u32(sfs + kSfRaw + 1024)));
               }
-              uint8_t* sw = ring + (size_t)stage * stage_bytes;
-              const uint32_t a0 = smem_u32(sw), b0 = smem_u32(sw + kWTileBytes);
-              const uint32_t sid = (uint32_t)(kb & 3);
-              const uint32_t idesc = p.fp8 ? (idesc0 | (sid << 4) | (sid << 29)) : idesc0;
 #pragma unroll
-              for (int ks = 0; ks < 4; ++ks) {
+              for (int ks = 0; ks < 3; ++ks) {
                 const uint64_t ad = desc_kmajor_sw128(a0 + ks * 32);
                 const uint64_t bd = desc_kmajor_sw128(b0 + ks * 32);
                 const uint32_t accum = (kb | ks) != 0 ? 1u : 0u;
@@ -387,13 +392,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 else
                   mma_f16_pair(d_tmem, ad, bd, idesc, accum);
               }
+            }
+            const uint32_t nstage = stage + 1 == (uint32_t)S ? 0u : stage + 1;
+            const uint32_t nphase = stage + 1 == (uint32_t)S ? phase ^ 1u : phase;
+            if (kb + 1 < KB)
+              ok = warp_wait(&sh.full[nstage], nphase, deadline, &sh.abort_flag, p.status) &&
+                   (!p.fp8 || warp_wait(&sh.sf_ready[nstage], nphase, deadline, &sh.abort_flag, p.status));
+            tc_fence_after();
+            if (lane == 0) {
+              const uint64_t ad = desc_kmajor_sw128(a0 + 96);
+              const uint64_t bd = desc_kmajor_sw128(b0 + 96);
+              if (p.fp8)
+                mma_mxf8_pair(d_tmem, ad, bd, idesc, tmem + kSfaCol, tmem + kSfbCol, 1u);
+              else
+                mma_f16_pair(d_tmem, ad, bd, idesc, 1u);
               mma_commit_pair(&sh.empty[stage], 0x3);
             }
             __syncwarp();
-          }
-          if (++stage == (uint32_t)S) {
-            stage = 0;
-            phase ^= 1u;
+            stage = nstage;
+            phase = nphase;
           }
         }
         if (!ok) break;

@@ -27,7 +27,9 @@ struct FwdArgs {
   int64_t wait_ns = 0;
   CUtensorMap tmW{}, tmA64{}, tmA16{}, tmA8{}, tmSF{};
 };
-cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s);
+// Single-CTA kernel: 128 weight rows per tile, or 256 with `two_blocks`
+// (needs N % 256 == 0).
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s, bool two_blocks);
 // CTA-pair variant (cluster of two, cta_group::2); needs N % 256 == 0.
 cudaError_t launch_fwd2(const FwdArgs& a, cudaStream_t s);
 
@@ -45,7 +47,7 @@ cudaError_t launch_kgrouped(const KgArgs& a, cudaStream_t s);
 cudaError_t launch_plan(const int32_t* counts, int32_t E, int32_t q, int64_t* offsets,
                         int32_t* tiles, int32_t max_tiles, mg_plan_stats* stats,
                         int32_t* status, cudaStream_t s);
-cudaError_t launch_select(bool fp8, bool pair, const int32_t* counts, int32_t E, int32_t N,
+cudaError_t launch_select(bool fp8, int variant, const int32_t* counts, int32_t E, int32_t N,
                           int32_t K, int32_t* tile_q, int32_t* status, cudaStream_t s);
 cudaError_t launch_wait_selftest(int32_t* status, int64_t limit_ns, cudaStream_t s);
 

@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(kPlanThreads)
 }
 
 __global__ void select_kernel(const int32_t* __restrict__ counts, int32_t E, int32_t fp8,
-                              int32_t pair, int32_t N, int32_t KB, int32_t num_sms,
+                              int32_t variant, int32_t N, int32_t KB, int32_t num_sms,
                               int32_t* tile_q, int32_t* status) {
   const int lane = threadIdx.x;
   int64_t tiles[kNumTileCand];
@@ -119,8 +119,7 @@ __global__ void select_kernel(const int32_t* __restrict__ counts, int32_t E, int
     tiles[i] = s;
   }
   if (lane == 0)
-    *tile_q = pair ? pick_tile_pair(fp8 != 0, tiles, N / 256, KB, num_sms / 2)
-                   : pick_tile(fp8 != 0, tiles, N / 128, KB, num_sms);
+    *tile_q = pick_tile(fp8 != 0, tiles, variant, N, KB, num_sms);
 }
 
 __global__ void wait_selftest_kernel(int32_t* status, int64_t limit_ns) {
@@ -158,9 +157,9 @@ cudaError_t launch_plan(const int32_t* counts, int32_t E, int32_t q, int64_t* of
   return cudaGetLastError();
 }
 
-cudaError_t launch_select(bool fp8, bool pair, const int32_t* counts, int32_t E, int32_t N,
+cudaError_t launch_select(bool fp8, int variant, const int32_t* counts, int32_t E, int32_t N,
                           int32_t K, int32_t* tile_q, int32_t* status, cudaStream_t s) {
-  select_kernel<<<1, 32, 0, s>>>(counts, E, fp8 ? 1 : 0, pair ? 1 : 0, N,
+  select_kernel<<<1, 32, 0, s>>>(counts, E, fp8 ? 1 : 0, variant, N,
                                  (int32_t)sel_kblocks(fp8, K), num_sms_current_device(), tile_q,
                                  status);
   return cudaGetLastError();

@@ -60,21 +60,23 @@ MG_HD int tile_candidate(bool fp8, int i) {
   return i == 0 ? 32 : i == 1 ? 64 : i == 2 ? 128 : (fp8 ? 240 : 256);
 }
 
-// Cost of one 128-weight-row x q-token tile, in SM cycles, for KB K-blocks
-// of 128 bytes.  Per K-block the tensor core needs about 2q cycles (128 x q x
-// 64 bf16 or 128 x q x 128 e4m3 multiply-adds) and the tile's operands
-// (128 + q rows of 128 bytes) must stream in from L2; whichever is slower
-// sets the pace, plus a fixed cost per tile for the pipeline fill and the
-// accumulator hand-off.  These are the three kernel-side terms of "MoE
-// GroupGEMM padding under expert skew", "Padding is not the whole cost model"
-// (padded MMA work, weight/activation traffic, scheduling overhead).
-constexpr int64_t kSelMmaCyclesPerTok = 2;        // per K-block, per token column
+// Cost of one tile on one SM, in SM cycles, for KB K-blocks of 128 bytes:
+// w_blocks 128-row weight blocks against q token columns, of which the SM
+// stages b_rows token rows itself.  Per K-block and weight block the tensor
+// core needs about 2q cycles (128 x q x 64 bf16 or 128 x q x 128 e4m3
+// multiply-adds) and the operands (128 w_blocks + b_rows rows of 128 bytes)
+// must stream into shared memory; whichever is slower sets the pace, plus a
+// fixed cost per tile for the pipeline fill and the accumulator hand-off.
+// These are the three kernel-side terms of "MoE GroupGEMM padding under
+// expert skew", "Padding is not the whole cost model" (padded MMA work,
+// weight/activation traffic, scheduling overhead).
+constexpr int64_t kSelMmaCyclesPerTok = 2;        // per K-block, weight block and token column
 constexpr int64_t kSelLoadNum = 8, kSelLoadDen = 5;  // cycles per 128-byte row (1.6)
 constexpr int64_t kSelTileOverhead = 2500;        // per tile
 
-MG_HD int64_t tile_cost_cycles(int q, int64_t KB, int b_rows_per_sm) {
-  const int64_t mma = kSelMmaCyclesPerTok * q;
-  const int64_t load = (128 + b_rows_per_sm) * kSelLoadNum / kSelLoadDen;
+MG_HD int64_t tile_cost_cycles(int q, int64_t KB, int w_blocks, int b_rows) {
+  const int64_t mma = kSelMmaCyclesPerTok * q * w_blocks;
+  const int64_t load = (128 * (int64_t)w_blocks + b_rows) * kSelLoadNum / kSelLoadDen;
   return KB * max64(mma, load) + kSelTileOverhead;
 }
 
@@ -82,38 +84,31 @@ MG_HD int64_t tile_cost_cycles(int q, int64_t KB, int b_rows_per_sm) {
 // is expressed in (64 bf16 or 128 e4m3 elements).
 MG_HD int64_t sel_kblocks(bool fp8, int64_t K) { return K * (fp8 ? 1 : 2) / 128; }
 
+// Kernel families of the contiguous and masked forms.
+enum FwdVariant : int {
+  kFwdSingle = 0,  // one CTA: 128 weight rows x q tokens
+  kFwdDual = 1,    // one CTA: 256 weight rows x q tokens (N % 256 == 0)
+  kFwdPair = 2,    // two CTAs sharing each MMA: 256 weight rows x q tokens
+};
+
 // Picks the token tile from the per-candidate token-tile counts
 // sum_e ceil(t_e/q).  The kernel's makespan is priced as whole waves of
-// tiles over the SMs times the cost of one tile; ties go to the larger tile.
-MG_HD int pick_tile(bool fp8, const int64_t (&token_tiles)[kNumTileCand], int64_t NB,
+// tiles over the workers times the cost of one tile; ties go to the larger
+// tile.  A single or dual tile is one CTA's work (N/128 or N/256 tiles per
+// token tile, num_sms workers); a pair tile covers 256 weight rows on two
+// SMs, each staging half of the token rows (num_sms/2 workers).
+MG_HD int pick_tile(bool fp8, const int64_t (&token_tiles)[kNumTileCand], int variant, int64_t N,
                     int64_t KB, int num_sms) {
+  const int64_t NB = variant == kFwdSingle ? N / 128 : N / 256;
+  const int workers = variant == kFwdPair ? (num_sms >= 2 ? num_sms / 2 : 1) : num_sms;
+  const int w_blocks = variant == kFwdDual ? 2 : 1;
   int best_q = tile_candidate(fp8, kNumTileCand - 1);
   int64_t best = -1;
   for (int i = 0; i < kNumTileCand; ++i) {
     const int q = tile_candidate(fp8, i);
     const int64_t T = token_tiles[i] * NB;
-    const int64_t waves = cdiv64(T, num_sms);
-    const int64_t cost = waves * tile_cost_cycles(q, KB, q);
-    if (best < 0 || cost <= best) {
-      best = cost;
-      best_q = q;
-    }
-  }
-  return best_q;
-}
-
-// Same choice for the CTA-pair kernel: a pair tile covers 256 weight rows
-// (NB_pair = N/256 per token tile), each SM stages q/2 token rows, and the
-// pairs are the workers.
-MG_HD int pick_tile_pair(bool fp8, const int64_t (&token_tiles)[kNumTileCand], int64_t NB_pair,
-                         int64_t KB, int num_pairs) {
-  int best_q = tile_candidate(fp8, kNumTileCand - 1);
-  int64_t best = -1;
-  for (int i = 0; i < kNumTileCand; ++i) {
-    const int q = tile_candidate(fp8, i);
-    const int64_t T = token_tiles[i] * NB_pair;
-    const int64_t waves = cdiv64(T, num_pairs);
-    const int64_t cost = waves * tile_cost_cycles(q, KB, q / 2);
+    const int64_t waves = cdiv64(T, workers);
+    const int64_t cost = waves * tile_cost_cycles(q, KB, w_blocks, variant == kFwdPair ? q / 2 : q);
     if (best < 0 || cost <= best) {
       best = cost;
       best_q = q;

@@ -11,11 +11,13 @@ from tests import gpu_util as gu
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(autouse=True, params=["single_cta", "cta_pair"])
+@pytest.fixture(autouse=True, params=["dual", "single_cta", "cta_pair"])
 def kernel_policy(request, lib):
-    """Run every case on both kernel families (the pair kernel needs N % 256 == 0;
-    other shapes fall back to the single-CTA kernel)."""
-    mb.set_kernel_policy(mb.POLICY_SINGLE_CTA if request.param == "single_cta" else mb.POLICY_CTA_PAIR)
+    """Run every case on every kernel family: two weight blocks per CTA (the
+    default), one block per CTA, and CTA pairs.  The 256-row variants need
+    N % 256 == 0; other shapes fall back to one block per CTA."""
+    mb.set_kernel_policy({"dual": mb.POLICY_AUTO, "single_cta": mb.POLICY_SINGLE_CTA,
+                          "cta_pair": mb.POLICY_CTA_PAIR}[request.param])
     yield request.param
     mb.set_kernel_policy(mb.POLICY_AUTO)
 
