@@ -28,9 +28,13 @@
 // epilogue is not overlapped); the one-block shape keeps two accumulators
 // and overlaps the epilogue of a tile with the next main loop.
 //
-// CTA = 6 warps: warp 0 issues TMA, warp 1 owns TMEM and issues tcgen05.mma
-// (and stages the fp8 block scales into TMEM, four K-blocks per copy),
-// warps 2-5 drain the fp32 accumulators from TMEM and store bf16 rows.
+// CTA = 7 warps: warp 0 issues TMA; warp 1 owns TMEM and one of its threads
+// issues every tcgen05.mma and tcgen05.cp; warps 2-5 drain the fp32
+// accumulators from TMEM and store bf16 rows; warp 6 (fp8 only) turns each
+// stage's raw UE8M0 bytes into the TMEM scale-word layout, four K-blocks per
+// word.  The tensor pipe queues only a few MMAs, so the issuing thread does
+// nothing between MMAs but wait for the next stage: any other work there
+// (warp-wide synchronisation, building scale words) left the pipe idle.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -40,7 +44,8 @@
 namespace mg {
 namespace fwd {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
+constexpr int kSfWarp = 6;
 constexpr int kMaxStages = 16;
 constexpr int kWRows = 128;                      // rows of one weight block (MMA M)
 constexpr int kRowBytes = 128;                   // K bytes per stage and row
@@ -70,6 +75,7 @@ struct Params {
 struct Shared {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
+  uint64_t sf_ready[kMaxStages];  // fp8: stage loaded and its scale words built
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint64_t drain;
@@ -155,6 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kMaxStages; ++i) {
       mbar_init(&sh.full[i], 1);
       mbar_init(&sh.empty[i], 1);
+      mbar_init(&sh.sf_ready[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh.acc_full[i], 1);
@@ -316,80 +323,53 @@ __global__ void __launch_bounds__(kThreads, 1)
         wait_drain(&sh.full[i % S], (uint32_t)((i / S) & 1), dl);
     }
   } else if (warp == 1) {
-    // ================================================= MMA issuer
-    if (S > 0) {
+    // ================================================= MMA issuer (one thread)
+    if (lane == 0 && S > 0) {
+      // fp8 stages are ready once warp 6 has built their scale words
+      uint64_t* ready = p.fp8 ? sh.sf_ready : sh.full;
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       for (int32_t t = blockIdx.x; ok && t < total; t += gridDim.x) {
         const Tile tl = decode_tile(t, tpre, cnt, rowbase, E, NB, q, p.masked);
-        // weight scales of the tile's blocks: lane l holds K-blocks l + 32 i
-        uint32_t wsf[kBlocks][4];
-#pragma unroll
-        for (int b = 0; b < kBlocks; ++b)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int32_t kb = (int32_t)lane + 32 * i;
-            wsf[b][i] = (p.fp8 && kb < KB)
-                            ? __ldg(p.sfb + ((int64_t)tl.e * KB + kb) * NB128 + tl.nb * kBlocks + b)
-                            : 127u;
-          }
-        if (!warp_wait(&sh.acc_empty[acc], acc_phase ^ 1u, deadline, &sh.abort_flag, p.status)) break;
+        if (!wait_bounded(&sh.acc_empty[acc], acc_phase ^ 1u, deadline, &sh.abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t d0 = tmem + acc * kAccStride;   // block b accumulates at d0 + b * 256
         const uint32_t idesc0 = p.fp8 ? idesc_mxf8(kWRows, tl.qn) : idesc_bf16(kWRows, tl.qn, 0, 0);
         // The wait for stage kb+1 sits between the third and the fourth
-        // K-step of stage kb, so the tensor pipe still holds queued work
-        // while the warp waits; waiting after the whole stage left the pipe
-        // idle at every stage boundary.
-        if (!warp_wait(&sh.full[stage], phase, deadline, &sh.abort_flag, p.status)) break;
-        tc_fence_after();
+        // K-step of stage kb, so the tensor pipe holds queued work while the
+        // thread waits.  No tcgen05 fence follows the stage waits: the
+        // stage's bytes are published by the mbarrier.
+        if (!wait_bounded(&ready[stage], phase, deadline, &sh.abort_flag, p.status)) break;
         for (int32_t kb = 0; kb < KB; ++kb) {
           uint8_t* sw = ring + (size_t)stage * stage_bytes;
-          uint8_t* sfs = sf_area + (size_t)stage * kSfStage;
-          const bool group = p.fp8 && (kb % kSfGroup) == 0;
-          if (group) {
-            // TMEM scale words for K-blocks kb..kb+3: lane l, column c holds
-            // the word of row c*32 + l.
-            sf_build_words(sfs, sf_weight_word(wsf[0], kb, KB), lane);
-            if (kBlocks == 2) {
-              const uint32_t w1 = sf_weight_word(wsf[kBlocks - 1], kb, KB);
-              *reinterpret_cast<uint4*>(sfs + kSfW1 + lane * 16) = make_uint4(w1, w1, w1, w1);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-          }
           const uint32_t a0 = smem_u32(sw), b0 = smem_u32(sw + kBlocks * kWTileBytes);
           const uint32_t sid = (uint32_t)(kb & 3);
           const uint32_t idesc = p.fp8 ? (idesc0 | (sid << 4) | (sid << 29)) : idesc0;
-          if (lane == 0) {
-            if (group) {
-              tmem_cp_32x128b_x4(tmem + sfa_col, desc_sf_32x16(smem_u32(sfs + kSfRaw)));
-              if (kBlocks == 2)
-                tmem_cp_32x128b_x4(tmem + sfa_col + 4, desc_sf_32x16(smem_u32(sfs + kSfW1)));
-              tmem_cp_32x128b_x4(tmem + sfb_col, desc_sf_32x16(smem_u32(sfs + kSfRaw + 512)));
-              if (tl.qn > 128)
-                tmem_cp_32x128b_x4(tmem + sfb_col + 4, desc_sf_32x16(smem_u32(sfs + kSfRaw + 1024)));
-            }
+          if (p.fp8 && sid == 0) {
+            const uint32_t sfs = smem_u32(sf_area + (size_t)stage * kSfStage);
+            tmem_cp_32x128b_x4(tmem + sfa_col, desc_sf_32x16(sfs + kSfRaw));
+            if (kBlocks == 2) tmem_cp_32x128b_x4(tmem + sfa_col + 4, desc_sf_32x16(sfs + kSfW1));
+            tmem_cp_32x128b_x4(tmem + sfb_col, desc_sf_32x16(sfs + kSfRaw + 512));
+            if (tl.qn > 128) tmem_cp_32x128b_x4(tmem + sfb_col + 4, desc_sf_32x16(sfs + kSfRaw + 1024));
+          }
 #pragma unroll
-            for (int ks = 0; ks < 3; ++ks) {
-              const uint64_t bd = desc_kmajor_sw128(b0 + ks * 32);
-              const uint32_t accum = (kb | ks) != 0 ? 1u : 0u;
+          for (int ks = 0; ks < 3; ++ks) {
+            const uint64_t bd = desc_kmajor_sw128(b0 + ks * 32);
+            const uint32_t accum = (kb | ks) != 0 ? 1u : 0u;
 #pragma unroll
-              for (int b = 0; b < kBlocks; ++b) {
-                const uint64_t ad = desc_kmajor_sw128(a0 + b * kWTileBytes + ks * 32);
-                if (p.fp8)
-                  mma_mxf8(d0 + b * kAccStride, ad, bd, idesc, tmem + sfa_col + 4 * b, tmem + sfb_col, accum);
-                else
-                  mma_f16(d0 + b * kAccStride, ad, bd, idesc, accum);
-              }
+            for (int b = 0; b < kBlocks; ++b) {
+              const uint64_t ad = desc_kmajor_sw128(a0 + b * kWTileBytes + ks * 32);
+              if (p.fp8)
+                mma_mxf8(d0 + b * kAccStride, ad, bd, idesc, tmem + sfa_col + 4 * b, tmem + sfb_col, accum);
+              else
+                mma_f16(d0 + b * kAccStride, ad, bd, idesc, accum);
             }
           }
           const uint32_t nstage = stage + 1 == (uint32_t)S ? 0u : stage + 1;
           const uint32_t nphase = stage + 1 == (uint32_t)S ? phase ^ 1u : phase;
-          if (kb + 1 < KB && !warp_wait(&sh.full[nstage], nphase, deadline, &sh.abort_flag, p.status))
+          if (kb + 1 < KB && !wait_bounded(&ready[nstage], nphase, deadline, &sh.abort_flag, p.status))
             ok = false;
-          tc_fence_after();
-          if (lane == 0) {
+          {
             const uint64_t bd = desc_kmajor_sw128(b0 + 96);
 #pragma unroll
             for (int b = 0; b < kBlocks; ++b) {
@@ -401,26 +381,67 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             mma_commit(&sh.empty[stage]);
           }
-          __syncwarp();
           stage = nstage;
           phase = nphase;
           if (!ok) break;
         }
         if (!ok) break;
-        if (lane == 0) mma_commit(&sh.acc_full[acc]);
-        __syncwarp();
+        mma_commit(&sh.acc_full[acc]);
         if (++acc == n_acc) {
           acc = 0;
           acc_phase ^= 1u;
         }
       }
-    }
-    // all tcgen05 work of this CTA completes before TMEM is released
-    if (lane == 0) {
+      // all tcgen05 work of this CTA completes before TMEM is released
       mma_commit(&sh.drain);
       wait_drain(&sh.drain, 0, globaltimer_ns() + kDrainNs);
     }
     __syncwarp();
+  } else if (warp == kSfWarp) {
+    // ================================================= fp8 scale words
+    // For every stage, in the order the MMA thread consumes them: wait until
+    // it has landed; on the first K-block of each group of four, write the
+    // TMEM scale words (weights of each block, tokens) next to the raw bytes;
+    // then mark the stage ready.  A stage's words are rewritten only after it
+    // has been refilled, i.e. after the MMAs and copies that read them.
+    if (p.fp8 && S > 0) {
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (int32_t t = blockIdx.x; ok && t < total; t += gridDim.x) {
+        const Tile tl = decode_tile(t, tpre, cnt, rowbase, E, NB, q, p.masked);
+        // weight scales of the tile's blocks: lane l holds K-blocks l + 32 i
+        uint32_t wsf[kBlocks][4];
+#pragma unroll
+        for (int b = 0; b < kBlocks; ++b)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int32_t kb = (int32_t)lane + 32 * i;
+            wsf[b][i] = kb < KB ? __ldg(p.sfb + ((int64_t)tl.e * KB + kb) * NB128 + tl.nb * kBlocks + b) : 127u;
+          }
+        for (int32_t kb = 0; kb < KB; ++kb) {
+          if (!warp_wait(&sh.full[stage], phase, deadline, &sh.abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          if ((kb % kSfGroup) == 0) {
+            uint8_t* sfs = sf_area + (size_t)stage * kSfStage;
+            // lane l, column c of a word block holds the word of row c*32 + l
+            sf_build_words(sfs, sf_weight_word(wsf[0], kb, KB), lane);
+            if (kBlocks == 2) {
+              const uint32_t w1 = sf_weight_word(wsf[kBlocks - 1], kb, KB);
+              *reinterpret_cast<uint4*>(sfs + kSfW1 + lane * 16) = make_uint4(w1, w1, w1, w1);
+            }
+            fence_proxy_async_smem();
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh.sf_ready[stage]);
+          if (++stage == (uint32_t)S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
   } else {
     // ================================================= epilogue
     const uint32_t quad = warp & 3u;  // TMEM lanes this warp may access
