@@ -28,9 +28,10 @@
 // epilogue is not overlapped); the one-block shape keeps two accumulators
 // and overlaps the epilogue of a tile with the next main loop.
 //
-// CTA = 7 warps: warp 0 issues TMA; warp 1 owns TMEM and one of its threads
-// issues every tcgen05.mma and tcgen05.cp; warps 2-5 drain the fp32
-// accumulators from TMEM and store bf16 rows; warp 6 (fp8 only) turns each
+// CTA = 11 warps: warp 0 issues TMA; warp 1 owns TMEM and one of its threads
+// issues every tcgen05.mma and tcgen05.cp; warps 2-5 and 7-10 drain the fp32
+// accumulators from TMEM (two warps per 32-lane quadrant, alternate 16-token
+// chunks) and store bf16 rows; warp 6 (fp8 only) turns each
 // stage's raw UE8M0 bytes into the TMEM scale-word layout, four K-blocks per
 // word.  The tensor pipe queues only a few MMAs, so the issuing thread does
 // nothing between MMAs but wait for the next stage: any other work there
@@ -44,8 +45,9 @@
 namespace mg {
 namespace fwd {
 
-constexpr int kThreads = 224;
+constexpr int kThreads = 352;
 constexpr int kSfWarp = 6;
+constexpr int kEpiThreads = 8 * 32;  // warps 2-5 and 7-10: two per TMEM lane quadrant
 constexpr int kMaxStages = 16;
 constexpr int kWRows = 128;                      // rows of one weight block (MMA M)
 constexpr int kRowBytes = 128;                   // K bytes per stage and row
@@ -56,6 +58,10 @@ constexpr int kSfRaw = kSfRawBytes;              // [4][256] token scale bytes
 constexpr int kSfStage = kSfStageBytes + 512;
 constexpr int kSfW1 = kSfStageBytes;             // offset of block-1 weight words
 constexpr int kGroupTiles = 8;                   // token tiles per raster group
+// Token-tile widths the producer publishes for the MMA thread, one slot per
+// tile; more slots than stages, so a slot is rewritten only after the MMA
+// thread has read it.
+constexpr int kInfoRing = 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccStride = 256;             // TMEM columns between accumulators
 constexpr int kSmemBytes = 227 * 1024;
@@ -84,6 +90,7 @@ struct Shared {
   int32_t q;         // token tile of full tiles
   int32_t qn_max;    // widest tile of this launch
   int32_t total;     // tiles of this launch
+  int32_t tile_qn[kInfoRing];
 };
 
 struct Tile {
@@ -165,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh.acc_full[i], 1);
-      mbar_init(&sh.acc_empty[i], 4 * 32);
+      mbar_init(&sh.acc_empty[i], kEpiThreads);
     }
     mbar_init(&sh.drain, 1);
     sh.abort_flag = 0;
@@ -283,8 +290,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t stage = 0, phase = 0;
       int64_t issued = 0;
       bool ok = true;
-      for (int32_t t = blockIdx.x; ok && t < total; t += gridDim.x) {
-        const Tile tl = decode_tile(t, tpre, cnt, rowbase, E, NB, q, p.masked);
+      // The next tile is decoded right after the current tile's first stage
+      // is issued, while the thread would wait for a free slot anyway.
+      Tile nxt{};
+      if ((int32_t)blockIdx.x < total) nxt = decode_tile(blockIdx.x, tpre, cnt, rowbase, E, NB, q, p.masked);
+      for (int32_t t = blockIdx.x, ti = 0; ok && t < total; t += gridDim.x, ++ti) {
+        const Tile tl = nxt;
         const int32_t wy = tl.e * p.N + tl.nb * kBlocks * kWRows;
         const uint32_t bytes = kBlocks * kWTileBytes + tl.qn * kRowBytes;
         for (int32_t kb = 0; kb < KB; ++kb) {
@@ -295,6 +306,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint8_t* sw = ring + (size_t)stage * stage_bytes;
           uint8_t* sa = sw + kBlocks * kWTileBytes;
+          // the stage's barrier publishes the tile's width with its bytes
+          if (kb == 0) sh.tile_qn[ti % kInfoRing] = tl.qn;
           mbar_arrive_expect_tx(&sh.full[stage], bytes + (group ? (uint32_t)kSfRaw : 0u));
           const int32_t kx = kb * (p.fp8 ? 128 : 64);
 #pragma unroll
@@ -310,6 +323,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (group) tma_load_3d(sf_area + (size_t)stage * kSfStage, &tmSF, &sh.full[stage], tl.sf_x, kb, tl.sf_z);
+          if (kb == 0 && t + (int32_t)gridDim.x < total)
+            nxt = decode_tile(t + gridDim.x, tpre, cnt, rowbase, E, NB, q, p.masked);
           ++issued;
           if (++stage == (uint32_t)S) {
             stage = 0;
@@ -329,17 +344,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint64_t* ready = p.fp8 ? sh.sf_ready : sh.full;
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
-      for (int32_t t = blockIdx.x; ok && t < total; t += gridDim.x) {
-        const Tile tl = decode_tile(t, tpre, cnt, rowbase, E, NB, q, p.masked);
+      for (int32_t t = blockIdx.x, ti = 0; ok && t < total; t += gridDim.x, ++ti) {
         if (!wait_bounded(&sh.acc_empty[acc], acc_phase ^ 1u, deadline, &sh.abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t d0 = tmem + acc * kAccStride;   // block b accumulates at d0 + b * 256
-        const uint32_t idesc0 = p.fp8 ? idesc_mxf8(kWRows, tl.qn) : idesc_bf16(kWRows, tl.qn, 0, 0);
         // The wait for stage kb+1 sits between the third and the fourth
         // K-step of stage kb, so the tensor pipe holds queued work while the
         // thread waits.  No tcgen05 fence follows the stage waits: the
         // stage's bytes are published by the mbarrier.
         if (!wait_bounded(&ready[stage], phase, deadline, &sh.abort_flag, p.status)) break;
+        // The tile's width comes from the producer through the first stage's
+        // barrier: decoding the tile here (a binary search and several
+        // divisions) left the tensor pipe idle at every tile boundary.
+        const int32_t qn = *reinterpret_cast<volatile int32_t*>(&sh.tile_qn[ti % kInfoRing]);
+        const uint32_t idesc0 = p.fp8 ? idesc_mxf8(kWRows, qn) : idesc_bf16(kWRows, qn, 0, 0);
         for (int32_t kb = 0; kb < KB; ++kb) {
           uint8_t* sw = ring + (size_t)stage * stage_bytes;
           const uint32_t a0 = smem_u32(sw), b0 = smem_u32(sw + kBlocks * kWTileBytes);
@@ -350,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_cp_32x128b_x4(tmem + sfa_col, desc_sf_32x16(sfs + kSfRaw));
             if (kBlocks == 2) tmem_cp_32x128b_x4(tmem + sfa_col + 4, desc_sf_32x16(sfs + kSfW1));
             tmem_cp_32x128b_x4(tmem + sfb_col, desc_sf_32x16(sfs + kSfRaw + 512));
-            if (tl.qn > 128) tmem_cp_32x128b_x4(tmem + sfb_col + 4, desc_sf_32x16(sfs + kSfRaw + 1024));
+            if (qn > 128) tmem_cp_32x128b_x4(tmem + sfb_col + 4, desc_sf_32x16(sfs + kSfRaw + 1024));
           }
 #pragma unroll
           for (int ks = 0; ks < 3; ++ks) {
@@ -407,17 +425,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (p.fp8 && S > 0) {
       uint32_t stage = 0, phase = 0;
       bool ok = true;
-      for (int32_t t = blockIdx.x; ok && t < total; t += gridDim.x) {
+      // weight scales of a tile's blocks: lane l holds K-blocks l + 32 i;
+      // the next tile's are fetched while the current tile streams
+      uint32_t wsf[kBlocks][4], wsf_nxt[kBlocks][4];
+      auto fetch_wsf = [&](int32_t t, uint32_t (&w)[kBlocks][4]) {
         const Tile tl = decode_tile(t, tpre, cnt, rowbase, E, NB, q, p.masked);
-        // weight scales of the tile's blocks: lane l holds K-blocks l + 32 i
-        uint32_t wsf[kBlocks][4];
 #pragma unroll
         for (int b = 0; b < kBlocks; ++b)
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int32_t kb = (int32_t)lane + 32 * i;
-            wsf[b][i] = kb < KB ? __ldg(p.sfb + ((int64_t)tl.e * KB + kb) * NB128 + tl.nb * kBlocks + b) : 127u;
+            w[b][i] = kb < KB ? __ldg(p.sfb + ((int64_t)tl.e * KB + kb) * NB128 + tl.nb * kBlocks + b) : 127u;
           }
+      };
+      if ((int32_t)blockIdx.x < total) fetch_wsf(blockIdx.x, wsf_nxt);
+      for (int32_t t = blockIdx.x; ok && t < total; t += gridDim.x) {
+#pragma unroll
+        for (int b = 0; b < kBlocks; ++b)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) wsf[b][i] = wsf_nxt[b][i];
         for (int32_t kb = 0; kb < KB; ++kb) {
           if (!warp_wait(&sh.full[stage], phase, deadline, &sh.abort_flag, p.status)) {
             ok = false;
@@ -435,6 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&sh.sf_ready[stage]);
+          if (kb == 0 && t + (int32_t)gridDim.x < total) fetch_wsf(t + gridDim.x, wsf_nxt);
           if (++stage == (uint32_t)S) {
             stage = 0;
             phase ^= 1u;
@@ -445,6 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ================================================= epilogue
     const uint32_t quad = warp & 3u;  // TMEM lanes this warp may access
+    const int32_t half = warp >= kSfWarp ? 1 : 0;
     uint32_t acc = 0, acc_phase = 0;
     for (int32_t t = blockIdx.x; S > 0 && t < total; t += gridDim.x) {
       const Tile tl = decode_tile(t, tpre, cnt, rowbase, E, NB, q, p.masked);
@@ -452,19 +480,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int32_t n = tl.nb * kBlocks * kWRows + (int32_t)(quad * 32 + lane);
       const uint32_t taddr = tmem + ((quad * 32u) << 16) + acc * kAccStride;
-      __nv_bfloat16* dcol = p.D + (int64_t)tl.row0 * p.N + n;
-      for (int32_t c0 = 0; c0 < tl.qn; c0 += 16) {
+      const bool odd = (lane & 1u) != 0;
+      __nv_bfloat16* dpair = p.D + (int64_t)tl.row0 * p.N + (n & ~1);
+      // the two warps of a lane quadrant take alternate 16-token chunks
+      for (int32_t c0 = 16 * half; c0 < tl.qn; c0 += 32) {
         uint32_t r[kBlocks][16];
 #pragma unroll
         for (int b = 0; b < kBlocks; ++b) tmem_ld16(taddr + b * kAccStride + (uint32_t)c0, r[b]);
         tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          if (c0 + i < tl.rows) {
+        for (int b = 0; b < kBlocks; ++b) tmem_regs_ready(r[b]);
+        // Lanes 2j and 2j+1 hold adjacent output columns.  One exchange per
+        // pair of tokens gives the even lane both columns of token i and the
+        // odd lane both columns of token i+1, so each store writes 4 bytes:
+        // half the store instructions of one 2-byte store per value.
 #pragma unroll
-            for (int b = 0; b < kBlocks; ++b)
-              dcol[(int64_t)(c0 + i) * p.N + b * kWRows] = __float2bfloat16_rn(__uint_as_float(r[b][i]));
+        for (int i = 0; i < 16; i += 2) {
+          const int32_t row = c0 + i + (odd ? 1 : 0);
+#pragma unroll
+          for (int b = 0; b < kBlocks; ++b) {
+            const float mine = __uint_as_float(odd ? r[b][i + 1] : r[b][i]);
+            const float recv = __shfl_xor_sync(0xffffffffu, __uint_as_float(odd ? r[b][i] : r[b][i + 1]), 1);
+            const __nv_bfloat162 v = odd ? __floats2bfloat162_rn(recv, mine) : __floats2bfloat162_rn(mine, recv);
+            if (row < tl.rows)
+              *reinterpret_cast<__nv_bfloat162*>(dpair + (int64_t)row * p.N + b * kWRows) = v;
           }
+        }
       }
       tc_fence_before();
       mbar_arrive(&sh.acc_empty[acc]);
