@@ -473,8 +473,7 @@ def run_ours(args):
     ws, rank, local = dist_setup()
     dev = torch.device("cuda", local)
     lib = mb.load()
-    mb.set_kernel_policy({"auto": mb.POLICY_AUTO, "single": mb.POLICY_SINGLE_CTA,
-                          "pair": mb.POLICY_CTA_PAIR}[args.kernel_policy])
+    mb.set_kernel_policy(mb.POLICIES[args.kernel_policy])
     w = make_workload(args.workload, dev)
     stream = torch.cuda.current_stream()
     peaks = load_peaks()
@@ -600,8 +599,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
-    ap.add_argument("--kernel-policy", choices=["auto", "single", "pair"], default="auto",
-                    help="grouped GEMM kernel family (auto: two 128-row weight blocks per CTA when N %% 256 == 0)")
+    ap.add_argument("--kernel-policy", choices=["auto", "single", "dual", "pair", "pair_dual"], default="auto",
+                    help="grouped GEMM kernel family (auto: two 128-row weight blocks per SM when N %% 256 == 0)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

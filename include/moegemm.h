@@ -232,13 +232,17 @@ mg_status mg_set_wait_limit_ns(int64_t ns);
 int64_t mg_get_wait_limit_ns(void);
 
 /* ------------------------------------------------------------------------
- * Kernel family for the contiguous and masked forms.  0 (default): when
- * N % 256 == 0 each CTA computes two adjacent 128-row weight blocks against
- * one token tile (more multiply-adds per byte brought into shared memory),
- * one block otherwise; 1: one 128-row weight block per CTA always; 2: the
- * CTA-pair kernel (two SMs of a cluster share each MMA, 256 weight rows per
- * tile) when N % 256 == 0, one block per CTA otherwise.
- * Results are identical up to fp32 summation order.
+ * Kernel family for the contiguous and masked forms.  A tile is one or two
+ * weight blocks against one token tile; a block is 128 weight rows on one SM
+ * or 256 rows on the two SMs of a cluster sharing each MMA (cta_group::2).
+ *   0 (default): single SM, two blocks when N % 256 == 0, one otherwise
+ *      (the fastest family measured on GB300);
+ *   1: single SM, one block (128 rows);
+ *   2: single SM, two blocks (256 rows; needs N % 256 == 0);
+ *   3: SM pair, one block (256 rows; needs N % 256 == 0);
+ *   4: SM pair, two blocks (512 rows; needs N % 512 == 0).
+ * A family whose tile does not divide N falls back to the next narrower one
+ * (4 -> 3 -> 1, 2 -> 1, 0 -> 1).  Results are identical up to fp32 summation order.
  * Process-wide.  Returns MG_ERR_INVALID_ARG for other values.
  * ------------------------------------------------------------------------ */
 mg_status mg_set_kernel_policy(int32_t policy);

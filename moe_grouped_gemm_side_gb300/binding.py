@@ -49,7 +49,10 @@ SIGNATURES = {
     "mg_get_kernel_policy": (_i32, []),
 }
 
-POLICY_AUTO, POLICY_SINGLE_CTA, POLICY_CTA_PAIR = 0, 1, 2   # AUTO: two weight blocks per CTA
+# Kernel families of the contiguous and masked forms (mg_set_kernel_policy).
+POLICY_AUTO, POLICY_SINGLE, POLICY_DUAL, POLICY_PAIR, POLICY_PAIR_DUAL = 0, 1, 2, 3, 4
+POLICIES = {"auto": POLICY_AUTO, "single": POLICY_SINGLE, "dual": POLICY_DUAL,
+            "pair": POLICY_PAIR, "pair_dual": POLICY_PAIR_DUAL}
 
 _LIB = None
 

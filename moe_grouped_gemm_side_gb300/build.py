@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libmoegemm.so")
 
-SOURCES = ["api.cu", "plan.cu", "gemm_fwd.cu", "gemm_fwd2.cu", "gemm_kgrouped.cu"]
+SOURCES = ["api.cu", "plan.cu", "gemm_fwd.cu", "gemm_kgrouped.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + [
     "-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",

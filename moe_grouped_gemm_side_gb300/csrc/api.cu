@@ -21,19 +21,21 @@ constexpr int64_t kDefaultWaitNs = 2000000000LL;
 std::atomic<int64_t> g_wait_ns{kDefaultWaitNs};
 std::atomic<int32_t> g_policy{0};
 
-// Policy 0 (default): one CTA computes two 128-row weight blocks per tile
-// when N % 256 == 0, one block otherwise; 1: one block per CTA always;
-// 2: the CTA-pair kernel (cta_group::2) when N % 256 == 0.
+// Kernel family for N.  Policy 0 (default) takes two 128-row weight blocks
+// per SM when N allows it: measured on GB300 it is the fastest family for
+// prefill and decode shapes alike (the SM-pair families lose on the
+// block-scaled fp8 path).  Policies 1-4 force single, dual, pair or
+// pair-dual, falling back to the widest family N allows when N is not a
+// multiple of the family's tile rows.
 int fwd_variant(int32_t N) {
   const int32_t pol = g_policy.load();
-  if (N % 256 != 0 || pol == 1) return kFwdSingle;
-  return pol == 2 ? kFwdPair : kFwdDual;
+  int v = pol == 0 ? kFwdDual : pol == 1 ? kFwdSingle : pol == 2 ? kFwdDual : pol == 3 ? kFwdPair : kFwdPairDual;
+  if (v == kFwdPairDual && N % 512 != 0) v = kFwdPair;
+  if ((v == kFwdPair || v == kFwdDual) && N % 256 != 0) v = kFwdSingle;
+  return v;
 }
 
-cudaError_t launch_fwd_any(const FwdArgs& a, cudaStream_t s) {
-  const int v = fwd_variant(a.N);
-  return v == kFwdPair ? launch_fwd2(a, s) : launch_fwd(a, s, v == kFwdDual);
-}
+cudaError_t launch_fwd_any(const FwdArgs& a, cudaStream_t s) { return launch_fwd(a, s, fwd_variant(a.N)); }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -325,7 +327,7 @@ mg_status mg_set_wait_limit_ns(int64_t ns) {
 int64_t mg_get_wait_limit_ns(void) { return g_wait_ns.load(); }
 
 mg_status mg_set_kernel_policy(int32_t policy) {
-  if (policy < 0 || policy > 2) return MG_ERR_INVALID_ARG;
+  if (policy < 0 || policy > 4) return MG_ERR_INVALID_ARG;
   g_policy.store(policy);
   return MG_OK;
 }

@@ -10,32 +10,35 @@
 // actual counts, experts with no tokens produce no tiles (so their weights are
 // never loaded) and tail rows are not written.
 //
-// Tile shape.  Tokens sit on the MMA N axis and 128-row weight blocks on the
-// MMA M axis.  A tile is kBlocks weight blocks (128 or 256 output columns)
-// x q_n token rows, q_n any multiple of 16 up to 256 chosen per tile at run
-// time: full tiles use the selected token tile q, an expert's last tile is
-// trimmed to round_up(rows, 16).  The instruction descriptor and the TMA box
-// count are runtime values, so one launch serves every tile size with no
-// host round trip ("Adapt kernels without adding a CPU stall").
+// Tile shape.  Tokens sit on the MMA N axis and weight rows on the MMA M
+// axis.  A tile is kBlocks weight blocks x q_n token rows, q_n any multiple
+// of 16 up to 256 chosen per tile at run time: full tiles use the selected
+// token tile q, an expert's last tile is trimmed to round_up(rows, 16).  The
+// instruction descriptor and the TMA box count are runtime values, so one
+// launch serves every tile size with no host round trip ("Adapt kernels
+// without adding a CPU stall").  A weight block is 128 rows on one SM
+// (cta_group::1) or 256 rows on the two SMs of a cluster (kPair,
+// cta_group::2: each SM holds 128 weight rows and half of the token rows,
+// and the MMA reads the other half from the peer).
 //
-// Why two weight blocks.  A K-block stage must arrive in shared memory
-// before its MMAs run, and on GB300 an SM takes in about 46 bytes per cycle
-// however the copies are issued; with one 128-row block and 256 tokens a
-// stage carries 48 KB for 2.1 M multiply-adds and the SM waits on data.  Two
-// weight blocks against the same token tile carry 64 KB for twice the
-// multiply-adds (1.5x the work per byte).  Their two 256-column fp32
-// accumulators fill TMEM, so that tile shape runs one tile at a time (the
-// epilogue is not overlapped); the one-block shape keeps two accumulators
-// and overlaps the epilogue of a tile with the next main loop.
+// Why bigger tiles.  Every MMA reads both operands from shared memory while
+// TMA writes the next stages into it; with one 128-row block a K-block stage
+// moves ~94 KB through an SM's shared memory for 3.9 M fp8 multiply-adds and
+// the tensor pipe waits.  Two blocks against the same token tile, and the
+// pair's split of the token operand, cut the bytes per multiply-add.  Two
+// 240/256-column fp32 accumulators fill TMEM, so two-block tiles run one at
+// a time (the epilogue is not overlapped); one-block tiles keep two
+// accumulators and overlap the epilogue with the next main loop.
 //
 // CTA = 11 warps: warp 0 issues TMA; warp 1 owns TMEM and one of its threads
-// issues every tcgen05.mma and tcgen05.cp; warps 2-5 and 7-10 drain the fp32
-// accumulators from TMEM (two warps per 32-lane quadrant, alternate 16-token
-// chunks) and store bf16 rows; warp 6 (fp8 only) turns each
-// stage's raw UE8M0 bytes into the TMEM scale-word layout, four K-blocks per
-// word.  The tensor pipe queues only a few MMAs, so the issuing thread does
-// nothing between MMAs but wait for the next stage: any other work there
-// (warp-wide synchronisation, building scale words) left the pipe idle.
+// (of the pair's first CTA) issues every tcgen05.mma and tcgen05.cp; warps
+// 2-5 and 7-10 drain the fp32 accumulators from TMEM (two warps per 32-lane
+// quadrant, alternate 16-token chunks) and store bf16 rows; warp 6 (fp8
+// only) turns each stage's raw UE8M0 bytes into the TMEM scale-word layout,
+// four K-blocks per word.  The tensor pipe queues only a few MMAs, so the
+// issuing thread does nothing between MMAs but wait for the next stage: any
+// other work there (warp-wide synchronisation, building scale words,
+// decoding tiles) left the pipe idle.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -47,11 +50,11 @@ namespace fwd {
 
 constexpr int kThreads = 352;
 constexpr int kSfWarp = 6;
-constexpr int kEpiThreads = 8 * 32;  // warps 2-5 and 7-10: two per TMEM lane quadrant
+constexpr int kEpiWarps = 8;                     // warps 2-5 and 7-10: two per TMEM lane quadrant
 constexpr int kMaxStages = 16;
-constexpr int kWRows = 128;                      // rows of one weight block (MMA M)
+constexpr int kCtaRows = 128;                    // weight rows of one block on one SM
 constexpr int kRowBytes = 128;                   // K bytes per stage and row
-constexpr int kWTileBytes = kWRows * kRowBytes;  // 16 KB
+constexpr int kWTileBytes = kCtaRows * kRowBytes;  // 16 KB
 constexpr int kSfRaw = kSfRawBytes;              // [4][256] token scale bytes
 // per-stage scale area: raw bytes, weight words of block 0, token words,
 // weight words of block 1
@@ -79,9 +82,10 @@ struct Params {
 };
 
 struct Shared {
-  uint64_t full[kMaxStages];
-  uint64_t empty[kMaxStages];
-  uint64_t sf_ready[kMaxStages];  // fp8: stage loaded and its scale words built
+  uint64_t full[kMaxStages];      // operand bytes (of both CTAs of a pair) landed
+  uint64_t empty[kMaxStages];     // the MMAs reading the stage are done
+  uint64_t sf_full[kMaxStages];   // fp8: this CTA's raw scale bytes of the stage landed
+  uint64_t sf_ready[kMaxStages];  // fp8: scale words of the stage built (in every CTA)
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint64_t drain;
@@ -133,12 +137,14 @@ __device__ __forceinline__ Tile decode_tile(int32_t t, const int32_t* tpre, cons
   return tl;
 }
 
-template <int kBlocks>
+template <int kBlocks, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA64,
-               const __grid_constant__ CUtensorMap tmA16, const __grid_constant__ CUtensorMap tmSF,
-               const Params p) {
+               const __grid_constant__ CUtensorMap tmA16, const __grid_constant__ CUtensorMap tmA8,
+               const __grid_constant__ CUtensorMap tmSF, const Params p) {
   static_assert(kBlocks == 1 || kBlocks == 2, "one or two weight blocks per tile");
+  constexpr int kBlockRows = kPair ? 2 * kCtaRows : kCtaRows;  // rows of one weight block (MMA M)
+  constexpr int kTileRows = kBlocks * kBlockRows;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -151,9 +157,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sf_area = reinterpret_cast<uint8_t*>((sched_end + 1023) & ~uintptr_t(1023));
 
   const uint32_t warp = warp_id(), lane = lane_id();
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  // workers: CTAs, or CTA pairs
+  const int32_t unit = kPair ? (int32_t)(blockIdx.x >> 1) : (int32_t)blockIdx.x;
+  const int32_t n_units = kPair ? (int32_t)(gridDim.x >> 1) : (int32_t)gridDim.x;
   const uint64_t deadline = globaltimer_ns() + (uint64_t)p.wait_ns;
-  const int32_t NB = p.N / (kBlocks * kWRows);   // tiles per token tile
-  const int32_t NB128 = p.N / kWRows;
+  const int32_t NB = p.N / kTileRows;   // tiles per token tile
+  const int32_t NB128 = p.N / kCtaRows;
   const int32_t KB = p.K / (p.fp8 ? 128 : 64);
   // TMEM: accumulator(s) at columns 0 and 256; fp8 scale words after the
   // last accumulator: weight words of each block (4 columns each), then the
@@ -168,17 +179,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kMaxStages; ++i) {
       mbar_init(&sh.full[i], 1);
       mbar_init(&sh.empty[i], 1);
-      mbar_init(&sh.sf_ready[i], 1);
+      mbar_init(&sh.sf_full[i], 1);
+      mbar_init(&sh.sf_ready[i], kPair ? 2 : 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh.acc_full[i], 1);
-      mbar_init(&sh.acc_empty[i], kEpiThreads);
+      mbar_init(&sh.acc_empty[i], kEpiWarps * (kPair ? 2 : 1));  // one arrival per epilogue warp
     }
     mbar_init(&sh.drain, 1);
     sh.abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 1) tmem_alloc(&sh.tmem_base, kTmemCols);
+  if (warp == 1) {
+    if constexpr (kPair) tmem_alloc_pair(&sh.tmem_base, kTmemCols);
+    else tmem_alloc(&sh.tmem_base, kTmemCols);
+  }
 
   // ---- validated counts
   for (int32_t e = threadIdx.x; e < E; e += kThreads) {
@@ -233,8 +248,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
         tiles[i] = s;
       }
-      q = pick_tile(p.fp8 != 0, tiles, kBlocks == 2 ? kFwdDual : kFwdSingle, p.N,
-                    sel_kblocks(p.fp8 != 0, p.K), (int)gridDim.x);
+      const int variant = kPair ? (kBlocks == 2 ? kFwdPairDual : kFwdPair) : (kBlocks == 2 ? kFwdDual : kFwdSingle);
+      q = pick_tile(p.fp8 != 0, tiles, variant, p.N, sel_kblocks(p.fp8 != 0, p.K), (int)gridDim.x);
     }
     q = min(q, q_cap);
     int32_t carry = 0, qmax = 0;
@@ -263,11 +278,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   tc_fence_after();
+  // barriers of both CTAs are initialised before any cross-CTA traffic
+  if constexpr (kPair) cluster_sync();
 
   // ---- ring layout, identical in every CTA
   const int32_t q = sh.q;
   const int32_t total = sh.total;
-  const int32_t stage_bytes = kBlocks * kWTileBytes + sh.qn_max * kRowBytes;
+  // token rows this CTA stages per tile: all of them, or its half of a pair
+  const int32_t stage_bytes = kBlocks * kWTileBytes + (kPair ? sh.qn_max / 2 : sh.qn_max) * kRowBytes;
   const int32_t sf_bytes = p.fp8 ? kSfStage : 0;
   const int32_t avail = kSmemBytes - 1024 - (int32_t)(reinterpret_cast<uintptr_t>(sf_area) -
                                                      reinterpret_cast<uintptr_t>(smem)) - 1024;
@@ -286,6 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmW);
       tma_prefetch_desc(&tmA64);
       tma_prefetch_desc(&tmA16);
+      if (kPair) tma_prefetch_desc(&tmA8);
       if (p.fp8) tma_prefetch_desc(&tmSF);
       uint32_t stage = 0, phase = 0;
       int64_t issued = 0;
@@ -293,11 +312,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // The next tile is decoded right after the current tile's first stage
       // is issued, while the thread would wait for a free slot anyway.
       Tile nxt{};
-      if ((int32_t)blockIdx.x < total) nxt = decode_tile(blockIdx.x, tpre, cnt, rowbase, E, NB, q, p.masked);
-      for (int32_t t = blockIdx.x, ti = 0; ok && t < total; t += gridDim.x, ++ti) {
+      if (unit < total) nxt = decode_tile(unit, tpre, cnt, rowbase, E, NB, q, p.masked);
+      for (int32_t t = unit, ti = 0; ok && t < total; t += n_units, ++ti) {
         const Tile tl = nxt;
-        const int32_t wy = tl.e * p.N + tl.nb * kBlocks * kWRows;
-        const uint32_t bytes = kBlocks * kWTileBytes + tl.qn * kRowBytes;
+        const int32_t qc = kPair ? tl.qn >> 1 : tl.qn;   // token rows staged here
+        const int32_t wy = tl.e * p.N + tl.nb * kTileRows + (int32_t)rank * kCtaRows;
+        const int32_t ty = tl.row0 + (int32_t)rank * qc;
+        const uint32_t bytes = (kPair ? 2u : 1u) * (uint32_t)(kBlocks * kWTileBytes + qc * kRowBytes);
         for (int32_t kb = 0; kb < KB; ++kb) {
           const bool group = p.fp8 && (kb % kSfGroup) == 0;
           if (!wait_bounded(&sh.empty[stage], phase ^ 1u, deadline, &sh.abort_flag, p.status)) {
@@ -306,25 +327,42 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint8_t* sw = ring + (size_t)stage * stage_bytes;
           uint8_t* sa = sw + kBlocks * kWTileBytes;
-          // the stage's barrier publishes the tile's width with its bytes
-          if (kb == 0) sh.tile_qn[ti % kInfoRing] = tl.qn;
-          mbar_arrive_expect_tx(&sh.full[stage], bytes + (group ? (uint32_t)kSfRaw : 0u));
+          if (leader) {
+            // the stage's barrier publishes the tile's width with its bytes
+            if (kb == 0) sh.tile_qn[ti % kInfoRing] = tl.qn;
+            mbar_arrive_expect_tx(&sh.full[stage], bytes);
+          }
+          // The raw scale bytes have a barrier of their own and are issued
+          // first: the 1 KB lands well before the operands, so warp 6 builds
+          // the scale words while the operands are still in flight.
+          if (p.fp8) {
+            mbar_arrive_expect_tx(&sh.sf_full[stage], group ? (uint32_t)kSfRaw : 0u);
+            if (group) tma_load_3d(sf_area + (size_t)stage * kSfStage, &tmSF, &sh.sf_full[stage], tl.sf_x, kb, tl.sf_z);
+          }
           const int32_t kx = kb * (p.fp8 ? 128 : 64);
+          if constexpr (kPair) {
+            // operand bytes of both CTAs complete the first CTA's barrier
+            const uint32_t bar = mapa_shared(smem_u32(&sh.full[stage]), 0);
 #pragma unroll
-          for (int b = 0; b < kBlocks; ++b)
-            tma_load_2d(sw + b * kWTileBytes, &tmW, &sh.full[stage], kx, wy + b * kWRows);
-          for (int32_t r = 0; r < tl.qn;) {
-            if (tl.qn - r >= 64) {
-              tma_load_2d(sa + r * kRowBytes, &tmA64, &sh.full[stage], kx, tl.row0 + r);
-              r += 64;
-            } else {
-              tma_load_2d(sa + r * kRowBytes, &tmA16, &sh.full[stage], kx, tl.row0 + r);
-              r += 16;
+            for (int b = 0; b < kBlocks; ++b)
+              tma_load_2d_pair(sw + b * kWTileBytes, &tmW, bar, kx, wy + b * kBlockRows);
+            for (int32_t r = 0; r < qc;) {
+              const int32_t left = qc - r;
+              const CUtensorMap* m = left >= 64 ? &tmA64 : (left >= 16 ? &tmA16 : &tmA8);
+              tma_load_2d_pair(sa + r * kRowBytes, m, bar, kx, ty + r);
+              r += left >= 64 ? 64 : (left >= 16 ? 16 : 8);
+            }
+          } else {
+#pragma unroll
+            for (int b = 0; b < kBlocks; ++b)
+              tma_load_2d(sw + b * kWTileBytes, &tmW, &sh.full[stage], kx, wy + b * kBlockRows);
+            for (int32_t r = 0; r < qc;) {
+              const bool wide = qc - r >= 64;
+              tma_load_2d(sa + r * kRowBytes, wide ? &tmA64 : &tmA16, &sh.full[stage], kx, ty + r);
+              r += wide ? 64 : 16;
             }
           }
-          if (group) tma_load_3d(sf_area + (size_t)stage * kSfStage, &tmSF, &sh.full[stage], tl.sf_x, kb, tl.sf_z);
-          if (kb == 0 && t + (int32_t)gridDim.x < total)
-            nxt = decode_tile(t + gridDim.x, tpre, cnt, rowbase, E, NB, q, p.masked);
+          if (kb == 0 && t + n_units < total) nxt = decode_tile(t + n_units, tpre, cnt, rowbase, E, NB, q, p.masked);
           ++issued;
           if (++stage == (uint32_t)S) {
             stage = 0;
@@ -332,19 +370,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      // every issued copy lands before the CTA can exit
+      // every copy this CTA can observe lands before it can exit (a pair's
+      // second CTA signals its operand copies on the first CTA's barriers,
+      // which the first CTA drains)
       const uint64_t dl = globaltimer_ns() + kDrainNs;
-      for (int64_t i = issued > S ? issued - S : 0; i < issued; ++i)
-        wait_drain(&sh.full[i % S], (uint32_t)((i / S) & 1), dl);
+      for (int64_t i = issued > S ? issued - S : 0; i < issued; ++i) {
+        if (leader) wait_drain(&sh.full[i % S], (uint32_t)((i / S) & 1), dl);
+        if (p.fp8) wait_drain(&sh.sf_full[i % S], (uint32_t)((i / S) & 1), dl);
+      }
+      if (kPair && !ok) {
+        // give the second CTA's operand copies still in flight time to land
+        const uint64_t until = globaltimer_ns() + 100000ull;
+        while (globaltimer_ns() < until) {
+        }
+      }
     }
   } else if (warp == 1) {
     // ================================================= MMA issuer (one thread)
-    if (lane == 0 && S > 0) {
-      // fp8 stages are ready once warp 6 has built their scale words
-      uint64_t* ready = p.fp8 ? sh.sf_ready : sh.full;
+    if (leader && lane == 0 && S > 0) {
+      // a stage is ready once its operands landed and (fp8) its scale words
+      // are built
+      auto ready = [&](uint32_t st, uint32_t ph) {
+        return wait_bounded(&sh.full[st], ph, deadline, &sh.abort_flag, p.status) &&
+               (!p.fp8 || wait_bounded(&sh.sf_ready[st], ph, deadline, &sh.abort_flag, p.status));
+      };
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
-      for (int32_t t = blockIdx.x, ti = 0; ok && t < total; t += gridDim.x, ++ti) {
+      for (int32_t t = unit, ti = 0; ok && t < total; t += n_units, ++ti) {
         if (!wait_bounded(&sh.acc_empty[acc], acc_phase ^ 1u, deadline, &sh.abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t d0 = tmem + acc * kAccStride;   // block b accumulates at d0 + b * 256
@@ -352,12 +404,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // K-step of stage kb, so the tensor pipe holds queued work while the
         // thread waits.  No tcgen05 fence follows the stage waits: the
         // stage's bytes are published by the mbarrier.
-        if (!wait_bounded(&ready[stage], phase, deadline, &sh.abort_flag, p.status)) break;
+        if (!ready(stage, phase)) break;
         // The tile's width comes from the producer through the first stage's
         // barrier: decoding the tile here (a binary search and several
         // divisions) left the tensor pipe idle at every tile boundary.
         const int32_t qn = *reinterpret_cast<volatile int32_t*>(&sh.tile_qn[ti % kInfoRing]);
-        const uint32_t idesc0 = p.fp8 ? idesc_mxf8(kWRows, qn) : idesc_bf16(kWRows, qn, 0, 0);
+        const uint32_t idesc0 = p.fp8 ? idesc_mxf8(kBlockRows, qn) : idesc_bf16(kBlockRows, qn, 0, 0);
         for (int32_t kb = 0; kb < KB; ++kb) {
           uint8_t* sw = ring + (size_t)stage * stage_bytes;
           const uint32_t a0 = smem_u32(sw), b0 = smem_u32(sw + kBlocks * kWTileBytes);
@@ -365,87 +417,96 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t idesc = p.fp8 ? (idesc0 | (sid << 4) | (sid << 29)) : idesc0;
           if (p.fp8 && sid == 0) {
             const uint32_t sfs = smem_u32(sf_area + (size_t)stage * kSfStage);
-            tmem_cp_32x128b_x4(tmem + sfa_col, desc_sf_32x16(sfs + kSfRaw));
-            if (kBlocks == 2) tmem_cp_32x128b_x4(tmem + sfa_col + 4, desc_sf_32x16(sfs + kSfW1));
-            tmem_cp_32x128b_x4(tmem + sfb_col, desc_sf_32x16(sfs + kSfRaw + 512));
-            if (qn > 128) tmem_cp_32x128b_x4(tmem + sfb_col + 4, desc_sf_32x16(sfs + kSfRaw + 1024));
+            if constexpr (kPair) {
+              tmem_cp_32x128b_x4_pair(tmem + sfa_col, desc_sf_32x16(sfs + kSfRaw));
+              if (kBlocks == 2) tmem_cp_32x128b_x4_pair(tmem + sfa_col + 4, desc_sf_32x16(sfs + kSfW1));
+              tmem_cp_32x128b_x4_pair(tmem + sfb_col, desc_sf_32x16(sfs + kSfRaw + 512));
+              if (qn > 128) tmem_cp_32x128b_x4_pair(tmem + sfb_col + 4, desc_sf_32x16(sfs + kSfRaw + 1024));
+            } else {
+              tmem_cp_32x128b_x4(tmem + sfa_col, desc_sf_32x16(sfs + kSfRaw));
+              if (kBlocks == 2) tmem_cp_32x128b_x4(tmem + sfa_col + 4, desc_sf_32x16(sfs + kSfW1));
+              tmem_cp_32x128b_x4(tmem + sfb_col, desc_sf_32x16(sfs + kSfRaw + 512));
+              if (qn > 128) tmem_cp_32x128b_x4(tmem + sfb_col + 4, desc_sf_32x16(sfs + kSfRaw + 1024));
+            }
           }
-#pragma unroll
-          for (int ks = 0; ks < 3; ++ks) {
+          auto kstep = [&](int ks, uint32_t accum) {
             const uint64_t bd = desc_kmajor_sw128(b0 + ks * 32);
-            const uint32_t accum = (kb | ks) != 0 ? 1u : 0u;
 #pragma unroll
             for (int b = 0; b < kBlocks; ++b) {
               const uint64_t ad = desc_kmajor_sw128(a0 + b * kWTileBytes + ks * 32);
-              if (p.fp8)
-                mma_mxf8(d0 + b * kAccStride, ad, bd, idesc, tmem + sfa_col + 4 * b, tmem + sfb_col, accum);
-              else
-                mma_f16(d0 + b * kAccStride, ad, bd, idesc, accum);
+              const uint32_t d = d0 + b * kAccStride;
+              if constexpr (kPair) {
+                if (p.fp8) mma_mxf8_pair(d, ad, bd, idesc, tmem + sfa_col + 4 * b, tmem + sfb_col, accum);
+                else mma_f16_pair(d, ad, bd, idesc, accum);
+              } else {
+                if (p.fp8) mma_mxf8(d, ad, bd, idesc, tmem + sfa_col + 4 * b, tmem + sfb_col, accum);
+                else mma_f16(d, ad, bd, idesc, accum);
+              }
             }
-          }
+          };
+#pragma unroll
+          for (int ks = 0; ks < 3; ++ks) kstep(ks, (kb | ks) != 0 ? 1u : 0u);
           const uint32_t nstage = stage + 1 == (uint32_t)S ? 0u : stage + 1;
           const uint32_t nphase = stage + 1 == (uint32_t)S ? phase ^ 1u : phase;
-          if (kb + 1 < KB && !wait_bounded(&ready[nstage], nphase, deadline, &sh.abort_flag, p.status))
+          if (kb + 1 < KB && !ready(nstage, nphase))
             ok = false;
-          {
-            const uint64_t bd = desc_kmajor_sw128(b0 + 96);
-#pragma unroll
-            for (int b = 0; b < kBlocks; ++b) {
-              const uint64_t ad = desc_kmajor_sw128(a0 + b * kWTileBytes + 96);
-              if (p.fp8)
-                mma_mxf8(d0 + b * kAccStride, ad, bd, idesc, tmem + sfa_col + 4 * b, tmem + sfb_col, 1u);
-              else
-                mma_f16(d0 + b * kAccStride, ad, bd, idesc, 1u);
-            }
-            mma_commit(&sh.empty[stage]);
-          }
+          kstep(3, 1u);
+          if constexpr (kPair) mma_commit_pair(&sh.empty[stage], 0x3);
+          else mma_commit(&sh.empty[stage]);
           stage = nstage;
           phase = nphase;
           if (!ok) break;
         }
         if (!ok) break;
-        mma_commit(&sh.acc_full[acc]);
+        if constexpr (kPair) mma_commit_pair(&sh.acc_full[acc], 0x3);
+        else mma_commit(&sh.acc_full[acc]);
         if (++acc == n_acc) {
           acc = 0;
           acc_phase ^= 1u;
         }
       }
-      // all tcgen05 work of this CTA completes before TMEM is released
-      mma_commit(&sh.drain);
-      wait_drain(&sh.drain, 0, globaltimer_ns() + kDrainNs);
+      // all tcgen05 work of the CTA (pair) completes before TMEM is released
+      if constexpr (kPair) mma_commit_pair(&sh.drain, 0x3);
+      else mma_commit(&sh.drain);
     }
+    if (lane == 0 && S > 0) wait_drain(&sh.drain, 0, globaltimer_ns() + kDrainNs);
     __syncwarp();
   } else if (warp == kSfWarp) {
     // ================================================= fp8 scale words
     // For every stage, in the order the MMA thread consumes them: wait until
-    // it has landed; on the first K-block of each group of four, write the
-    // TMEM scale words (weights of each block, tokens) next to the raw bytes;
-    // then mark the stage ready.  A stage's words are rewritten only after it
-    // has been refilled, i.e. after the MMAs and copies that read them.
+    // its raw scale bytes have landed; on the first K-block of each group of
+    // four, write the
+    // TMEM scale words (weights of each of this CTA's blocks, tokens) next to
+    // the raw bytes; then mark the stage ready on the first CTA of the pair.
+    // A stage's words are rewritten only after it has been refilled, i.e.
+    // after the MMAs and copies that read them.
     if (p.fp8 && S > 0) {
       uint32_t stage = 0, phase = 0;
       bool ok = true;
+      const uint32_t ready0 = mapa_shared(smem_u32(&sh.sf_ready[0]), 0);
       // weight scales of a tile's blocks: lane l holds K-blocks l + 32 i;
       // the next tile's are fetched while the current tile streams
       uint32_t wsf[kBlocks][4], wsf_nxt[kBlocks][4];
       auto fetch_wsf = [&](int32_t t, uint32_t (&w)[kBlocks][4]) {
         const Tile tl = decode_tile(t, tpre, cnt, rowbase, E, NB, q, p.masked);
 #pragma unroll
-        for (int b = 0; b < kBlocks; ++b)
+        for (int b = 0; b < kBlocks; ++b) {
+          const int32_t nb128 = (tl.nb * kTileRows + b * kBlockRows) / kCtaRows + (int32_t)rank;
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int32_t kb = (int32_t)lane + 32 * i;
-            w[b][i] = kb < KB ? __ldg(p.sfb + ((int64_t)tl.e * KB + kb) * NB128 + tl.nb * kBlocks + b) : 127u;
+            w[b][i] = kb < KB ? __ldg(p.sfb + ((int64_t)tl.e * KB + kb) * NB128 + nb128) : 127u;
           }
+        }
       };
-      if ((int32_t)blockIdx.x < total) fetch_wsf(blockIdx.x, wsf_nxt);
-      for (int32_t t = blockIdx.x; ok && t < total; t += gridDim.x) {
+      if (unit < total) fetch_wsf(unit, wsf_nxt);
+      for (int32_t t = unit; ok && t < total; t += n_units) {
 #pragma unroll
         for (int b = 0; b < kBlocks; ++b)
 #pragma unroll
           for (int i = 0; i < 4; ++i) wsf[b][i] = wsf_nxt[b][i];
         for (int32_t kb = 0; kb < KB; ++kb) {
-          if (!warp_wait(&sh.full[stage], phase, deadline, &sh.abort_flag, p.status)) {
+          if (!warp_wait(&sh.sf_full[stage], phase, deadline, &sh.abort_flag, p.status)) {
             ok = false;
             break;
           }
@@ -460,8 +521,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async_smem();
           }
           __syncwarp();
-          if (lane == 0) mbar_arrive(&sh.sf_ready[stage]);
-          if (kb == 0 && t + (int32_t)gridDim.x < total) fetch_wsf(t + gridDim.x, wsf_nxt);
+          if (lane == 0) {
+            if constexpr (kPair) mbar_arrive_cluster(ready0 + stage * (uint32_t)sizeof(uint64_t));
+            else mbar_arrive(&sh.sf_ready[stage]);
+          }
+          if (kb == 0 && t + n_units < total) fetch_wsf(t + n_units, wsf_nxt);
           if (++stage == (uint32_t)S) {
             stage = 0;
             phase ^= 1u;
@@ -473,14 +537,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================================================= epilogue
     const uint32_t quad = warp & 3u;  // TMEM lanes this warp may access
     const int32_t half = warp >= kSfWarp ? 1 : 0;
+    const uint32_t acc_empty0 = mapa_shared(smem_u32(&sh.acc_empty[0]), 0);
+    const bool odd = (lane & 1u) != 0;
     uint32_t acc = 0, acc_phase = 0;
-    for (int32_t t = blockIdx.x; S > 0 && t < total; t += gridDim.x) {
+    for (int32_t t = unit; S > 0 && t < total; t += n_units) {
       const Tile tl = decode_tile(t, tpre, cnt, rowbase, E, NB, q, p.masked);
       if (!warp_wait(&sh.acc_full[acc], acc_phase, deadline, &sh.abort_flag, p.status)) break;
       tc_fence_after();
-      const int32_t n = tl.nb * kBlocks * kWRows + (int32_t)(quad * 32 + lane);
+      // this thread's output column of block 0; block b is b * kBlockRows further
+      const int32_t n = tl.nb * kTileRows + (int32_t)(rank * kCtaRows + quad * 32 + lane);
       const uint32_t taddr = tmem + ((quad * 32u) << 16) + acc * kAccStride;
-      const bool odd = (lane & 1u) != 0;
       __nv_bfloat16* dpair = p.D + (int64_t)tl.row0 * p.N + (n & ~1);
       // the two warps of a lane quadrant take alternate 16-token chunks
       for (int32_t c0 = 16 * half; c0 < tl.qn; c0 += 32) {
@@ -492,8 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int b = 0; b < kBlocks; ++b) tmem_regs_ready(r[b]);
         // Lanes 2j and 2j+1 hold adjacent output columns.  One exchange per
         // pair of tokens gives the even lane both columns of token i and the
-        // odd lane both columns of token i+1, so each store writes 4 bytes:
-        // half the store instructions of one 2-byte store per value.
+        // odd lane both columns of token i+1, so each store writes 4 bytes.
 #pragma unroll
         for (int i = 0; i < 16; i += 2) {
           const int32_t row = c0 + i + (odd ? 1 : 0);
@@ -503,12 +568,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float recv = __shfl_xor_sync(0xffffffffu, __uint_as_float(odd ? r[b][i] : r[b][i + 1]), 1);
             const __nv_bfloat162 v = odd ? __floats2bfloat162_rn(recv, mine) : __floats2bfloat162_rn(mine, recv);
             if (row < tl.rows)
-              *reinterpret_cast<__nv_bfloat162*>(dpair + (int64_t)row * p.N + b * kWRows) = v;
+              *reinterpret_cast<__nv_bfloat162*>(dpair + (int64_t)row * p.N + b * kBlockRows) = v;
           }
         }
       }
       tc_fence_before();
-      mbar_arrive(&sh.acc_empty[acc]);
+      __syncwarp();
+      if (lane == 0) {
+        if constexpr (kPair) mbar_arrive_cluster(acc_empty0 + acc * (uint32_t)sizeof(uint64_t));
+        else mbar_arrive(&sh.acc_empty[acc]);
+      }
       if (++acc == n_acc) {
         acc = 0;
         acc_phase ^= 1u;
@@ -517,26 +586,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   __syncthreads();
+  // neither CTA of a pair releases TMEM or exits while the pair shares work
+  if constexpr (kPair) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    if constexpr (kPair) tmem_dealloc_pair(tmem, kTmemCols);
+    else tmem_dealloc(tmem, kTmemCols);
   }
 }
 
-}  // namespace fwd
-
-cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s, bool two_blocks) {
-  static bool attr_done[2][64] = {};
+template <int kBlocks, bool kPair>
+cudaError_t launch(const FwdArgs& a, cudaStream_t s) {
+  static bool attr_done[64] = {};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
-  auto kernel = two_blocks ? fwd::fwd_kernel<2> : fwd::fwd_kernel<1>;
-  if (dev < 64 && !attr_done[two_blocks][dev]) {
-    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, fwd::kSmemBytes);
+  auto kernel = fwd_kernel<kBlocks, kPair>;
+  if (dev < 64 && !attr_done[dev]) {
+    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (err != cudaSuccess) return err;
-    attr_done[two_blocks][dev] = true;
+    attr_done[dev] = true;
   }
-  fwd::Params p;
+  Params p;
   p.counts = a.counts;
   p.sfb = a.sfb;
   p.D = static_cast<__nv_bfloat16*>(a.D);
@@ -551,9 +622,32 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s, bool two_blocks) {
   p.M_max = a.M_max;
   p.align_q = a.align_q;
   p.tile_q = a.tile_q;
-  kernel<<<num_sms_current_device(), fwd::kThreads, fwd::kSmemBytes, s>>>(a.tmW, a.tmA64, a.tmA16,
-                                                                          a.tmSF, p);
-  return cudaGetLastError();
+  const int sms = num_sms_current_device();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kPair ? (unsigned)(sms / 2) * 2u : (unsigned)sms);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kPair ? 2 : 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = kPair ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, a.tmW, a.tmA64, a.tmA16, a.tmA8, a.tmSF, p);
+}
+
+}  // namespace fwd
+
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s, int variant) {
+  switch (variant) {
+    case kFwdSingle: return fwd::launch<1, false>(a, s);
+    case kFwdDual: return fwd::launch<2, false>(a, s);
+    case kFwdPair: return fwd::launch<1, true>(a, s);
+    case kFwdPairDual: return fwd::launch<2, true>(a, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace mg

@@ -27,11 +27,8 @@ struct FwdArgs {
   int64_t wait_ns = 0;
   CUtensorMap tmW{}, tmA64{}, tmA16{}, tmA8{}, tmSF{};
 };
-// Single-CTA kernel: 128 weight rows per tile, or 256 with `two_blocks`
-// (needs N % 256 == 0).
-cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s, bool two_blocks);
-// CTA-pair variant (cluster of two, cta_group::2); needs N % 256 == 0.
-cudaError_t launch_fwd2(const FwdArgs& a, cudaStream_t s);
+// Contiguous/masked kernel of one family (FwdVariant in sched.cuh).
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s, int variant);
 
 struct KgArgs {
   const int32_t* counts = nullptr;

@@ -63,19 +63,24 @@ MG_HD int tile_candidate(bool fp8, int i) {
 // Cost of one tile on one SM, in SM cycles, for KB K-blocks of 128 bytes:
 // w_blocks 128-row weight blocks against q token columns, of which the SM
 // stages b_rows token rows itself.  Per K-block and weight block the tensor
-// core needs about 2q cycles (128 x q x 64 bf16 or 128 x q x 128 e4m3
-// multiply-adds) and the operands (128 w_blocks + b_rows rows of 128 bytes)
-// must stream into shared memory; whichever is slower sets the pace, plus a
-// fixed cost per tile for the pipeline fill and the accumulator hand-off.
-// These are the three kernel-side terms of "MoE GroupGEMM padding under
-// expert skew", "Padding is not the whole cost model" (padded MMA work,
-// weight/activation traffic, scheduling overhead).
-constexpr int64_t kSelMmaCyclesPerTok = 2;        // per K-block, weight block and token column
+// core needs about 2.1q cycles for bf16 (128 x q x 64 multiply-adds) and
+// 2.7q for block-scaled e4m3 (128 x q x 128), but never less than a floor
+// that narrow tiles do not go below (about 350 and 600 cycles measured on
+// GB300); the operands (128 w_blocks + b_rows rows of 128 bytes) must stream
+// into shared memory; whichever is slower sets the pace, plus a fixed cost
+// per tile for the pipeline fill and the accumulator hand-off.  These are the
+// three kernel-side terms of "MoE GroupGEMM padding under expert skew",
+// "Padding is not the whole cost model" (padded MMA work, weight/activation
+// traffic, scheduling overhead).
+constexpr int64_t kSelMmaSlopeX10Bf16 = 21, kSelMmaSlopeX10Fp8 = 27;  // cycles x10 per token column
+constexpr int64_t kSelMmaFloorBf16 = 350, kSelMmaFloorFp8 = 600;      // cycles per K-block and block
 constexpr int64_t kSelLoadNum = 8, kSelLoadDen = 5;  // cycles per 128-byte row (1.6)
 constexpr int64_t kSelTileOverhead = 2500;        // per tile
 
-MG_HD int64_t tile_cost_cycles(int q, int64_t KB, int w_blocks, int b_rows) {
-  const int64_t mma = kSelMmaCyclesPerTok * q * w_blocks;
+MG_HD int64_t tile_cost_cycles(bool fp8, int q, int64_t KB, int w_blocks, int b_rows) {
+  const int64_t per_block = fp8 ? max64(kSelMmaSlopeX10Fp8 * q / 10, kSelMmaFloorFp8)
+                                : max64(kSelMmaSlopeX10Bf16 * q / 10, kSelMmaFloorBf16);
+  const int64_t mma = per_block * w_blocks;
   const int64_t load = (128 * (int64_t)w_blocks + b_rows) * kSelLoadNum / kSelLoadDen;
   return KB * max64(mma, load) + kSelTileOverhead;
 }
@@ -84,31 +89,35 @@ MG_HD int64_t tile_cost_cycles(int q, int64_t KB, int w_blocks, int b_rows) {
 // is expressed in (64 bf16 or 128 e4m3 elements).
 MG_HD int64_t sel_kblocks(bool fp8, int64_t K) { return K * (fp8 ? 1 : 2) / 128; }
 
-// Kernel families of the contiguous and masked forms.
+// Kernel families of the contiguous and masked forms: weight rows per tile
+// and whether two SMs share each MMA (cta_group::2).
 enum FwdVariant : int {
-  kFwdSingle = 0,  // one CTA: 128 weight rows x q tokens
-  kFwdDual = 1,    // one CTA: 256 weight rows x q tokens (N % 256 == 0)
-  kFwdPair = 2,    // two CTAs sharing each MMA: 256 weight rows x q tokens
+  kFwdSingle = 0,    // one CTA: 128 weight rows x q tokens
+  kFwdDual = 1,      // one CTA: 256 weight rows x q tokens (N % 256 == 0)
+  kFwdPair = 2,      // CTA pair: 256 weight rows x q tokens, q/2 staged per SM (N % 256 == 0)
+  kFwdPairDual = 3,  // CTA pair: 512 weight rows x q tokens, q/2 staged per SM (N % 512 == 0)
 };
+MG_HD int fwd_tile_rows(int variant) {
+  return variant == kFwdSingle ? 128 : variant == kFwdPairDual ? 512 : 256;
+}
 
 // Picks the token tile from the per-candidate token-tile counts
 // sum_e ceil(t_e/q).  The kernel's makespan is priced as whole waves of
-// tiles over the workers times the cost of one tile; ties go to the larger
-// tile.  A single or dual tile is one CTA's work (N/128 or N/256 tiles per
-// token tile, num_sms workers); a pair tile covers 256 weight rows on two
-// SMs, each staging half of the token rows (num_sms/2 workers).
+// tiles over the workers (CTAs, or CTA pairs) times the cost of one tile on
+// one SM; ties go to the larger tile.
 MG_HD int pick_tile(bool fp8, const int64_t (&token_tiles)[kNumTileCand], int variant, int64_t N,
                     int64_t KB, int num_sms) {
-  const int64_t NB = variant == kFwdSingle ? N / 128 : N / 256;
-  const int workers = variant == kFwdPair ? (num_sms >= 2 ? num_sms / 2 : 1) : num_sms;
-  const int w_blocks = variant == kFwdDual ? 2 : 1;
+  const bool pair = variant == kFwdPair || variant == kFwdPairDual;
+  const int64_t NB = N / fwd_tile_rows(variant);
+  const int workers = pair ? (num_sms >= 2 ? num_sms / 2 : 1) : num_sms;
+  const int w_blocks = (variant == kFwdDual || variant == kFwdPairDual) ? 2 : 1;  // per SM
   int best_q = tile_candidate(fp8, kNumTileCand - 1);
   int64_t best = -1;
   for (int i = 0; i < kNumTileCand; ++i) {
     const int q = tile_candidate(fp8, i);
     const int64_t T = token_tiles[i] * NB;
     const int64_t waves = cdiv64(T, workers);
-    const int64_t cost = waves * tile_cost_cycles(q, KB, w_blocks, variant == kFwdPair ? q / 2 : q);
+    const int64_t cost = waves * tile_cost_cycles(fp8, q, KB, w_blocks, pair ? q / 2 : q);
     if (best < 0 || cost <= best) {
       best = cost;
       best_q = q;

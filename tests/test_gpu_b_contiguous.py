@@ -12,13 +12,12 @@ from tests import gpu_util as gu
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(autouse=True, params=["dual", "single_cta", "cta_pair"])
+@pytest.fixture(autouse=True, params=["auto", "single", "dual", "pair", "pair_dual"])
 def kernel_policy(request, lib):
-    """Run every case on every kernel family: two weight blocks per CTA (the
-    default), one block per CTA, and CTA pairs.  The 256-row variants need
-    N % 256 == 0; other shapes fall back to one block per CTA."""
-    mb.set_kernel_policy({"dual": mb.POLICY_AUTO, "single_cta": mb.POLICY_SINGLE_CTA,
-                          "cta_pair": mb.POLICY_CTA_PAIR}[request.param])
+    """Run every case on every kernel family: one or two weight blocks per
+    tile, on one SM or on a CTA pair sharing each MMA.  A family whose tile
+    does not divide N falls back to a narrower one."""
+    mb.set_kernel_policy(mb.POLICIES[request.param])
     yield request.param
     mb.set_kernel_policy(mb.POLICY_AUTO)
 
