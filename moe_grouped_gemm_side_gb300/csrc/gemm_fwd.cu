@@ -94,11 +94,17 @@ struct Shared {
   int32_t q;         // token tile of full tiles
   int32_t qn_max;    // widest tile of this launch
   int32_t total;     // tiles of this launch
+  int32_t nblk;      // weight blocks per tile of this launch
   int32_t tile_qn[kInfoRing];
 };
 
 struct Tile {
   int32_t e, nb, row0, rows, qn, sf_x, sf_z;
+};
+
+template <int V>
+struct IntC {
+  static constexpr int value = V;
 };
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64_t deadline,
@@ -144,7 +150,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                const __grid_constant__ CUtensorMap tmSF, const Params p) {
   static_assert(kBlocks == 1 || kBlocks == 2, "one or two weight blocks per tile");
   constexpr int kBlockRows = kPair ? 2 * kCtaRows : kCtaRows;  // rows of one weight block (MMA M)
-  constexpr int kTileRows = kBlocks * kBlockRows;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -163,14 +168,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int32_t unit = kPair ? (int32_t)(blockIdx.x >> 1) : (int32_t)blockIdx.x;
   const int32_t n_units = kPair ? (int32_t)(gridDim.x >> 1) : (int32_t)gridDim.x;
   const uint64_t deadline = globaltimer_ns() + (uint64_t)p.wait_ns;
-  const int32_t NB = p.N / kTileRows;   // tiles per token tile
   const int32_t NB128 = p.N / kCtaRows;
   const int32_t KB = p.K / (p.fp8 ? 128 : 64);
   // TMEM: accumulator(s) at columns 0 and 256; fp8 scale words after the
   // last accumulator: weight words of each block (4 columns each), then the
   // token words (8 columns).
   const uint32_t sfa_col = 496u;
-  const uint32_t sfb_col = kBlocks == 2 ? 504u : 500u;
+  // (sfb_col: after the block-1 weight words when tiles have two blocks)
   // widest token tile: 256, but 240 where two fp8 accumulators must leave
   // room for the scale words
   const int32_t q_cap = (kBlocks == 2 && p.fp8) ? 240 : 256;
@@ -252,6 +256,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       q = pick_tile(p.fp8 != 0, tiles, variant, p.N, sel_kblocks(p.fp8 != 0, p.K), (int)gridDim.x);
     }
     q = min(q, q_cap);
+    // The two-block kernel runs one-block tiles when two-block tiles would
+    // not fill two waves of workers: with few tiles (decode) the finer
+    // split balances the SMs, which all stream weights from DRAM then.
+    int32_t nblk = kBlocks;
+    if (kBlocks == 2) {
+      int64_t tt = 0;
+      for (int32_t e = lane; e < E; e += 32) tt += cdiv64(cnt[e], q);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) tt += __shfl_xor_sync(0xffffffffu, tt, o);
+      if (tt * (p.N / (2 * kBlockRows)) < 2 * (int64_t)n_units) nblk = 1;
+    }
+    const int32_t NB = p.N / (nblk * kBlockRows);
     int32_t carry = 0, qmax = 0;
     for (int32_t b = 0; b < E; b += 32) {
       const int32_t e = b + lane;
@@ -274,6 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       sh.total = carry;
       sh.q = q;
       sh.qn_max = max(qmax, 16);
+      sh.nblk = nblk;
     }
   }
   __syncthreads();
@@ -284,8 +301,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- ring layout, identical in every CTA
   const int32_t q = sh.q;
   const int32_t total = sh.total;
+  const int32_t nblk = sh.nblk;
+  const int32_t NB = p.N / (nblk * kBlockRows);  // tiles per token tile
+  const int32_t tile_rows = nblk * kBlockRows;
+  const uint32_t sfb_col = nblk == 2 ? 504u : 500u;
+  // Runs body with the launch's block count as a compile-time constant.
+  auto with_blocks = [&](auto&& body) {
+    if constexpr (kBlocks == 2) {
+      if (nblk == 2) body(IntC<2>{});
+      else body(IntC<1>{});
+    } else {
+      body(IntC<1>{});
+    }
+  };
   // token rows this CTA stages per tile: all of them, or its half of a pair
-  const int32_t stage_bytes = kBlocks * kWTileBytes + (kPair ? sh.qn_max / 2 : sh.qn_max) * kRowBytes;
+  const int32_t stage_bytes = nblk * kWTileBytes + (kPair ? sh.qn_max / 2 : sh.qn_max) * kRowBytes;
   const int32_t sf_bytes = p.fp8 ? kSfStage : 0;
   const int32_t avail = kSmemBytes - 1024 - (int32_t)(reinterpret_cast<uintptr_t>(sf_area) -
                                                      reinterpret_cast<uintptr_t>(smem)) - 1024;
@@ -295,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(sf_area) + (uintptr_t)S * sf_bytes + 1023) & ~uintptr_t(1023));
   // accumulator sets: two (double buffered) with one block, unless fp8 scale
   // words need the columns; one with two blocks
-  const uint32_t n_acc = (kBlocks == 1 && (!p.fp8 || sh.qn_max <= 240)) ? 2u : 1u;
+  const uint32_t n_acc = (nblk == 1 && (!p.fp8 || sh.qn_max <= 240)) ? 2u : 1u;
   const uint32_t tmem = sh.tmem_base;
 
   if (warp == 0) {
@@ -316,9 +346,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int32_t t = unit, ti = 0; ok && t < total; t += n_units, ++ti) {
         const Tile tl = nxt;
         const int32_t qc = kPair ? tl.qn >> 1 : tl.qn;   // token rows staged here
-        const int32_t wy = tl.e * p.N + tl.nb * kTileRows + (int32_t)rank * kCtaRows;
+        const int32_t wy = tl.e * p.N + tl.nb * tile_rows + (int32_t)rank * kCtaRows;
         const int32_t ty = tl.row0 + (int32_t)rank * qc;
-        const uint32_t bytes = (kPair ? 2u : 1u) * (uint32_t)(kBlocks * kWTileBytes + qc * kRowBytes);
+        const uint32_t bytes = (kPair ? 2u : 1u) * (uint32_t)(nblk * kWTileBytes + qc * kRowBytes);
         for (int32_t kb = 0; kb < KB; ++kb) {
           const bool group = p.fp8 && (kb % kSfGroup) == 0;
           if (!wait_bounded(&sh.empty[stage], phase ^ 1u, deadline, &sh.abort_flag, p.status)) {
@@ -326,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           uint8_t* sw = ring + (size_t)stage * stage_bytes;
-          uint8_t* sa = sw + kBlocks * kWTileBytes;
+          uint8_t* sa = sw + nblk * kWTileBytes;
           if (leader) {
             // the stage's barrier publishes the tile's width with its bytes
             if (kb == 0) sh.tile_qn[ti % kInfoRing] = tl.qn;
@@ -345,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t bar = mapa_shared(smem_u32(&sh.full[stage]), 0);
 #pragma unroll
             for (int b = 0; b < kBlocks; ++b)
-              tma_load_2d_pair(sw + b * kWTileBytes, &tmW, bar, kx, wy + b * kBlockRows);
+              if (b < nblk) tma_load_2d_pair(sw + b * kWTileBytes, &tmW, bar, kx, wy + b * kBlockRows);
             for (int32_t r = 0; r < qc;) {
               const int32_t left = qc - r;
               const CUtensorMap* m = left >= 64 ? &tmA64 : (left >= 16 ? &tmA16 : &tmA8);
@@ -355,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
 #pragma unroll
             for (int b = 0; b < kBlocks; ++b)
-              tma_load_2d(sw + b * kWTileBytes, &tmW, &sh.full[stage], kx, wy + b * kBlockRows);
+              if (b < nblk) tma_load_2d(sw + b * kWTileBytes, &tmW, &sh.full[stage], kx, wy + b * kBlockRows);
             for (int32_t r = 0; r < qc;) {
               const bool wide = qc - r >= 64;
               tma_load_2d(sa + r * kRowBytes, wide ? &tmA64 : &tmA16, &sh.full[stage], kx, ty + r);
@@ -394,6 +424,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         return wait_bounded(&sh.full[st], ph, deadline, &sh.abort_flag, p.status) &&
                (!p.fp8 || wait_bounded(&sh.sf_ready[st], ph, deadline, &sh.abort_flag, p.status));
       };
+      with_blocks([&](auto bc) {
+      constexpr int kB = decltype(bc)::value;
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       for (int32_t t = unit, ti = 0; ok && t < total; t += n_units, ++ti) {
@@ -412,19 +444,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t idesc0 = p.fp8 ? idesc_mxf8(kBlockRows, qn) : idesc_bf16(kBlockRows, qn, 0, 0);
         for (int32_t kb = 0; kb < KB; ++kb) {
           uint8_t* sw = ring + (size_t)stage * stage_bytes;
-          const uint32_t a0 = smem_u32(sw), b0 = smem_u32(sw + kBlocks * kWTileBytes);
+          const uint32_t a0 = smem_u32(sw), b0 = smem_u32(sw + kB * kWTileBytes);
           const uint32_t sid = (uint32_t)(kb & 3);
           const uint32_t idesc = p.fp8 ? (idesc0 | (sid << 4) | (sid << 29)) : idesc0;
           if (p.fp8 && sid == 0) {
             const uint32_t sfs = smem_u32(sf_area + (size_t)stage * kSfStage);
             if constexpr (kPair) {
               tmem_cp_32x128b_x4_pair(tmem + sfa_col, desc_sf_32x16(sfs + kSfRaw));
-              if (kBlocks == 2) tmem_cp_32x128b_x4_pair(tmem + sfa_col + 4, desc_sf_32x16(sfs + kSfW1));
+              if (kB == 2) tmem_cp_32x128b_x4_pair(tmem + sfa_col + 4, desc_sf_32x16(sfs + kSfW1));
               tmem_cp_32x128b_x4_pair(tmem + sfb_col, desc_sf_32x16(sfs + kSfRaw + 512));
               if (qn > 128) tmem_cp_32x128b_x4_pair(tmem + sfb_col + 4, desc_sf_32x16(sfs + kSfRaw + 1024));
             } else {
               tmem_cp_32x128b_x4(tmem + sfa_col, desc_sf_32x16(sfs + kSfRaw));
-              if (kBlocks == 2) tmem_cp_32x128b_x4(tmem + sfa_col + 4, desc_sf_32x16(sfs + kSfW1));
+              if (kB == 2) tmem_cp_32x128b_x4(tmem + sfa_col + 4, desc_sf_32x16(sfs + kSfW1));
               tmem_cp_32x128b_x4(tmem + sfb_col, desc_sf_32x16(sfs + kSfRaw + 512));
               if (qn > 128) tmem_cp_32x128b_x4(tmem + sfb_col + 4, desc_sf_32x16(sfs + kSfRaw + 1024));
             }
@@ -432,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           auto kstep = [&](int ks, uint32_t accum) {
             const uint64_t bd = desc_kmajor_sw128(b0 + ks * 32);
 #pragma unroll
-            for (int b = 0; b < kBlocks; ++b) {
+            for (int b = 0; b < kB; ++b) {
               const uint64_t ad = desc_kmajor_sw128(a0 + b * kWTileBytes + ks * 32);
               const uint32_t d = d0 + b * kAccStride;
               if constexpr (kPair) {
@@ -465,6 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           acc_phase ^= 1u;
         }
       }
+      });
       // all tcgen05 work of the CTA (pair) completes before TMEM is released
       if constexpr (kPair) mma_commit_pair(&sh.drain, 0x3);
       else mma_commit(&sh.drain);
@@ -486,12 +519,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t ready0 = mapa_shared(smem_u32(&sh.sf_ready[0]), 0);
       // weight scales of a tile's blocks: lane l holds K-blocks l + 32 i;
       // the next tile's are fetched while the current tile streams
-      uint32_t wsf[kBlocks][4], wsf_nxt[kBlocks][4];
-      auto fetch_wsf = [&](int32_t t, uint32_t (&w)[kBlocks][4]) {
+      with_blocks([&](auto bc) {
+      constexpr int kB = decltype(bc)::value;
+      uint32_t wsf[kB][4], wsf_nxt[kB][4];
+      auto fetch_wsf = [&](int32_t t, uint32_t (&w)[kB][4]) {
         const Tile tl = decode_tile(t, tpre, cnt, rowbase, E, NB, q, p.masked);
 #pragma unroll
-        for (int b = 0; b < kBlocks; ++b) {
-          const int32_t nb128 = (tl.nb * kTileRows + b * kBlockRows) / kCtaRows + (int32_t)rank;
+        for (int b = 0; b < kB; ++b) {
+          const int32_t nb128 = (tl.nb * tile_rows + b * kBlockRows) / kCtaRows + (int32_t)rank;
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int32_t kb = (int32_t)lane + 32 * i;
@@ -502,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (unit < total) fetch_wsf(unit, wsf_nxt);
       for (int32_t t = unit; ok && t < total; t += n_units) {
 #pragma unroll
-        for (int b = 0; b < kBlocks; ++b)
+        for (int b = 0; b < kB; ++b)
 #pragma unroll
           for (int i = 0; i < 4; ++i) wsf[b][i] = wsf_nxt[b][i];
         for (int32_t kb = 0; kb < KB; ++kb) {
@@ -514,8 +549,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint8_t* sfs = sf_area + (size_t)stage * kSfStage;
             // lane l, column c of a word block holds the word of row c*32 + l
             sf_build_words(sfs, sf_weight_word(wsf[0], kb, KB), lane);
-            if (kBlocks == 2) {
-              const uint32_t w1 = sf_weight_word(wsf[kBlocks - 1], kb, KB);
+            if (kB == 2) {
+              const uint32_t w1 = sf_weight_word(wsf[kB - 1], kb, KB);
               *reinterpret_cast<uint4*>(sfs + kSfW1 + lane * 16) = make_uint4(w1, w1, w1, w1);
             }
             fence_proxy_async_smem();
@@ -532,6 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      });
     }
   } else {
     // ================================================= epilogue
@@ -539,23 +575,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int32_t half = warp >= kSfWarp ? 1 : 0;
     const uint32_t acc_empty0 = mapa_shared(smem_u32(&sh.acc_empty[0]), 0);
     const bool odd = (lane & 1u) != 0;
+    with_blocks([&](auto bc) {
+    constexpr int kB = decltype(bc)::value;
     uint32_t acc = 0, acc_phase = 0;
     for (int32_t t = unit; S > 0 && t < total; t += n_units) {
       const Tile tl = decode_tile(t, tpre, cnt, rowbase, E, NB, q, p.masked);
       if (!warp_wait(&sh.acc_full[acc], acc_phase, deadline, &sh.abort_flag, p.status)) break;
       tc_fence_after();
       // this thread's output column of block 0; block b is b * kBlockRows further
-      const int32_t n = tl.nb * kTileRows + (int32_t)(rank * kCtaRows + quad * 32 + lane);
+      const int32_t n = tl.nb * tile_rows + (int32_t)(rank * kCtaRows + quad * 32 + lane);
       const uint32_t taddr = tmem + ((quad * 32u) << 16) + acc * kAccStride;
       __nv_bfloat16* dpair = p.D + (int64_t)tl.row0 * p.N + (n & ~1);
       // the two warps of a lane quadrant take alternate 16-token chunks
       for (int32_t c0 = 16 * half; c0 < tl.qn; c0 += 32) {
-        uint32_t r[kBlocks][16];
+        uint32_t r[kB][16];
 #pragma unroll
-        for (int b = 0; b < kBlocks; ++b) tmem_ld16(taddr + b * kAccStride + (uint32_t)c0, r[b]);
+        for (int b = 0; b < kB; ++b) tmem_ld16(taddr + b * kAccStride + (uint32_t)c0, r[b]);
         tmem_ld_wait();
 #pragma unroll
-        for (int b = 0; b < kBlocks; ++b) tmem_regs_ready(r[b]);
+        for (int b = 0; b < kB; ++b) tmem_regs_ready(r[b]);
         // Lanes 2j and 2j+1 hold adjacent output columns.  One exchange per
         // pair of tokens gives the even lane both columns of token i and the
         // odd lane both columns of token i+1, so each store writes 4 bytes.
@@ -563,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 16; i += 2) {
           const int32_t row = c0 + i + (odd ? 1 : 0);
 #pragma unroll
-          for (int b = 0; b < kBlocks; ++b) {
+          for (int b = 0; b < kB; ++b) {
             const float mine = __uint_as_float(odd ? r[b][i + 1] : r[b][i]);
             const float recv = __shfl_xor_sync(0xffffffffu, __uint_as_float(odd ? r[b][i] : r[b][i + 1]), 1);
             const __nv_bfloat162 v = odd ? __floats2bfloat162_rn(recv, mine) : __floats2bfloat162_rn(mine, recv);
@@ -583,6 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc_phase ^= 1u;
       }
     }
+    });
   }
 
   __syncthreads();
