@@ -42,6 +42,38 @@ def ptr(t):
     return None if t is None else t.data_ptr()
 
 
+# DRAM bytes per step measured by ncu (dram__bytes_read.sum +
+# dram__bytes_write.sum over the step's GEMM launches), valid only for the
+# kernel sources they were taken with.
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
+KERNEL_SOURCES = {
+    "fwd": ["gemm_fwd.cu", "common.cuh", "sched.cuh"],
+    "kg": ["gemm_kgrouped.cu", "common.cuh"],
+}
+
+
+def kernel_sources_sha(kind):
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kind]:
+        with open(os.path.join(ROOT, "moe_grouped_gemm_side_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def measured_traffic(workload, kind):
+    """ncu DRAM bytes of one step of `workload`, or None when none were taken
+    with the current kernel sources."""
+    try:
+        with open(TRAFFIC_FILE) as fh:
+            rec = json.load(fh).get(workload)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("sources_sha256") != kernel_sources_sha(kind):
+        return None
+    return rec.get("bytes_per_step")
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -229,11 +261,12 @@ class Contiguous:
         if t_compute >= t_mem:
             ach = flops / (ms * 1e-3) / 1e12
             return {"bound": "tensor", "achieved": ach, "peak": tensor_peak, "unit": "TFLOP/s",
-                    "frac": ach / tensor_peak, "traffic": None,
+                    "frac": ach / tensor_peak, "traffic": measured_traffic(self.name, "fwd"),
                     "peak_source": f"{peaks['source']} bf16 burst x{FP8_OVER_BF16 if self.fp8 else 1.0:g}"}
         ach = byts / (ms * 1e-3) / 1e9
         return {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": ach / peaks["hbm_gbs"], "traffic": None, "peak_source": f"{peaks['source']} copy"}
+                "frac": ach / peaks["hbm_gbs"], "traffic": measured_traffic(self.name, "fwd"),
+                "peak_source": f"{peaks['source']} copy"}
 
     def config(self):
         d = {"workload": self.name, "form": "contiguous", "experts": self.E, "assignments": self.U,
@@ -330,7 +363,8 @@ class Masked:
         ms = sum(per_gemm_ms)
         ach = self.bytes_alg() / (ms * 1e-3) / 1e9
         return {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": ach / peaks["hbm_gbs"], "traffic": None, "peak_source": f"{peaks['source']} copy"}
+                "frac": ach / peaks["hbm_gbs"], "traffic": measured_traffic(self.name, "fwd"),
+                "peak_source": f"{peaks['source']} copy"}
 
     def config(self):
         return {"workload": self.name, "form": "masked", "experts": self.E, "M_max": self.M,
@@ -404,7 +438,8 @@ class KGrouped:
     def roofline(self, per_gemm_ms, peaks):
         ach = self.flops() / (sum(per_gemm_ms) * 1e-3) / 1e12
         return {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": ach / peaks["bf16_tflops"], "traffic": None, "peak_source": f"{peaks['source']} bf16 burst"}
+                "frac": ach / peaks["bf16_tflops"], "traffic": measured_traffic(self.name, "kg"),
+                "peak_source": f"{peaks['source']} bf16 burst"}
 
     def config(self):
         return {"workload": self.name, "form": "kgrouped", "experts": self.E, "tokens": self.U,
