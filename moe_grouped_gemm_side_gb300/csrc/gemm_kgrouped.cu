@@ -8,15 +8,22 @@
 // Tokens are packed by expert with no alignment, so both operands arrive
 // MN-major: a TMA box is 64 tokens x 64 contiguous columns of dY or X, and
 // the MMA reads them through transposed (MN-major) descriptors.  A tile is a
-// 128 x 256 block of dW; its main loop walks the expert's tokens 64 at a
-// time.  The last, partial block of an expert may hold the next expert's
-// tokens: the MMA warp zeroes those rows of the staged operands in shared
-// memory and issues only the 16-token MMA steps that still hold valid tokens.
+// kBlocks*128 x 256 block of dW (two 128-row blocks when N allows: the token
+// block of X is then shared by two MMAs, 1.5x the multiply-adds per staged
+// byte); its main loop walks the expert's tokens 64 at a time.  The last,
+// partial block of an expert may hold the next expert's tokens: warp 6
+// zeroes those rows of the staged operands in shared memory, and the MMA
+// thread issues only the 16-token steps that still hold valid tokens.
 //
 // Tiles of all experts are ordered by descending token count and dealt to
 // the persistent CTAs in a snake order, so every CTA receives a similar mix
 // of long and short tiles.  Experts with no tokens produce zero tiles that
 // the epilogue writes without any load or MMA.
+//
+// CTA = 11 warps: warp 0 issues TMA; warp 1 owns TMEM and one of its threads
+// issues every tcgen05.mma (nothing else runs between MMAs, so the tensor
+// pipe's short queue stays fed); warps 2-5 and 7-10 drain the accumulators
+// (two warps per TMEM lane quadrant); warp 6 zeroes the tail rows.
 #include "common.cuh"
 #include "mg_internal.h"
 #include "sched.cuh"
@@ -24,13 +31,14 @@
 namespace mg {
 namespace kg {
 
-constexpr int kThreads = 192;
-constexpr int kMaxStages = 6;
-constexpr int kBlockT = 64;          // tokens per stage
+constexpr int kThreads = 352;
+constexpr int kFixWarp = 6;
+constexpr int kEpiWarps = 8;
+constexpr int kMaxStages = 8;
+constexpr int kBlockT = 64;               // tokens per stage
 constexpr int kBoxBytes = kBlockT * 128;  // one 64 x 64 bf16 box
-constexpr int kTileM = 128;          // dW rows per tile
-constexpr int kTileN = 256;          // dW columns per tile (max)
-constexpr int kStageBytes = (kTileM / 64 + kTileN / 64) * kBoxBytes;  // 48 KB
+constexpr int kBlockM = 128;              // dW rows per block (MMA M)
+constexpr int kTileN = 256;               // dW columns per tile (max, MMA N)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccStride = 256;
 constexpr int kSmemBytes = 227 * 1024;
@@ -46,6 +54,7 @@ struct Params {
 
 struct Shared {
   uint64_t full[kMaxStages];
+  uint64_t fixed[kMaxStages];  // warp 6 has zeroed the stage's tail rows (if any)
   uint64_t empty[kMaxStages];
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
@@ -89,9 +98,15 @@ __device__ __forceinline__ int32_t snake_pos(int32_t r, int32_t total) {
   return pos < total ? (int32_t)pos : -2;
 }
 
+template <int kBlocks>
 __global__ void __launch_bounds__(kThreads, 1)
     kg_kernel(const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmX,
               const Params p) {
+  static_assert(kBlocks == 1 || kBlocks == 2, "one or two 128-row blocks per tile");
+  constexpr int kTileM = kBlocks * kBlockM;                              // dW rows per tile
+  constexpr int kBoxesY = kTileM / 64;                                   // dY boxes per stage
+  constexpr int kStageBytes = (kBoxesY + kTileN / 64) * kBoxBytes;       // 48 or 64 KB
+  constexpr uint32_t kNAcc = kBlocks == 1 ? 2u : 1u;                     // accumulator sets
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -111,11 +126,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kMaxStages; ++i) {
       mbar_init(&sh.full[i], 1);
+      mbar_init(&sh.fixed[i], 1);
       mbar_init(&sh.empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh.acc_full[i], 1);
-      mbar_init(&sh.acc_empty[i], 4 * 32);
+      mbar_init(&sh.acc_empty[i], kEpiWarps);  // one arrival per epilogue warp
     }
     mbar_init(&sh.drain, 1);
     sh.abort_flag = 0;
@@ -182,6 +198,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                      reinterpret_cast<uintptr_t>(smem));
   const int32_t S = min(kMaxStages, avail / kStageBytes);
   const uint32_t tmem = sh.tmem_base;
+  auto next_stage = [&](uint32_t& stage, uint32_t& phase) {
+    if (++stage == (uint32_t)S) {
+      stage = 0;
+      phase ^= 1u;
+    }
+  };
 
   if (warp == 0) {
     // ================================================= TMA producer
@@ -198,26 +220,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Tile tl = decode_tile(pos, order, cnt, tokoff, NBk, NT, p.K);
         if (tl.cnt == 0) continue;
         const int32_t nkb = (tl.cnt + kBlockT - 1) / kBlockT;
-        const uint32_t bytes = (uint32_t)(2 + tl.w / 64) * kBoxBytes;
+        const uint32_t bytes = (uint32_t)(kBoxesY + tl.w / 64) * kBoxBytes;
         for (int32_t kb = 0; kb < nkb; ++kb) {
           if (!wait_bounded(&sh.empty[stage], phase ^ 1u, deadline, &sh.abort_flag, p.status)) {
             ok = false;
             break;
           }
           uint8_t* sa = ring + (size_t)stage * kStageBytes;
-          uint8_t* sb = sa + 2 * kBoxBytes;
+          uint8_t* sb = sa + kBoxesY * kBoxBytes;
           mbar_arrive_expect_tx(&sh.full[stage], bytes);
           const int32_t y = tl.tok0 + kb * kBlockT;
 #pragma unroll
-          for (int i = 0; i < 2; ++i)
+          for (int i = 0; i < kBoxesY; ++i)
             tma_load_2d(sa + i * kBoxBytes, &tmY, &sh.full[stage], tl.mb * kTileM + i * 64, y);
           for (int i = 0; i < tl.w / 64; ++i)
             tma_load_2d(sb + i * kBoxBytes, &tmX, &sh.full[stage], tl.nb * kTileN + i * 64, y);
           ++issued;
-          if (++stage == (uint32_t)S) {
-            stage = 0;
-            phase ^= 1u;
-          }
+          next_stage(stage, phase);
         }
       }
       const uint64_t dl = globaltimer_ns() + kDrainNs;
@@ -225,8 +244,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         wait_drain(&sh.full[i % S], (uint32_t)((i / S) & 1), dl);
     }
   } else if (warp == 1) {
-    // ================================================= MMA issuer
-    if (S > 0) {
+    // ================================================= MMA issuer (one thread)
+    if (lane == 0 && S > 0) {
+      auto ready = [&](uint32_t st, uint32_t ph) {
+        return wait_bounded(&sh.full[st], ph, deadline, &sh.abort_flag, p.status) &&
+               wait_bounded(&sh.fixed[st], ph, deadline, &sh.abort_flag, p.status);
+      };
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       for (int32_t r = 0; ok; ++r) {
@@ -236,96 +259,133 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Tile tl = decode_tile(pos, order, cnt, tokoff, NBk, NT, p.K);
         if (tl.cnt == 0) continue;
         const int32_t nkb = (tl.cnt + kBlockT - 1) / kBlockT;
-        if (!warp_wait(&sh.acc_empty[acc], acc_phase ^ 1u, deadline, &sh.abort_flag, p.status)) break;
+        if (!wait_bounded(&sh.acc_empty[acc], acc_phase ^ 1u, deadline, &sh.abort_flag, p.status)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem + acc * kAccStride;
-        const uint32_t idesc = idesc_bf16(kTileM, (uint32_t)tl.w, 1, 1);
-        const int32_t nbox = 2 + tl.w / 64;
+        const uint32_t d0 = tmem + acc * kAccStride;  // block b accumulates at d0 + b * 256
+        const uint32_t idesc = idesc_bf16(kBlockM, (uint32_t)tl.w, 1, 1);
+        // The wait for stage kb+1 sits between the third and the fourth
+        // 16-token step of stage kb, so the tensor pipe holds queued work
+        // while the thread waits.
+        if (!ready(stage, phase)) break;
+        for (int32_t kb = 0; kb < nkb; ++kb) {
+          const uint32_t a0 = smem_u32(ring + (size_t)stage * kStageBytes);
+          const uint32_t b0 = a0 + kBoxesY * kBoxBytes;
+          const int32_t rem = tl.cnt - kb * kBlockT;
+          const int nks = rem >= kBlockT ? 4 : (rem + 15) >> 4;
+          auto kstep = [&](int ks) {
+            const uint64_t bd = desc_mnmajor_sw128(b0 + ks * 2048, kBoxBytes);
+#pragma unroll
+            for (int b = 0; b < kBlocks; ++b) {
+              const uint64_t ad = desc_mnmajor_sw128(a0 + b * 2 * kBoxBytes + ks * 2048, kBoxBytes);
+              mma_f16(d0 + b * kAccStride, ad, bd, idesc, (kb | ks) != 0 ? 1u : 0u);
+            }
+          };
+          for (int ks = 0; ks < nks && ks < 3; ++ks) kstep(ks);
+          uint32_t nstage = stage, nphase = phase;
+          next_stage(nstage, nphase);
+          if (kb + 1 < nkb && !ready(nstage, nphase)) ok = false;
+          if (nks == 4) kstep(3);
+          mma_commit(&sh.empty[stage]);
+          stage = nstage;
+          phase = nphase;
+          if (!ok) break;
+        }
+        if (!ok) break;
+        mma_commit(&sh.acc_full[acc]);
+        if (++acc == kNAcc) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      // all tcgen05 work of this CTA completes before TMEM is released
+      mma_commit(&sh.drain);
+      wait_drain(&sh.drain, 0, globaltimer_ns() + kDrainNs);
+    }
+    __syncwarp();
+  } else if (warp == kFixWarp) {
+    // ================================================= tail rows
+    // Every stage, in order: once it has landed, zero the rows of a partial
+    // token block that belong to no token of the expert (up to the next
+    // multiple of 16, the last rows an MMA step reads), then mark it fixed.
+    if (S > 0) {
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (int32_t r = 0; ok; ++r) {
+        const int32_t pos = snake_pos(r, total);
+        if (pos == -1) break;
+        if (pos < 0) continue;
+        const Tile tl = decode_tile(pos, order, cnt, tokoff, NBk, NT, p.K);
+        if (tl.cnt == 0) continue;
+        const int32_t nkb = (tl.cnt + kBlockT - 1) / kBlockT;
+        const int32_t nbox = kBoxesY + tl.w / 64;
         for (int32_t kb = 0; kb < nkb; ++kb) {
           if (!warp_wait(&sh.full[stage], phase, deadline, &sh.abort_flag, p.status)) {
             ok = false;
             break;
           }
-          tc_fence_after();
-          uint8_t* sa = ring + (size_t)stage * kStageBytes;
-          uint8_t* sb = sa + 2 * kBoxBytes;
           const int32_t rem = tl.cnt - kb * kBlockT;
-          int32_t nks = 4;
           if (rem < kBlockT) {
-            nks = (rem + 15) >> 4;
-            const int32_t z0 = rem, z1 = nks * 16;  // rows [z0, z1) belong to no token of e
+            const int32_t z0 = rem, z1 = ((rem + 15) >> 4) * 16;
             if (z1 > z0) {
+              uint8_t* sa = ring + (size_t)stage * kStageBytes;
               const int32_t per_box = (z1 - z0) * 8;  // 16-byte chunks
               for (int32_t i = lane; i < per_box * nbox; i += 32) {
                 const int32_t box = i / per_box, c = i - box * per_box;
-                *reinterpret_cast<uint4*>(sa + box * kBoxBytes + z0 * 128 + c * 16) =
-                    make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(sa + box * kBoxBytes + z0 * 128 + c * 16) = make_uint4(0u, 0u, 0u, 0u);
               }
               fence_proxy_async_smem();
             }
-            __syncwarp();
-          }
-          if (lane == 0) {
-            const uint32_t a0 = smem_u32(sa), b0 = smem_u32(sb);
-            for (int ks = 0; ks < nks; ++ks) {
-              const uint64_t ad = desc_mnmajor_sw128(a0 + ks * 2048, kBoxBytes);
-              const uint64_t bd = desc_mnmajor_sw128(b0 + ks * 2048, kBoxBytes);
-              mma_f16(d_tmem, ad, bd, idesc, (kb | ks) != 0 ? 1u : 0u);
-            }
-            mma_commit(&sh.empty[stage]);
           }
           __syncwarp();
-          if (++stage == (uint32_t)S) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-        if (!ok) break;
-        if (lane == 0) mma_commit(&sh.acc_full[acc]);
-        __syncwarp();
-        if (++acc == 2) {
-          acc = 0;
-          acc_phase ^= 1u;
+          if (lane == 0) mbar_arrive(&sh.fixed[stage]);
+          next_stage(stage, phase);
         }
       }
     }
-    if (lane == 0) {
-      mma_commit(&sh.drain);
-      wait_drain(&sh.drain, 0, globaltimer_ns() + kDrainNs);
-    }
-    __syncwarp();
   } else {
     // ================================================= epilogue
     const uint32_t quad = warp & 3u;
+    const int32_t half = warp >= kFixWarp ? 1 : 0;
     uint32_t acc = 0, acc_phase = 0;
     for (int32_t r = 0; S > 0; ++r) {
       const int32_t pos = snake_pos(r, total);
       if (pos == -1) break;
       if (pos < 0) continue;
       const Tile tl = decode_tile(pos, order, cnt, tokoff, NBk, NT, p.K);
-      const int32_t row = tl.mb * kTileM + (int32_t)(quad * 32 + lane);
-      float* dst = p.dW + ((int64_t)tl.e * p.N + row) * p.K + tl.nb * kTileN;
       if (tl.cnt == 0) {
-        for (int32_t c = 0; c < tl.w; c += 4)
-          *reinterpret_cast<float4*>(dst + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+        // empty expert: dW = 0, split over the eight warps
+#pragma unroll
+        for (int b = 0; b < kBlocks; ++b) {
+          const int32_t row = tl.mb * kTileM + b * kBlockM + (int32_t)(quad * 32 + lane);
+          float* dst = p.dW + ((int64_t)tl.e * p.N + row) * p.K + tl.nb * kTileN;
+          for (int32_t c = 4 * half; c < tl.w; c += 8)
+            *reinterpret_cast<float4*>(dst + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
         continue;
       }
       if (!warp_wait(&sh.acc_full[acc], acc_phase, deadline, &sh.abort_flag, p.status)) break;
       tc_fence_after();
-      const uint32_t taddr = tmem + ((quad * 32u) << 16) + acc * kAccStride;
-      for (int32_t c0 = 0; c0 < tl.w; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld32(taddr + (uint32_t)c0, v);
-        tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; i += 4)
-          *reinterpret_cast<float4*>(dst + c0 + i) =
-              make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
-                          __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+      for (int b = 0; b < kBlocks; ++b) {
+        const int32_t row = tl.mb * kTileM + b * kBlockM + (int32_t)(quad * 32 + lane);
+        float* dst = p.dW + ((int64_t)tl.e * p.N + row) * p.K + tl.nb * kTileN;
+        const uint32_t taddr = tmem + ((quad * 32u) << 16) + acc * kAccStride + b * kAccStride;
+        // the two warps of a lane quadrant take alternate 32-column chunks
+        for (int32_t c0 = 32 * half; c0 < tl.w; c0 += 64) {
+          uint32_t v[32];
+          tmem_ld32(taddr + (uint32_t)c0, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4*>(dst + c0 + i) =
+                make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+                            __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+        }
       }
       tc_fence_before();
-      mbar_arrive(&sh.acc_empty[acc]);
-      if (++acc == 2) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.acc_empty[acc]);
+      if (++acc == kNAcc) {
         acc = 0;
         acc_phase ^= 1u;
       }
@@ -339,20 +399,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-}  // namespace kg
-
-cudaError_t launch_kgrouped(const KgArgs& a, cudaStream_t s) {
+template <int kBlocks>
+cudaError_t launch(const KgArgs& a, cudaStream_t s) {
   static bool attr_done[64] = {};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 64 && !attr_done[dev]) {
-    err = cudaFuncSetAttribute(kg::kg_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kg::kSmemBytes);
+    err = cudaFuncSetAttribute(kg_kernel<kBlocks>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (err != cudaSuccess) return err;
     attr_done[dev] = true;
   }
-  kg::Params p;
+  Params p;
   p.counts = a.counts;
   p.dW = a.dW;
   p.status = a.status;
@@ -361,8 +419,15 @@ cudaError_t launch_kgrouped(const KgArgs& a, cudaStream_t s) {
   p.N = a.N;
   p.K = a.K;
   p.T_cap = a.T_cap;
-  kg::kg_kernel<<<num_sms_current_device(), kg::kThreads, kg::kSmemBytes, s>>>(a.tmY, a.tmX, p);
+  kg_kernel<kBlocks><<<num_sms_current_device(), kThreads, kSmemBytes, s>>>(a.tmY, a.tmX, p);
   return cudaGetLastError();
+}
+
+}  // namespace kg
+
+// Two 128-row blocks of dW per tile when N allows it.
+cudaError_t launch_kgrouped(const KgArgs& a, cudaStream_t s) {
+  return a.N % 256 == 0 ? kg::launch<2>(a, s) : kg::launch<1>(a, s);
 }
 
 }  // namespace mg

@@ -47,9 +47,11 @@ def check_dw(got, ref):
         assert np.all(err[~zero] <= 1e-2 * m[~zero]), f"expert {e}: worst {np.max(err[~zero] / m[~zero])}"
 
 
-def test_integer_exact(lib, cuda):
+@pytest.mark.parametrize("N", [256, 384, 512])
+def test_integer_exact(lib, cuda, N):
+    """N=384 runs one 128-row block of dW per tile, 256 and 512 two."""
     counts = [5, 0, 64, 17, 100, 1]
-    got, ref, status = run_kgrouped(counts, 256, 256, integer=True)
+    got, ref, status = run_kgrouped(counts, N, 256, integer=True)
     assert status == 0
     assert np.array_equal(got, ref)
 
