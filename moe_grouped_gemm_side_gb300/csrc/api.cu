@@ -316,6 +316,10 @@ mg_status kgemm_grouped(const void* dY, const void* X, float* dW, const int32_t*
   st = encode_2d(&a.tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, X, (uint64_t)K, (uint64_t)T_cap, 64,
                  64, CU_TENSOR_MAP_SWIZZLE_128B);
   if (st != MG_OK) return st;
+  // dW as [E*N, K] fp32, stored by the epilogue in 32 x 32 boxes
+  st = encode_2d(&a.tmDW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dW, (uint64_t)K, (uint64_t)E * N, 32, 32,
+                 CU_TENSOR_MAP_SWIZZLE_128B);
+  if (st != MG_OK) return st;
   return from_cuda(launch_kgrouped(a, static_cast<cudaStream_t>(stream)));
 }
 

@@ -39,6 +39,7 @@ constexpr int kBlockT = 64;               // tokens per stage
 constexpr int kBoxBytes = kBlockT * 128;  // one 64 x 64 bf16 box
 constexpr int kBlockM = 128;              // dW rows per block (MMA M)
 constexpr int kTileN = 256;               // dW columns per tile (max, MMA N)
+constexpr int kOutBox = 32 * 32 * 4;      // epilogue staging box: 32 rows x 32 fp32
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccStride = 256;
 constexpr int kSmemBytes = 227 * 1024;
@@ -101,7 +102,7 @@ __device__ __forceinline__ int32_t snake_pos(int32_t r, int32_t total) {
 template <int kBlocks>
 __global__ void __launch_bounds__(kThreads, 1)
     kg_kernel(const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmX,
-              const Params p) {
+              const __grid_constant__ CUtensorMap tmDW, const Params p) {
   static_assert(kBlocks == 1 || kBlocks == 2, "one or two 128-row blocks per tile");
   constexpr int kTileM = kBlocks * kBlockM;                              // dW rows per tile
   constexpr int kBoxesY = kTileM / 64;                                   // dY boxes per stage
@@ -115,8 +116,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   int32_t* cnt = reinterpret_cast<int32_t*>(smem + ((sizeof(Shared) + 15) & ~size_t(15)));
   int32_t* tokoff = cnt + E;
   int32_t* order = tokoff + E;
-  uint8_t* ring = reinterpret_cast<uint8_t*>(
+  // epilogue staging: one 32 x 32 fp32 box (4 KB, 128-byte swizzle) per warp
+  uint8_t* stage_out = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(order + E) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring = stage_out + kEpiWarps * kOutBox;
 
   const uint32_t warp = warp_id(), lane = lane_id();
   const uint64_t deadline = globaltimer_ns() + (uint64_t)p.wait_ns;
@@ -196,6 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int32_t total = sh.n_valid * NT;
   const int32_t avail = kSmemBytes - 1024 - (int32_t)(reinterpret_cast<uintptr_t>(ring) -
                                                      reinterpret_cast<uintptr_t>(smem));
+  if (threadIdx.x == 0 && avail < kStageBytes) set_status(p.status, MG_ERR_UNSUPPORTED);
   const int32_t S = min(kMaxStages, avail / kStageBytes);
   const uint32_t tmem = sh.tmem_base;
   auto next_stage = [&](uint32_t& stage, uint32_t& phase) {
@@ -210,6 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && S > 0) {
       tma_prefetch_desc(&tmY);
       tma_prefetch_desc(&tmX);
+      tma_prefetch_desc(&tmDW);
       uint32_t stage = 0, phase = 0;
       int64_t issued = 0;
       bool ok = true;
@@ -346,6 +351,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================================================= epilogue
     const uint32_t quad = warp & 3u;
     const int32_t half = warp >= kFixWarp ? 1 : 0;
+    uint8_t* out_box = stage_out + ((warp - 2) - (half ? 1 : 0)) * kOutBox;  // warps 2-5, 7-10 -> 0-7
+    bool out_pending = false;
     uint32_t acc = 0, acc_phase = 0;
     for (int32_t r = 0; S > 0; ++r) {
       const int32_t pos = snake_pos(r, total);
@@ -367,19 +374,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
 #pragma unroll
       for (int b = 0; b < kBlocks; ++b) {
-        const int32_t row = tl.mb * kTileM + b * kBlockM + (int32_t)(quad * 32 + lane);
-        float* dst = p.dW + ((int64_t)tl.e * p.N + row) * p.K + tl.nb * kTileN;
+        const int32_t row0 = tl.mb * kTileM + b * kBlockM + (int32_t)(quad * 32);  // the warp's 32 rows
         const uint32_t taddr = tmem + ((quad * 32u) << 16) + acc * kAccStride + b * kAccStride;
-        // the two warps of a lane quadrant take alternate 32-column chunks
+        // The two warps of a lane quadrant take alternate 32-column chunks.
+        // Each chunk goes through this warp's staging box and a TMA store:
+        // full 128-byte rows reach L2, instead of one 16-byte piece of 32
+        // different rows per store instruction.
         for (int32_t c0 = 32 * half; c0 < tl.w; c0 += 64) {
           uint32_t v[32];
           tmem_ld32(taddr + (uint32_t)c0, v);
           tmem_ld_wait();
+          if (lane == 0 && out_pending) bulk_wait_read_all();  // the box is free again
+          __syncwarp();
+          // row `lane`, 16-byte chunk j at position j ^ (lane & 7) (128-byte swizzle)
 #pragma unroll
-          for (int i = 0; i < 32; i += 4)
-            *reinterpret_cast<float4*>(dst + c0 + i) =
-                make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
-                            __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<float4*>(out_box + lane * 128 + ((j ^ (int)(lane & 7u)) * 16)) =
+                make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                            __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmDW, out_box, tl.nb * kTileN + c0, tl.e * p.N + row0);
+            bulk_commit_group();
+          }
+          out_pending = true;
         }
       }
       tc_fence_before();
@@ -390,6 +409,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc_phase ^= 1u;
       }
     }
+    // every store has landed before the CTA exits
+    if (lane == 0 && out_pending) bulk_wait_all();
+    __syncwarp();
   }
 
   __syncthreads();
@@ -419,7 +441,7 @@ cudaError_t launch(const KgArgs& a, cudaStream_t s) {
   p.N = a.N;
   p.K = a.K;
   p.T_cap = a.T_cap;
-  kg_kernel<kBlocks><<<num_sms_current_device(), kThreads, kSmemBytes, s>>>(a.tmY, a.tmX, p);
+  kg_kernel<kBlocks><<<num_sms_current_device(), kThreads, kSmemBytes, s>>>(a.tmY, a.tmX, a.tmDW, p);
   return cudaGetLastError();
 }
 

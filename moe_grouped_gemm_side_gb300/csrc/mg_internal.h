@@ -37,7 +37,7 @@ struct KgArgs {
   float* dW = nullptr;
   int32_t* status = nullptr;
   int64_t wait_ns = 0;
-  CUtensorMap tmY{}, tmX{};
+  CUtensorMap tmY{}, tmX{}, tmDW{};
 };
 cudaError_t launch_kgrouped(const KgArgs& a, cudaStream_t s);
 
