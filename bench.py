@@ -143,13 +143,19 @@ class ClockSampler:
 
 
 def dist_setup():
+    """One process per GPU (torchrun env).  The ranks are independent
+    replicas; the only collectives are the timing barrier and the max of the
+    timed spans (NCCL on GPUs, gloo without)."""
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if ws > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group("gloo")
     elif torch.cuda.is_available():
         torch.cuda.set_device(local)
     return ws, rank, local
@@ -165,9 +171,16 @@ def max_over_ranks(x, ws):
     if ws == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def weak_scaling_value(units_per_rank, ws, ms_max):
+    """Whole-job throughput: the units every rank processed over the slowest
+    rank's span (per-rank work fixed as ranks are added)."""
+    return ws * units_per_rank / (ms_max * 1e-3)
 
 
 # ------------------------------------------------------------------ workloads
@@ -546,7 +559,7 @@ def run_ours(args):
                 for g in range(n_g)]
     if int(w.status.item()) != 0:
         raise RuntimeError("device status " + mb.status_str(int(w.status.item())))
-    value = ws * w.flops() * args.steps / (ms_max * 1e-3) / 1e12
+    value = weak_scaling_value(w.flops() * args.steps, ws, ms_max) / 1e12
 
     # end to end: host buffers in, results back to host, same step count
     e2e = None
@@ -565,7 +578,7 @@ def run_ours(args):
         torch.cuda.synchronize()
         barrier(ws)
         ms2 = max_over_ranks(s2.elapsed_time(e2), ws)
-        e2e = {"value": ws * w.flops() * n2 / (ms2 * 1e-3) / 1e12, "unit": "TFLOP/s",
+        e2e = {"value": weak_scaling_value(w.flops() * n2, ws, ms2) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": n2,
                "ms_per_step": ms2 / n2}
 

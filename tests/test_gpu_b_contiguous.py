@@ -174,3 +174,16 @@ def test_device_errors(lib, cuda):
     R = gu.deq_bf16(A)[:10] @ gu.deq_bf16(B).reshape(2, 128, 128)[1].T
     gu.check_rows_bf16(gu.bf16_bits(D)[:10], R)
     assert (gu.bf16_bits(D)[10:] == gu.SENTINEL_BITS).all()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_max_experts(lib, cuda, dtype):
+    """E = 1024 (the largest the library takes): the per-CTA schedule in
+    shared memory is at its largest, and most experts are tiny or empty."""
+    rng = np.random.default_rng(1024)
+    counts = [int(c) for c in rng.integers(0, 6, size=1024)]
+    counts[5] = 300
+    Dbits, written, R, status = run_contiguous(counts, 256, 256, dtype, 16, seed=17, integer=True)
+    assert status == 0
+    assert np.array_equal(Dbits[written], gu.round_bf16_bits(R[written]))
+    assert_sentinels(Dbits, written)

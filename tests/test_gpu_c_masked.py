@@ -113,3 +113,13 @@ def test_invalid_valid_m(lib, cuda):
     for e in (0, 3):
         gu.check_rows_bf16(Dbits[e, :v[e]], R[e, :v[e]])
     assert (Dbits[1] == gu.SENTINEL_BITS).all() and (Dbits[2] == gu.SENTINEL_BITS).all()
+
+
+def test_max_experts(lib, cuda):
+    """E = 1024 masked buffers of 16 rows, most of them empty."""
+    rng = np.random.default_rng(7)
+    v = [int(x) if x < 17 else 0 for x in rng.integers(0, 40, size=1024)]
+    Dbits, written, R, status = run_masked(v, 16, 256, 256, "fp8", seed=5, integer=True)
+    assert status == 0
+    assert np.array_equal(Dbits[written], gu.round_bf16_bits(R[written]))
+    assert (Dbits[~written] == gu.SENTINEL_BITS).all()

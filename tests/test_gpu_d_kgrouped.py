@@ -91,3 +91,13 @@ def test_empty_and_errors(lib, cuda):
     r0 = gu.deq_bf16(dY).reshape(40, 128)[:30].T @ gu.deq_bf16(X).reshape(40, 128)[:30]
     check_dw(dW.cpu().numpy()[:1].astype(np.float64), r0[None])
     assert np.all(dW.cpu().numpy()[1] == F32_SENTINEL)
+
+
+def test_max_experts(lib, cuda):
+    """E = 1024 experts of a few tokens each (many empty): the descending-count
+    order of 1024 experts and many partial token blocks."""
+    rng = np.random.default_rng(3)
+    counts = [int(c) for c in rng.integers(0, 9, size=1024)]
+    got, ref, status = run_kgrouped(counts, 256, 128, integer=True, T_extra=5)
+    assert status == 0
+    assert np.array_equal(got, ref)
