@@ -72,3 +72,51 @@ def test_wrong_weight_scale_index_is_caught(monkeypatch):
         return on.decode_e4m3(codes) * full
     monkeypatch.setattr(on, "dequant_weight", bad)
     assert fails(tn.test_dequant_weight_brute_force)
+
+
+# --- SwiGLU / FP8 re-quantisation (oracle/epilogue.py) ---------------------
+import oracle.epilogue as oe                     # noqa: E402
+from tests import test_oracle_epilogue as te     # noqa: E402
+
+
+def test_sigmoid_sign_flip_is_caught(monkeypatch):
+    monkeypatch.setattr(oe, "silu", lambda x: np.asarray(x, float) / (1.0 + np.exp(np.asarray(x, float))))
+    assert fails(te.test_silu_closed_forms)
+
+
+def test_ties_away_from_zero_is_caught(monkeypatch):
+    mag = oe._MAG
+
+    def bad(x):
+        x = np.asarray(x, dtype=np.float64)
+        a = np.minimum(np.abs(x), 448.0)
+        hi = np.clip(np.searchsorted(mag, a, side="left"), 0, 126)
+        lo = np.clip(hi - 1, 0, 126)
+        code = np.where(a - mag[lo] < mag[hi] - a, lo, hi).astype(np.uint8)
+        return np.where(np.signbit(x), code | 0x80, code).astype(np.uint8)
+    monkeypatch.setattr(oe, "encode_e4m3", bad)
+    assert fails(te.test_encode_rounds_to_nearest_even_and_saturates)
+
+
+def test_scale_off_by_one_is_caught(monkeypatch):
+    orig = oe.ue8m0_for_amax
+    monkeypatch.setattr(oe, "ue8m0_for_amax", lambda a: np.where(np.asarray(a) == 0, 127, orig(a) + 1).astype(np.uint8))
+    assert fails(te.test_ue8m0_boundaries)
+    assert fails(te.test_quantize_blocks_bounds_and_layout)
+
+
+def test_amax_bound_strictness_is_caught(monkeypatch):
+    # using m >= 0.875 instead of m > 0.875 doubles the scale exactly on the bound
+    def bad(amax):
+        amax = np.asarray(amax, dtype=np.float64)
+        m, e = np.frexp(amax)
+        s = np.clip(e.astype(np.int64) + 118 + (m >= 0.875), 1, 254)
+        return np.where(amax == 0, 127, s).astype(np.uint8)
+    monkeypatch.setattr(oe, "ue8m0_for_amax", bad)
+    assert fails(te.test_ue8m0_boundaries)
+
+
+def test_swapped_gate_and_up_is_caught(monkeypatch):
+    orig = oe.gate_up_halves
+    monkeypatch.setattr(oe, "gate_up_halves", lambda H: orig(H)[::-1])
+    assert fails(te.test_gate_up_halves_layout)
