@@ -205,6 +205,55 @@ mg_status mgemm_masked(mg_dtype dt, const void* A, const uint8_t* SFA,
                        int32_t N, int32_t K, int32_t* d_status, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Grouped GEMM with the expert's SwiGLU fused into the epilogue
+ * ("flops/deepgemm-grouped-masked-moe-gemm", "Workarounds": the fused MoE
+ * kernel runs SwiGLU between the two grouped GEMMs, and the FP8 path hands
+ * the second GEMM E4M3 activations with UE8M0 per-128 scales).  The pages
+ * name SwiGLU without writing it out; this is the standard definition
+ *     y = SiLU(g) * u,   SiLU(x) = x / (1 + exp(-x)).
+ *
+ * B holds GEMM1's gate and up weights interleaved in 128-row blocks: for
+ * feature block j (features 128j..128j+127 of I = N/2), rows 256j..256j+127
+ * are the gate rows and rows 256j+128..256j+255 the up rows.  With
+ * H = A * B[e]^T (fp32 accumulation, as in mgemm_contiguous / mgemm_masked):
+ *     Y[row, 128j + i] = SiLU(H[row, 256j + i]) * H[row, 256j + 128 + i]
+ * computed in fp32, for the same rows the plain call would write; no other
+ * row of Y (or column of SFY) is written.
+ *
+ *   out = MG_SWIGLU_BF16:  Y bf16 [rows, I] (round to nearest even); SFY
+ *         unused (may be NULL).
+ *   out = MG_SWIGLU_FP8_E4M3_UE8M0:  Y E4M3 bytes [rows, I] and SFY uint8:
+ *         for each (row, 128-feature block j) the scale byte s is the
+ *         smallest with max|y| <= 448 * 2^(s-127), clamped to [1, 254]
+ *         (127 for an all-zero block), and each code is the nearest E4M3
+ *         value of y * 2^(127-s), ties to even, magnitudes past 448
+ *         saturating to 448.  SFY is laid out like the activation scales of
+ *         the next GEMM: [I/128, rows_cap] (contiguous) or [E, I/128, M_max]
+ *         (masked), so Y and SFY feed mgemm_contiguous / mgemm_masked with
+ *         K = I directly (rows_cap, align_q and M_max multiples of 16).
+ *
+ * rows = rows_cap (contiguous) or E*M_max (masked).  All other arguments,
+ * requirements and device errors are those of mgemm_contiguous /
+ * mgemm_masked.  N must be a multiple of 256 (else MG_ERR_UNSUPPORTED).
+ * These calls always run the single-SM two-block kernel (tile = one gate
+ * block and its up block), whatever mg_set_kernel_policy chose.
+ * ------------------------------------------------------------------------ */
+typedef enum {
+  MG_SWIGLU_BF16 = 1,
+  MG_SWIGLU_FP8_E4M3_UE8M0 = 2
+} mg_swiglu_out;
+
+mg_status mgemm_contiguous_swiglu(mg_dtype dt, mg_swiglu_out out, const void* A,
+                                  const uint8_t* SFA, const void* B, const uint8_t* SFB,
+                                  void* Y, uint8_t* SFY, const int32_t* d_counts, int32_t E,
+                                  int64_t rows_cap, int32_t N, int32_t K, int32_t align_q,
+                                  int32_t tile_q, int32_t* d_status, void* stream);
+mg_status mgemm_masked_swiglu(mg_dtype dt, mg_swiglu_out out, const void* A, const uint8_t* SFA,
+                              const void* B, const uint8_t* SFB, void* Y, uint8_t* SFY,
+                              const int32_t* d_valid_m, int32_t E, int32_t M_max, int32_t N,
+                              int32_t K, int32_t* d_status, void* stream);
+
+/* ------------------------------------------------------------------------
  * K-grouped weight-gradient GEMM ("flops/deepgemm-grouped-masked-moe-gemm",
  * "Workarounds": K-grouped GEMM for MoE weight backward, M and N fixed and
  * the contraction length varying per expert).

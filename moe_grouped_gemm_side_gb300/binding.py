@@ -18,6 +18,7 @@ STATUS_NAMES = {
     4: "MG_ERR_CAPACITY", 5: "MG_ERR_TIMEOUT", 6: "MG_ERR_DEVICE_ARG",
 }
 MG_BF16, MG_FP8_E4M3_UE8M0 = 0, 1
+MG_SWIGLU_BF16, MG_SWIGLU_FP8_E4M3_UE8M0 = 1, 2
 
 # Every function the header declares, with its ctypes signature.
 _c_i32p = ctypes.POINTER(ctypes.c_int32)
@@ -41,6 +42,10 @@ SIGNATURES = {
     "moe_select_tile_host": (_i32, [_i32, _c_i32p, _i32, _i32, _i32, _i32, _c_i32p]),
     "mgemm_contiguous": (_i32, [_i32, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32, _i32, _vp, _vp]),
     "mgemm_masked": (_i32, [_i32, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp]),
+    "mgemm_contiguous_swiglu": (_i32, [_i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32,
+                                       _i32, _i32, _vp, _vp]),
+    "mgemm_masked_swiglu": (_i32, [_i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp,
+                                   _vp]),
     "kgemm_grouped": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _vp, _vp]),
     "mg_set_wait_limit_ns": (_i32, [_i64]),
     "mg_get_wait_limit_ns": (_i64, []),
@@ -187,6 +192,37 @@ def mgemm_masked(A, B, D, d_valid_m, SFA=None, SFB=None, status=None, stream=Non
     _check("mgemm_masked", lib.mgemm_masked(
         _dtype_of(A), _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(D), _ptr(d_valid_m), E,
         M_max, N, K, _ptr(status), _stream(stream)))
+
+
+def _swiglu_out(Y):
+    import torch
+    if Y.dtype == torch.bfloat16:
+        return MG_SWIGLU_BF16
+    if Y.dtype in (torch.uint8, torch.float8_e4m3fn):
+        return MG_SWIGLU_FP8_E4M3_UE8M0
+    raise TypeError(f"unsupported SwiGLU output dtype {Y.dtype}")
+
+
+def mgemm_contiguous_swiglu(A, B, Y, d_counts, align_q: int, SFA=None, SFB=None, SFY=None,
+                            tile_q: int = 0, status=None, stream=None):
+    """GEMM1 with SwiGLU fused into its epilogue; Y bf16 [rows_cap, N/2], or
+    E4M3 bytes with UE8M0 scales SFY [N/256, rows_cap]."""
+    lib = load()
+    rows_cap, K = A.shape
+    E, N, _ = B.shape
+    _check("mgemm_contiguous_swiglu", lib.mgemm_contiguous_swiglu(
+        _dtype_of(A), _swiglu_out(Y), _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(Y), _ptr(SFY),
+        _ptr(d_counts), E, rows_cap, N, K, align_q, tile_q, _ptr(status), _stream(stream)))
+
+
+def mgemm_masked_swiglu(A, B, Y, d_valid_m, SFA=None, SFB=None, SFY=None, status=None, stream=None):
+    """Masked GEMM1 with SwiGLU fused; Y [E, M_max, N/2], SFY [E, N/256, M_max]."""
+    lib = load()
+    E, M_max, K = A.shape
+    N = B.shape[1]
+    _check("mgemm_masked_swiglu", lib.mgemm_masked_swiglu(
+        _dtype_of(A), _swiglu_out(Y), _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(Y), _ptr(SFY),
+        _ptr(d_valid_m), E, M_max, N, K, _ptr(status), _stream(stream)))
 
 
 def kgemm_grouped(dY, X, dW, d_counts, status=None, stream=None):

@@ -144,6 +144,74 @@ mg_status encode_operands(FwdArgs& a, const void* A, const uint8_t* SFA, const v
   return MG_OK;
 }
 
+mg_status prep_contiguous(FwdArgs& a, mg_dtype dt, const void* A, const uint8_t* SFA, const void* B,
+                          const uint8_t* SFB, void* D, const int32_t* d_counts, int32_t E,
+                          int64_t rows_cap, int32_t N, int32_t K, int32_t align_q, int32_t tile_q,
+                          int32_t* d_status) {
+  mg_status st = check_fwd_common(dt, A, SFA, B, SFB, D, d_counts, E, N, K);
+  if (st != MG_OK) return st;
+  const bool fp8 = dt == MG_FP8_E4M3_UE8M0;
+  if (rows_cap <= 0 || rows_cap >= (int64_t(1) << 31) || align_q <= 0) return MG_ERR_INVALID_ARG;
+  if (fp8 && (align_q % 16 != 0 || rows_cap % 16 != 0)) return MG_ERR_UNSUPPORTED;
+  if (tile_q != 0) {
+    if (tile_q < 16 || tile_q > 256 || tile_q % 16 != 0) return MG_ERR_INVALID_ARG;
+    if (fp8 && tile_q > 240 && tile_q != 256) return MG_ERR_INVALID_ARG;
+  }
+  a.fp8 = fp8;
+  a.masked = false;
+  a.counts = d_counts;
+  a.E = E;
+  a.N = N;
+  a.K = K;
+  a.rows_total = (int32_t)rows_cap;
+  a.align_q = align_q;
+  a.tile_q = tile_q;
+  a.sfb = SFB;
+  a.D = D;
+  a.status = d_status;
+  a.wait_ns = g_wait_ns.load();
+  return encode_operands(a, A, SFA, B, rows_cap, rows_cap, 1, 4u);
+}
+
+mg_status prep_masked(FwdArgs& a, mg_dtype dt, const void* A, const uint8_t* SFA, const void* B,
+                      const uint8_t* SFB, void* D, const int32_t* d_valid_m, int32_t E, int32_t M_max,
+                      int32_t N, int32_t K, int32_t* d_status) {
+  mg_status st = check_fwd_common(dt, A, SFA, B, SFB, D, d_valid_m, E, N, K);
+  if (st != MG_OK) return st;
+  const bool fp8 = dt == MG_FP8_E4M3_UE8M0;
+  if (M_max <= 0 || (int64_t)E * M_max >= (int64_t(1) << 31)) return MG_ERR_INVALID_ARG;
+  if (fp8 && M_max % 16 != 0) return MG_ERR_UNSUPPORTED;
+  a.fp8 = fp8;
+  a.masked = true;
+  a.counts = d_valid_m;
+  a.E = E;
+  a.N = N;
+  a.K = K;
+  a.rows_total = E * M_max;
+  a.M_max = M_max;
+  a.sfb = SFB;
+  a.D = D;
+  a.status = d_status;
+  a.wait_ns = g_wait_ns.load();
+  return encode_operands(a, A, SFA, B, (int64_t)E * M_max, M_max, E, 4u);
+}
+
+// The SwiGLU epilogue pairs the two 128-row weight blocks of a single-SM
+// tile (gate, then up), so N must hold whole 256-row gate/up pairs.
+mg_status check_swiglu(mg_swiglu_out out, int32_t N, const uint8_t* SFY) {
+  if (out != MG_SWIGLU_BF16 && out != MG_SWIGLU_FP8_E4M3_UE8M0) return MG_ERR_INVALID_ARG;
+  if (N <= 0) return MG_ERR_INVALID_ARG;
+  if (N % 256 != 0) return MG_ERR_UNSUPPORTED;
+  if (out == MG_SWIGLU_FP8_E4M3_UE8M0 && SFY == nullptr) return MG_ERR_INVALID_ARG;
+  return MG_OK;
+}
+
+void set_swiglu(FwdArgs& a, mg_swiglu_out out, uint8_t* SFY, int64_t sfy_ld) {
+  a.epi = out == MG_SWIGLU_BF16 ? kEpiSwigluBf16 : kEpiSwigluFp8;
+  a.sfy = out == MG_SWIGLU_BF16 ? nullptr : SFY;
+  a.sfy_ld = (int32_t)sfy_ld;
+}
+
 }  // namespace
 
 extern "C" {
@@ -237,60 +305,47 @@ mg_status mgemm_contiguous(mg_dtype dt, const void* A, const uint8_t* SFA, const
                            const uint8_t* SFB, void* D, const int32_t* d_counts, int32_t E,
                            int64_t rows_cap, int32_t N, int32_t K, int32_t align_q, int32_t tile_q,
                            int32_t* d_status, void* stream) {
-  mg_status st = check_fwd_common(dt, A, SFA, B, SFB, D, d_counts, E, N, K);
-  if (st != MG_OK) return st;
-  const bool fp8 = dt == MG_FP8_E4M3_UE8M0;
-  if (rows_cap <= 0 || rows_cap >= (int64_t(1) << 31) || align_q <= 0) return MG_ERR_INVALID_ARG;
-  if (fp8 && (align_q % 16 != 0 || rows_cap % 16 != 0)) return MG_ERR_UNSUPPORTED;
-  if (tile_q != 0) {
-    if (tile_q < 16 || tile_q > 256 || tile_q % 16 != 0) return MG_ERR_INVALID_ARG;
-    if (fp8 && tile_q > 240 && tile_q != 256) return MG_ERR_INVALID_ARG;
-  }
   FwdArgs a;
-  a.fp8 = fp8;
-  a.masked = false;
-  a.counts = d_counts;
-  a.E = E;
-  a.N = N;
-  a.K = K;
-  a.rows_total = (int32_t)rows_cap;
-  a.align_q = align_q;
-  a.tile_q = tile_q;
-  a.sfb = SFB;
-  a.D = D;
-  a.status = d_status;
-  a.wait_ns = g_wait_ns.load();
-  st = encode_operands(a, A, SFA, B, rows_cap, rows_cap, 1, 4u);
+  const mg_status st = prep_contiguous(a, dt, A, SFA, B, SFB, D, d_counts, E, rows_cap, N, K, align_q,
+                                       tile_q, d_status);
   if (st != MG_OK) return st;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return from_cuda(launch_fwd_any(a, s));
+  return from_cuda(launch_fwd_any(a, static_cast<cudaStream_t>(stream)));
 }
 
 mg_status mgemm_masked(mg_dtype dt, const void* A, const uint8_t* SFA, const void* B,
                        const uint8_t* SFB, void* D, const int32_t* d_valid_m, int32_t E,
                        int32_t M_max, int32_t N, int32_t K, int32_t* d_status, void* stream) {
-  mg_status st = check_fwd_common(dt, A, SFA, B, SFB, D, d_valid_m, E, N, K);
-  if (st != MG_OK) return st;
-  const bool fp8 = dt == MG_FP8_E4M3_UE8M0;
-  if (M_max <= 0 || (int64_t)E * M_max >= (int64_t(1) << 31)) return MG_ERR_INVALID_ARG;
-  if (fp8 && M_max % 16 != 0) return MG_ERR_UNSUPPORTED;
   FwdArgs a;
-  a.fp8 = fp8;
-  a.masked = true;
-  a.counts = d_valid_m;
-  a.E = E;
-  a.N = N;
-  a.K = K;
-  a.rows_total = E * M_max;
-  a.M_max = M_max;
-  a.sfb = SFB;
-  a.D = D;
-  a.status = d_status;
-  a.wait_ns = g_wait_ns.load();
-  st = encode_operands(a, A, SFA, B, (int64_t)E * M_max, M_max, E, 4u);
+  const mg_status st = prep_masked(a, dt, A, SFA, B, SFB, D, d_valid_m, E, M_max, N, K, d_status);
   if (st != MG_OK) return st;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return from_cuda(launch_fwd_any(a, s));
+  return from_cuda(launch_fwd_any(a, static_cast<cudaStream_t>(stream)));
+}
+
+mg_status mgemm_contiguous_swiglu(mg_dtype dt, mg_swiglu_out out, const void* A, const uint8_t* SFA,
+                                  const void* B, const uint8_t* SFB, void* Y, uint8_t* SFY,
+                                  const int32_t* d_counts, int32_t E, int64_t rows_cap, int32_t N,
+                                  int32_t K, int32_t align_q, int32_t tile_q, int32_t* d_status,
+                                  void* stream) {
+  mg_status st = check_swiglu(out, N, SFY);
+  if (st != MG_OK) return st;
+  FwdArgs a;
+  st = prep_contiguous(a, dt, A, SFA, B, SFB, Y, d_counts, E, rows_cap, N, K, align_q, tile_q, d_status);
+  if (st != MG_OK) return st;
+  set_swiglu(a, out, SFY, rows_cap);
+  return from_cuda(launch_fwd(a, static_cast<cudaStream_t>(stream), kFwdDual));
+}
+
+mg_status mgemm_masked_swiglu(mg_dtype dt, mg_swiglu_out out, const void* A, const uint8_t* SFA,
+                              const void* B, const uint8_t* SFB, void* Y, uint8_t* SFY,
+                              const int32_t* d_valid_m, int32_t E, int32_t M_max, int32_t N, int32_t K,
+                              int32_t* d_status, void* stream) {
+  mg_status st = check_swiglu(out, N, SFY);
+  if (st != MG_OK) return st;
+  FwdArgs a;
+  st = prep_masked(a, dt, A, SFA, B, SFB, Y, d_valid_m, E, M_max, N, K, d_status);
+  if (st != MG_OK) return st;
+  set_swiglu(a, out, SFY, M_max);
+  return from_cuda(launch_fwd(a, static_cast<cudaStream_t>(stream), kFwdDual));
 }
 
 mg_status kgemm_grouped(const void* dY, const void* X, float* dW, const int32_t* d_counts,

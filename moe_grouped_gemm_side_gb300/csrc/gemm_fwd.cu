@@ -40,6 +40,7 @@
 // other work there (warp-wide synchronisation, building scale words,
 // decoding tiles) left the pipe idle.
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 
 #include "common.cuh"
 #include "mg_internal.h"
@@ -73,12 +74,15 @@ constexpr uint64_t kDrainNs = 200ull * 1000 * 1000;
 struct Params {
   const int32_t* counts;
   const uint8_t* sfb;
-  __nv_bfloat16* D;
+  void* D;           // bf16 [rows, N]; with a SwiGLU epilogue Y [rows, N/2] (bf16 or E4M3)
+  uint8_t* sfy;      // SwiGLU to E4M3: UE8M0 scales of Y, [z][N/256][sfy_ld]
   int32_t* status;
   int64_t wait_ns;
   int32_t E, N, K;
   int32_t masked, fp8;
   int32_t rows_total, M_max, align_q, tile_q;
+  int32_t epi;       // kEpiPlain, kEpiSwigluBf16 or kEpiSwigluFp8
+  int32_t sfy_ld;
 };
 
 struct Shared {
@@ -96,6 +100,10 @@ struct Shared {
   int32_t total;     // tiles of this launch
   int32_t nblk;      // weight blocks per tile of this launch
   int32_t tile_qn[kInfoRing];
+  // SwiGLU to E4M3: per-token maxima of each lane quadrant, exchanged between
+  // the four epilogue warps of one half ([half][chunk parity][quadrant][token])
+  uint64_t amax_bar[2];
+  float amax[2][2][4][16];
 };
 
 struct Tile {
@@ -141,6 +149,99 @@ __device__ __forceinline__ Tile decode_tile(int32_t t, const int32_t* tpre, cons
   tl.sf_x = masked ? in_e : tl.row0;
   tl.sf_z = masked ? lo : 0;
   return tl;
+}
+
+// SwiGLU epilogue of a two-block tile on one SM ("flops/deepgemm-grouped-
+// masked-moe-gemm", "Workarounds": the expert's SwiGLU runs between the two
+// grouped GEMMs, and the FP8 path hands the second GEMM per-128 UE8M0-scaled
+// E4M3 activations).  GEMM1's weight rows are interleaved in 128-row blocks
+// (gate rows of features 128j..128j+127, then their up rows), so block 0 of
+// tile nb holds the gate and block 1 the up values of features
+// 128nb..128nb+127 and the thread owning TMEM lane l has both halves of one
+// feature:  y = SiLU(g) * u = g / (1 + e^-g) * u  in fp32.
+//
+// To bf16: lane pairs exchange so each store writes two features.  To E4M3:
+// the scale of (token, 128 features) needs the maximum over all four lane
+// quadrants, held by the four warps of this half; each warp reduces its 32
+// features per token with a transposing butterfly (16 shuffles for 16
+// tokens), publishes them in shared memory and waits on an mbarrier that the
+// four warps' 128 threads complete (double-buffered by chunk parity, so one
+// barrier per chunk suffices).  Scale byte: the smallest s with
+// amax <= 448 * 2^(s-127), clamped to [1, 254], 127 for an all-zero block;
+// codes round y * 2^(127-s) to the nearest E4M3 value, saturating.
+// Returns false if a wait gave up.
+__device__ __forceinline__ bool swiglu_chunks(const Params& p, Shared& sh, const Tile& tl,
+                                              uint32_t taddr, uint32_t quad, int32_t half,
+                                              uint32_t lane, uint32_t& chunk, uint64_t deadline) {
+  const int32_t I = p.N >> 1;
+  const int32_t f = tl.nb * kCtaRows + (int32_t)(quad * 32u + lane);  // this thread's feature
+  const bool odd = (lane & 1u) != 0;
+  for (int32_t c0 = 16 * half; c0 < tl.qn; c0 += 32, ++chunk) {
+    uint32_t g[16], u[16];
+    tmem_ld16(taddr + (uint32_t)c0, g);
+    tmem_ld16(taddr + kAccStride + (uint32_t)c0, u);
+    tmem_ld_wait();
+    tmem_regs_ready(g);
+    tmem_regs_ready(u);
+    float y[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float gi = __uint_as_float(g[i]);
+      y[i] = __fdividef(gi, 1.0f + __expf(-gi)) * __uint_as_float(u[i]);
+    }
+    if (p.epi == kEpiSwigluBf16) {
+      __nv_bfloat16* ypair = static_cast<__nv_bfloat16*>(p.D) + (int64_t)tl.row0 * I + (f & ~1);
+#pragma unroll
+      for (int i = 0; i < 16; i += 2) {
+        const int32_t row = c0 + i + (odd ? 1 : 0);
+        const float mine = odd ? y[i + 1] : y[i];
+        const float recv = __shfl_xor_sync(0xffffffffu, odd ? y[i] : y[i + 1], 1);
+        const __nv_bfloat162 v = odd ? __floats2bfloat162_rn(recv, mine) : __floats2bfloat162_rn(mine, recv);
+        if (row < tl.rows) *reinterpret_cast<__nv_bfloat162*>(ypair + (int64_t)row * I) = v;
+      }
+      continue;
+    }
+    // per-token maximum over the warp's 32 features: each step halves the
+    // live values; afterwards lanes 2t and 2t+1 hold token t's maximum
+    float m[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) m[i] = fabsf(y[i]);
+#pragma unroll
+    for (int w = 8; w >= 1; w >>= 1) {
+      const bool hi = (lane & (uint32_t)(2 * w)) != 0;
+#pragma unroll
+      for (int j = 0; j < w; ++j) {
+        const float keep = hi ? m[j + w] : m[j];
+        const float send = hi ? m[j] : m[j + w];
+        m[j] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 2 * w));
+      }
+    }
+    m[0] = fmaxf(m[0], __shfl_xor_sync(0xffffffffu, m[0], 1));
+    const uint32_t par = chunk & 1u;
+    float* slot = &sh.amax[half][par][0][0];
+    const int32_t t = (int32_t)(lane >> 1);
+    if (!odd) slot[quad * 16u + (uint32_t)t] = m[0];
+    mbar_arrive(&sh.amax_bar[half]);
+    if (!warp_wait(&sh.amax_bar[half], par, deadline, &sh.abort_flag, p.status)) return false;
+    const float amax = fmaxf(fmaxf(slot[t], slot[16 + t]), fmaxf(slot[32 + t], slot[48 + t]));
+    // amax = 1.m * 2^(E-127); 448 = 1.75 * 2^8: s = E - 8, plus one when 1.m > 1.75
+    const uint32_t bits = __float_as_uint(amax);
+    int32_t sc = (int32_t)(bits >> 23) - 8 + ((bits & 0x7fffffu) > 0x600000u ? 1 : 0);
+    sc = min(max(sc, 1), 254);
+    if (amax == 0.0f) sc = 127;
+    // 2^(127-s): a normal float for s <= 253, the subnormal 2^-127 for s = 254
+    const float inv = sc < 254 ? __uint_as_float((uint32_t)(254 - sc) << 23) : __uint_as_float(0x00400000u);
+    if (quad == 0 && !odd && c0 + t < tl.rows)
+      p.sfy[((int64_t)tl.sf_z * (I / kCtaRows) + tl.nb) * p.sfy_ld + tl.sf_x + c0 + t] = (uint8_t)sc;
+    uint8_t* yq = static_cast<uint8_t*>(p.D) + (int64_t)tl.row0 * I + f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float x = y[i] * __shfl_sync(0xffffffffu, inv, 2 * i);
+      const __nv_fp8_storage_t code = __nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
+      if (c0 + i < tl.rows) yq[(int64_t)(c0 + i) * I] = (uint8_t)code;
+    }
+  }
+  return true;
 }
 
 template <int kBlocks, bool kPair>
@@ -191,6 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sh.acc_empty[i], kEpiWarps * (kPair ? 2 : 1));  // one arrival per epilogue warp
     }
     mbar_init(&sh.drain, 1);
+    for (int i = 0; i < 2; ++i) mbar_init(&sh.amax_bar[i], 4 * 32);
     sh.abort_flag = 0;
     fence_barrier_init();
   }
@@ -260,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // not fill two waves of workers: with few tiles (decode) the finer
     // split balances the SMs, which all stream weights from DRAM then.
     int32_t nblk = kBlocks;
-    if (kBlocks == 2) {
+    if (kBlocks == 2 && p.epi == kEpiPlain) {  // a SwiGLU epilogue needs gate and up in one tile
       int64_t tt = 0;
       for (int32_t e = lane; e < E; e += 32) tt += cdiv64(cnt[e], q);
 #pragma unroll
@@ -578,35 +680,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     with_blocks([&](auto bc) {
     constexpr int kB = decltype(bc)::value;
     uint32_t acc = 0, acc_phase = 0;
+    uint32_t chunk = 0;  // SwiGLU to E4M3: chunks done, for the exchange barrier's phase
     for (int32_t t = unit; S > 0 && t < total; t += n_units) {
       const Tile tl = decode_tile(t, tpre, cnt, rowbase, E, NB, q, p.masked);
       if (!warp_wait(&sh.acc_full[acc], acc_phase, deadline, &sh.abort_flag, p.status)) break;
       tc_fence_after();
-      // this thread's output column of block 0; block b is b * kBlockRows further
-      const int32_t n = tl.nb * tile_rows + (int32_t)(rank * kCtaRows + quad * 32 + lane);
       const uint32_t taddr = tmem + ((quad * 32u) << 16) + acc * kAccStride;
-      __nv_bfloat16* dpair = p.D + (int64_t)tl.row0 * p.N + (n & ~1);
-      // the two warps of a lane quadrant take alternate 16-token chunks
-      for (int32_t c0 = 16 * half; c0 < tl.qn; c0 += 32) {
-        uint32_t r[kB][16];
+      bool swiglu = false;
+      if constexpr (kB == 2 && !kPair) swiglu = p.epi != kEpiPlain;
+      if (swiglu) {
+        if (!swiglu_chunks(p, sh, tl, taddr, quad, half, lane, chunk, deadline)) break;
+      } else {
+        // this thread's output column of block 0; block b is b * kBlockRows further
+        const int32_t n = tl.nb * tile_rows + (int32_t)(rank * kCtaRows + quad * 32 + lane);
+        __nv_bfloat16* dpair = static_cast<__nv_bfloat16*>(p.D) + (int64_t)tl.row0 * p.N + (n & ~1);
+        // the two warps of a lane quadrant take alternate 16-token chunks
+        for (int32_t c0 = 16 * half; c0 < tl.qn; c0 += 32) {
+          uint32_t r[kB][16];
 #pragma unroll
-        for (int b = 0; b < kB; ++b) tmem_ld16(taddr + b * kAccStride + (uint32_t)c0, r[b]);
-        tmem_ld_wait();
+          for (int b = 0; b < kB; ++b) tmem_ld16(taddr + b * kAccStride + (uint32_t)c0, r[b]);
+          tmem_ld_wait();
 #pragma unroll
-        for (int b = 0; b < kB; ++b) tmem_regs_ready(r[b]);
-        // Lanes 2j and 2j+1 hold adjacent output columns.  One exchange per
-        // pair of tokens gives the even lane both columns of token i and the
-        // odd lane both columns of token i+1, so each store writes 4 bytes.
+          for (int b = 0; b < kB; ++b) tmem_regs_ready(r[b]);
+          // Lanes 2j and 2j+1 hold adjacent output columns.  One exchange per
+          // pair of tokens gives the even lane both columns of token i and the
+          // odd lane both columns of token i+1, so each store writes 4 bytes.
 #pragma unroll
-        for (int i = 0; i < 16; i += 2) {
-          const int32_t row = c0 + i + (odd ? 1 : 0);
+          for (int i = 0; i < 16; i += 2) {
+            const int32_t row = c0 + i + (odd ? 1 : 0);
 #pragma unroll
-          for (int b = 0; b < kB; ++b) {
-            const float mine = __uint_as_float(odd ? r[b][i + 1] : r[b][i]);
-            const float recv = __shfl_xor_sync(0xffffffffu, __uint_as_float(odd ? r[b][i] : r[b][i + 1]), 1);
-            const __nv_bfloat162 v = odd ? __floats2bfloat162_rn(recv, mine) : __floats2bfloat162_rn(mine, recv);
-            if (row < tl.rows)
-              *reinterpret_cast<__nv_bfloat162*>(dpair + (int64_t)row * p.N + b * kBlockRows) = v;
+            for (int b = 0; b < kB; ++b) {
+              const float mine = __uint_as_float(odd ? r[b][i + 1] : r[b][i]);
+              const float recv = __shfl_xor_sync(0xffffffffu, __uint_as_float(odd ? r[b][i] : r[b][i + 1]), 1);
+              const __nv_bfloat162 v = odd ? __floats2bfloat162_rn(recv, mine) : __floats2bfloat162_rn(mine, recv);
+              if (row < tl.rows)
+                *reinterpret_cast<__nv_bfloat162*>(dpair + (int64_t)row * p.N + b * kBlockRows) = v;
+            }
           }
         }
       }
@@ -646,10 +755,15 @@ cudaError_t launch(const FwdArgs& a, cudaStream_t s) {
     if (err != cudaSuccess) return err;
     attr_done[dev] = true;
   }
+  // the SwiGLU epilogue pairs the two blocks of a single-SM tile
+  if (a.epi != kEpiPlain && (kBlocks != 2 || kPair)) return cudaErrorInvalidValue;
   Params p;
   p.counts = a.counts;
   p.sfb = a.sfb;
-  p.D = static_cast<__nv_bfloat16*>(a.D);
+  p.D = a.D;
+  p.sfy = a.sfy;
+  p.epi = a.epi;
+  p.sfy_ld = a.sfy_ld;
   p.status = a.status;
   p.wait_ns = a.wait_ns;
   p.E = a.E;

@@ -9,6 +9,10 @@
 
 namespace mg {
 
+// Epilogue of the contiguous/masked kernel: plain bf16 D, or SwiGLU of
+// interleaved gate/up blocks stored as bf16 or as E4M3 with UE8M0 scales.
+enum FwdEpilogue { kEpiPlain = 0, kEpiSwigluBf16 = 1, kEpiSwigluFp8 = 2 };
+
 // Contiguous and masked forms share one kernel: both place an expert's
 // token rows at a known row base of a 2-D [rows_total, K] activation view and
 // compute only its first t_e rows.
@@ -23,6 +27,9 @@ struct FwdArgs {
   int32_t tile_q = 0;               // 0: choose on the device
   const uint8_t* sfb = nullptr;     // fp8 weight scales [E, K/128, N/128]
   void* D = nullptr;
+  int32_t epi = kEpiPlain;
+  uint8_t* sfy = nullptr;           // kEpiSwigluFp8: scales [z][N/256][sfy_ld]
+  int32_t sfy_ld = 0;
   int32_t* status = nullptr;
   int64_t wait_ns = 0;
   CUtensorMap tmW{}, tmA64{}, tmA16{}, tmA8{}, tmSF{};

@@ -27,7 +27,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for f in ("moe_plan", "moe_plan_host", "mgemm_contiguous", "mgemm_masked", "kgemm_grouped",
-              "moe_select_tile", "mg_status_str"):
+              "moe_select_tile", "mg_status_str", "mgemm_contiguous_swiglu", "mgemm_masked_swiglu"):
         assert f in names
     assert set(names) == set(mb.SIGNATURES), "binding and header disagree"
 
@@ -149,6 +149,25 @@ def test_device_calls_reject_bad_arguments_before_launch(lib):
     mm = list(m)
     mm[0], mm[2], mm[4], mm[8] = 1, FAKE, FAKE, 40
     assert L.mgemm_masked(*mm) == 2            # fp8 M_max % 16
+    # contiguous / masked with the SwiGLU epilogue
+    sw = [mb.MG_BF16, mb.MG_SWIGLU_BF16, FAKE, None, FAKE, None, FAKE, None, FAKE, 8, 1024, 512, 256, 16, 0,
+          None, None]
+
+    def swig(kw):
+        a = list(sw)
+        for k_, v in kw.items():
+            a[k_] = v
+        return L.mgemm_contiguous_swiglu(*a)
+    assert swig({1: 0}) == 1                 # bad output kind
+    assert swig({1: 3}) == 1
+    assert swig({11: 384}) == 2              # N not whole gate/up pairs
+    assert swig({1: mb.MG_SWIGLU_FP8_E4M3_UE8M0}) == 1      # E4M3 output without scales
+    assert swig({6: None}) == 1              # Y NULL
+    assert swig({13: 0}) == 1                # align_q (checks of the plain call)
+    ms = [mb.MG_BF16, mb.MG_SWIGLU_BF16, FAKE, None, FAKE, None, FAKE, None, FAKE, 8, 64, 512, 256, None, None]
+    assert L.mgemm_masked_swiglu(*[128 if i == 11 else v for i, v in enumerate(ms)]) == 2
+    assert L.mgemm_masked_swiglu(*[0 if i == 10 else v for i, v in enumerate(ms)]) == 1
+    assert L.mgemm_masked_swiglu(*[mb.MG_SWIGLU_FP8_E4M3_UE8M0 if i == 1 else v for i, v in enumerate(ms)]) == 1
     # k-grouped
     k = [FAKE, FAKE, FAKE, FAKE, 4, 4096, 256, 256, None, None]
     assert L.kgemm_grouped(*[None if i == 2 else v for i, v in enumerate(k)]) == 1
