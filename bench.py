@@ -201,13 +201,24 @@ class Contiguous:
         shapes = [(spec["N"], spec["K"])]
         if "second" in spec:
             shapes.append((spec["second"]["N"], spec["second"]["K"]))
+        # swiglu: GEMM1's epilogue applies SwiGLU to interleaved gate/up blocks and
+        # re-quantises (E4M3 + UE8M0), and GEMM2 consumes that output (K = N1/2)
+        self.swiglu = bool(spec.get("swiglu", False))
         self.gemms = []
         for i, (N, K) in enumerate(shapes):
             seed = spec["seed"] + 100 * i
             ops = wl.make_contiguous(self.E, self.rows_cap, N, K, spec["dtype"], seed, dev,
                                      spec["a_std"] if i == 0 else 1.0, spec["b_std"] if i == 0 else 1.0)
-            D = torch.empty((self.rows_cap, N), dtype=torch.bfloat16, device=dev)
-            self.gemms.append(dict(N=N, K=K, A=ops.A, B=ops.B, SFA=ops.SFA, SFB=ops.SFB, D=D))
+            A, SFA = ops.A, ops.SFA
+            if self.swiglu and i == 1:
+                A, SFA = self.gemms[0]["D"], self.gemms[0]["SFD"]      # GEMM1's output
+            if self.swiglu and i == 0:
+                D = torch.empty((self.rows_cap, N // 2), dtype=torch.uint8, device=dev)
+                SFD = torch.empty((N // 256, self.rows_cap), dtype=torch.uint8, device=dev)
+            else:
+                D, SFD = torch.empty((self.rows_cap, N), dtype=torch.bfloat16, device=dev), None
+            self.gemms.append(dict(N=N, K=K, A=A, B=ops.B, SFA=SFA, SFB=ops.SFB, D=D, SFD=SFD,
+                                   swiglu=self.swiglu and i == 0))
         self.d_counts = torch.tensor(self.counts, dtype=torch.int32, device=dev)
         self.offsets = torch.empty(self.E + 1, dtype=torch.int64, device=dev)
         self.stats = torch.empty(48, dtype=torch.uint8, device=dev)
@@ -223,7 +234,8 @@ class Contiguous:
         valid activation rows (+scales), valid output rows."""
         act = sum(1 for t in self.counts if t > 0)
         N, K = g["N"], g["K"]
-        b = act * N * K * self.elem + self.U * K * self.elem + self.U * N * 2
+        out = self.U * (N // 2 + N // 256) if g["swiglu"] else self.U * N * 2   # E4M3 Y + scales, or bf16 D
+        b = act * N * K * self.elem + self.U * K * self.elem + out
         if self.fp8:
             b += act * (K // 128) * (N // 128) + self.U * (K // 128)
         return b
@@ -239,9 +251,15 @@ class Contiguous:
         for i, g in enumerate(self.gemms):
             if ev is not None:
                 ev[i][0].record(stream)
-            rc = lib.mgemm_contiguous(self.dtype, ptr(g["A"]), ptr(g["SFA"]), ptr(g["B"]), ptr(g["SFB"]),
-                                      ptr(g["D"]), ptr(self.d_counts), self.E, self.rows_cap, g["N"], g["K"],
-                                      self.align, 0, ptr(self.status), s)
+            if g["swiglu"]:
+                rc = lib.mgemm_contiguous_swiglu(self.dtype, mb.MG_SWIGLU_FP8_E4M3_UE8M0, ptr(g["A"]),
+                                                 ptr(g["SFA"]), ptr(g["B"]), ptr(g["SFB"]), ptr(g["D"]),
+                                                 ptr(g["SFD"]), ptr(self.d_counts), self.E, self.rows_cap,
+                                                 g["N"], g["K"], self.align, 0, ptr(self.status), s)
+            else:
+                rc = lib.mgemm_contiguous(self.dtype, ptr(g["A"]), ptr(g["SFA"]), ptr(g["B"]), ptr(g["SFB"]),
+                                          ptr(g["D"]), ptr(self.d_counts), self.E, self.rows_cap, g["N"], g["K"],
+                                          self.align, 0, ptr(self.status), s)
             assert rc == 0, rc
             if ev is not None:
                 ev[i][1].record(stream)
@@ -249,11 +267,14 @@ class Contiguous:
     # end-to-end: inputs from pinned host memory, outputs back to pinned host
     def e2e_setup(self):
         self.h_in = [(self.d_counts, self.d_counts.cpu().pin_memory())]
-        for g in self.gemms:
+        for i, g in enumerate(self.gemms):
+            if self.swiglu and i == 1:
+                continue                      # produced on the device by GEMM1
             for k in ("A", "SFA"):
                 if g[k] is not None:
                     self.h_in.append((g[k], g[k].cpu().pin_memory()))
-        self.h_out = [(g["D"], torch.empty(g["D"].shape, dtype=g["D"].dtype).pin_memory()) for g in self.gemms]
+        outs = [self.gemms[-1]] if self.swiglu else self.gemms
+        self.h_out = [(g["D"], torch.empty(g["D"].shape, dtype=g["D"].dtype).pin_memory()) for g in outs]
         return (sum(h.numel() * h.element_size() for _, h in self.h_in),
                 sum(h.numel() * h.element_size() for _, h in self.h_out))
 
@@ -287,6 +308,8 @@ class Contiguous:
              "gemms": [f"N={g['N']},K={g['K']}" for g in self.gemms],
              "operands": "e4m3 + ue8m0 per-128 scales" if self.fp8 else "bf16",
              "l2": "inputs larger than L2 (no flush)"}
+        if self.swiglu:
+            d["epilogue"] = "GEMM1: SwiGLU of interleaved gate/up blocks, re-quantised to e4m3 + ue8m0; feeds GEMM2"
         return d
 
     # ---- CPU oracle on a bounded sample (experts given by index)
@@ -294,6 +317,7 @@ class Contiguous:
         from oracle import gemm as og
         from oracle import numerics as on
         from oracle import plan as op
+        from oracle import epilogue as oe
         host = []
         for g in self.gemms:
             host.append({k: (g[k].cpu() if g[k] is not None else None) for k in ("A", "SFA")})
@@ -305,14 +329,22 @@ class Contiguous:
             if t == 0:
                 continue
             o = p.offsets[e]
+            prev = None
             for g, h in zip(self.gemms, host):
-                if self.fp8:
+                if prev is not None:
+                    a = prev                    # GEMM2 reads GEMM1's re-quantised SwiGLU output
+                elif self.fp8:
                     a = on.dequant_rows(h["A"][o:o + t].numpy(), h["SFA"][:, o:o + t].numpy())
-                    b = on.dequant_weight(g["B"][e].cpu().numpy(), g["SFB"][e].cpu().numpy())
                 else:
                     a = on.decode_bf16(h["A"][o:o + t].view(torch.int16).numpy().view(np.uint16))
+                if self.fp8:
+                    b = on.dequant_weight(g["B"][e].cpu().numpy(), g["SFB"][e].cpu().numpy())
+                else:
                     b = on.decode_bf16(g["B"][e].cpu().view(torch.int16).numpy().view(np.uint16))
-                og.expert_product(a, b)
+                r = og.expert_product(a, b)
+                if g["swiglu"]:
+                    codes, sf = oe.quantize_blocks(oe.swiglu(*oe.gate_up_halves(r)))
+                    prev = on.dequant_rows(codes, sf)
                 useful += 2.0 * t * g["N"] * g["K"]
         return useful, time.perf_counter() - t0
 
@@ -499,6 +531,12 @@ def blas_threads():
     return len(os.sched_getaffinity(0))
 
 
+def sample_steps(w):
+    if getattr(w, "swiglu", False):
+        return "plan + fp64 dequantise + per-expert GEMM1, SwiGLU, E4M3 re-quantisation, GEMM2"
+    return "plan + fp64 dequantise + per-expert GEMMs"
+
+
 def oracle_sample_bounded(w, budget_s):
     """The oracle on a bounded sample: active experts in index order, one at
     a time, until about `budget_s` seconds of CPU work have been spent.
@@ -589,7 +627,7 @@ def run_ours(args):
     if ws == 1 and not args.no_cpu_baseline:
         experts, useful, secs = oracle_sample_bounded(w, args.cpu_budget)
         cpu = {"value": useful / secs / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
-               "sample": f"experts {experts} of {args.workload}: plan + fp64 dequantise + per-expert GEMMs, "
+               "sample": f"experts {experts} of {args.workload}: {sample_steps(w)}, "
                          f"{useful / 1e9:.1f} useful GFLOP in {secs:.1f} s"}
     line = {
         "metric": "effective TFLOPS (valid rows only)",
@@ -631,7 +669,7 @@ def run_reference(args):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": w.config(),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": f"one active expert per step (rotating) of {args.workload}: "
-                                   "plan + fp64 dequantise + per-expert GEMMs"},
+                                   f"{sample_steps(w)}"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))

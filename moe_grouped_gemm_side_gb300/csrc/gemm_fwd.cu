@@ -100,10 +100,10 @@ struct Shared {
   int32_t total;     // tiles of this launch
   int32_t nblk;      // weight blocks per tile of this launch
   int32_t tile_qn[kInfoRing];
-  // SwiGLU to E4M3: per-token maxima of each lane quadrant, exchanged between
-  // the four epilogue warps of one half ([half][chunk parity][quadrant][token])
+  // SwiGLU to E4M3: per-token maxima of each lane quadrant over the tile's
+  // tokens, exchanged between the four epilogue warps of one half
   uint64_t amax_bar[2];
-  float amax[2][2][4][16];
+  float amax[4][256];
 };
 
 struct Tile {
@@ -151,6 +151,18 @@ __device__ __forceinline__ Tile decode_tile(int32_t t, const int32_t* tpre, cons
   return tl;
 }
 
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // SwiGLU epilogue of a two-block tile on one SM ("flops/deepgemm-grouped-
 // masked-moe-gemm", "Workarounds": the expert's SwiGLU runs between the two
 // grouped GEMMs, and the FP8 path hands the second GEMM per-128 UE8M0-scaled
@@ -158,54 +170,79 @@ __device__ __forceinline__ Tile decode_tile(int32_t t, const int32_t* tpre, cons
 // (gate rows of features 128j..128j+127, then their up rows), so block 0 of
 // tile nb holds the gate and block 1 the up values of features
 // 128nb..128nb+127 and the thread owning TMEM lane l has both halves of one
-// feature:  y = SiLU(g) * u = g / (1 + e^-g) * u  in fp32.
-//
-// To bf16: lane pairs exchange so each store writes two features.  To E4M3:
-// the scale of (token, 128 features) needs the maximum over all four lane
-// quadrants, held by the four warps of this half; each warp reduces its 32
-// features per token with a transposing butterfly (16 shuffles for 16
-// tokens), publishes them in shared memory and waits on an mbarrier that the
-// four warps' 128 threads complete (double-buffered by chunk parity, so one
-// barrier per chunk suffices).  Scale byte: the smallest s with
-// amax <= 448 * 2^(s-127), clamped to [1, 254], 127 for an all-zero block;
-// codes round y * 2^(127-s) to the nearest E4M3 value, saturating.
-// Returns false if a wait gave up.
-__device__ __forceinline__ bool swiglu_chunks(const Params& p, Shared& sh, const Tile& tl,
-                                              uint32_t taddr, uint32_t quad, int32_t half,
-                                              uint32_t lane, uint32_t& chunk, uint64_t deadline) {
+// feature:  y = SiLU(g) * u = g / (1 + e^-g) * u  in fp32.  The two warps of
+// a lane quadrant take alternate 16-token chunks, as in the plain epilogue.
+__device__ __forceinline__ float swiglu_f32(uint32_t g, uint32_t u) {
+  const float gf = __uint_as_float(g);
+  return __fdividef(gf, 1.0f + __expf(-gf)) * __uint_as_float(u);
+}
+
+// To bf16: lane pairs exchange so each store writes two features.
+__device__ __forceinline__ void swiglu_bf16_tile(const Params& p, const Tile& tl, uint32_t taddr,
+                                                 uint32_t quad, int32_t half, uint32_t lane) {
   const int32_t I = p.N >> 1;
   const int32_t f = tl.nb * kCtaRows + (int32_t)(quad * 32u + lane);  // this thread's feature
   const bool odd = (lane & 1u) != 0;
-  for (int32_t c0 = 16 * half; c0 < tl.qn; c0 += 32, ++chunk) {
+  __nv_bfloat16* ypair = static_cast<__nv_bfloat16*>(p.D) + (int64_t)tl.row0 * I + (f & ~1);
+  for (int32_t c0 = 16 * half; c0 < tl.qn; c0 += 32) {
     uint32_t g[16], u[16];
     tmem_ld16(taddr + (uint32_t)c0, g);
     tmem_ld16(taddr + kAccStride + (uint32_t)c0, u);
     tmem_ld_wait();
     tmem_regs_ready(g);
     tmem_regs_ready(u);
-    float y[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float gi = __uint_as_float(g[i]);
-      y[i] = __fdividef(gi, 1.0f + __expf(-gi)) * __uint_as_float(u[i]);
+    for (int i = 0; i < 16; i += 2) {
+      const float y0 = swiglu_f32(g[i], u[i]), y1 = swiglu_f32(g[i + 1], u[i + 1]);
+      const int32_t row = c0 + i + (odd ? 1 : 0);
+      const float mine = odd ? y1 : y0;
+      const float recv = __shfl_xor_sync(0xffffffffu, odd ? y0 : y1, 1);
+      const __nv_bfloat162 v = odd ? __floats2bfloat162_rn(recv, mine) : __floats2bfloat162_rn(mine, recv);
+      if (row < tl.rows) *reinterpret_cast<__nv_bfloat162*>(ypair + (int64_t)row * I) = v;
     }
-    if (p.epi == kEpiSwigluBf16) {
-      __nv_bfloat16* ypair = static_cast<__nv_bfloat16*>(p.D) + (int64_t)tl.row0 * I + (f & ~1);
-#pragma unroll
-      for (int i = 0; i < 16; i += 2) {
-        const int32_t row = c0 + i + (odd ? 1 : 0);
-        const float mine = odd ? y[i + 1] : y[i];
-        const float recv = __shfl_xor_sync(0xffffffffu, odd ? y[i] : y[i + 1], 1);
-        const __nv_bfloat162 v = odd ? __floats2bfloat162_rn(recv, mine) : __floats2bfloat162_rn(mine, recv);
-        if (row < tl.rows) *reinterpret_cast<__nv_bfloat162*>(ypair + (int64_t)row * I) = v;
-      }
-      continue;
-    }
-    // per-token maximum over the warp's 32 features: each step halves the
-    // live values; afterwards lanes 2t and 2t+1 hold token t's maximum
+  }
+}
+
+// To E4M3.  The scale of (token, 128 features) needs the maximum over all
+// four lane quadrants, held by the four warps of this half, so the tile is
+// drained in two passes with one exchange between them.  Pass 1: y of every
+// chunk goes back into TMEM over the gate values, and each warp reduces its
+// 32 features per token with a transposing butterfly (16 shuffles for 16
+// tokens) into shared memory.  Then the half's 128 threads complete an
+// mbarrier (bounded wait; one per tile, parity = tile count).  Pass 2: y is
+// read back, and per token the scale byte is the smallest s with
+// amax <= 448 * 2^(s-127), clamped to [1, 254] (127 for an all-zero block);
+// codes round y * 2^(127-s) to the nearest E4M3 value, saturating; a byte
+// transpose inside groups of four lanes turns each lane's 16 one-byte codes
+// (one feature, 16 tokens) into four 4-byte stores (four features of one
+// token), a quarter of the store instructions of byte stores.  The next
+// tile's pass 1 cannot start before every epilogue warp has released this
+// tile's accumulator, so one buffer of maxima suffices.  Returns false if
+// the wait gave up.
+__device__ __forceinline__ bool swiglu_fp8_tile(const Params& p, Shared& sh, const Tile& tl,
+                                                uint32_t taddr, uint32_t quad, int32_t half,
+                                                uint32_t lane, uint32_t tile_par, uint64_t deadline) {
+  const int32_t I = p.N >> 1;
+  const int32_t f = tl.nb * kCtaRows + (int32_t)(quad * 32u + lane);
+  const bool odd = (lane & 1u) != 0;
+  const int32_t t = (int32_t)(lane >> 1);
+  for (int32_t c0 = 16 * half; c0 < tl.qn; c0 += 32) {
+    uint32_t g[16], u[16];
+    tmem_ld16(taddr + (uint32_t)c0, g);
+    tmem_ld16(taddr + kAccStride + (uint32_t)c0, u);
+    tmem_ld_wait();
+    tmem_regs_ready(g);
+    tmem_regs_ready(u);
     float m[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) m[i] = fabsf(y[i]);
+    for (int i = 0; i < 16; ++i) {
+      const float y = swiglu_f32(g[i], u[i]);
+      g[i] = __float_as_uint(y);
+      m[i] = fabsf(y);
+    }
+    tmem_st16(taddr + (uint32_t)c0, g);
+    // each step halves the live values; afterwards lanes 2t and 2t+1 hold
+    // token t's maximum over the warp's 32 features
 #pragma unroll
     for (int w = 8; w >= 1; w >>= 1) {
       const bool hi = (lane & (uint32_t)(2 * w)) != 0;
@@ -217,13 +254,19 @@ __device__ __forceinline__ bool swiglu_chunks(const Params& p, Shared& sh, const
       }
     }
     m[0] = fmaxf(m[0], __shfl_xor_sync(0xffffffffu, m[0], 1));
-    const uint32_t par = chunk & 1u;
-    float* slot = &sh.amax[half][par][0][0];
-    const int32_t t = (int32_t)(lane >> 1);
-    if (!odd) slot[quad * 16u + (uint32_t)t] = m[0];
-    mbar_arrive(&sh.amax_bar[half]);
-    if (!warp_wait(&sh.amax_bar[half], par, deadline, &sh.abort_flag, p.status)) return false;
-    const float amax = fmaxf(fmaxf(slot[t], slot[16 + t]), fmaxf(slot[32 + t], slot[48 + t]));
+    if (!odd) sh.amax[quad][c0 + t] = m[0];
+  }
+  tmem_st_wait();
+  mbar_arrive(&sh.amax_bar[half]);
+  if (!warp_wait(&sh.amax_bar[half], tile_par, deadline, &sh.abort_flag, p.status)) return false;
+  uint8_t* yq4 = static_cast<uint8_t*>(p.D) + (int64_t)tl.row0 * I + (f & ~3);
+  for (int32_t c0 = 16 * half; c0 < tl.qn; c0 += 32) {
+    uint32_t y[16];
+    tmem_ld16(taddr + (uint32_t)c0, y);
+    tmem_ld_wait();
+    tmem_regs_ready(y);
+    const int32_t tok = c0 + t;
+    const float amax = fmaxf(fmaxf(sh.amax[0][tok], sh.amax[1][tok]), fmaxf(sh.amax[2][tok], sh.amax[3][tok]));
     // amax = 1.m * 2^(E-127); 448 = 1.75 * 2^8: s = E - 8, plus one when 1.m > 1.75
     const uint32_t bits = __float_as_uint(amax);
     int32_t sc = (int32_t)(bits >> 23) - 8 + ((bits & 0x7fffffu) > 0x600000u ? 1 : 0);
@@ -231,14 +274,34 @@ __device__ __forceinline__ bool swiglu_chunks(const Params& p, Shared& sh, const
     if (amax == 0.0f) sc = 127;
     // 2^(127-s): a normal float for s <= 253, the subnormal 2^-127 for s = 254
     const float inv = sc < 254 ? __uint_as_float((uint32_t)(254 - sc) << 23) : __uint_as_float(0x00400000u);
-    if (quad == 0 && !odd && c0 + t < tl.rows)
-      p.sfy[((int64_t)tl.sf_z * (I / kCtaRows) + tl.nb) * p.sfy_ld + tl.sf_x + c0 + t] = (uint8_t)sc;
-    uint8_t* yq = static_cast<uint8_t*>(p.D) + (int64_t)tl.row0 * I + f;
+    if (quad == 0 && !odd && tok < tl.rows)
+      p.sfy[((int64_t)tl.sf_z * (I / kCtaRows) + tl.nb) * p.sfy_ld + tl.sf_x + tok] = (uint8_t)sc;
+    // codes of tokens 4w..4w+3 of this lane's feature, one word per w
+    uint32_t wd[4];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float x = y[i] * __shfl_sync(0xffffffffu, inv, 2 * i);
-      const __nv_fp8_storage_t code = __nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
-      if (c0 + i < tl.rows) yq[(int64_t)(c0 + i) * I] = (uint8_t)code;
+    for (int w = 0; w < 4; ++w) {
+      float2 a, b;
+      a.x = __uint_as_float(y[4 * w]) * __shfl_sync(0xffffffffu, inv, 8 * w);
+      a.y = __uint_as_float(y[4 * w + 1]) * __shfl_sync(0xffffffffu, inv, 8 * w + 2);
+      b.x = __uint_as_float(y[4 * w + 2]) * __shfl_sync(0xffffffffu, inv, 8 * w + 4);
+      b.y = __uint_as_float(y[4 * w + 3]) * __shfl_sync(0xffffffffu, inv, 8 * w + 6);
+      const uint32_t lo = __nv_cvt_float2_to_fp8x2(a, __NV_SATFINITE, __NV_E4M3);
+      const uint32_t hi = __nv_cvt_float2_to_fp8x2(b, __NV_SATFINITE, __NV_E4M3);
+      wd[w] = (lo & 0xffffu) | (hi << 16);
+    }
+    // 4x4 byte transpose inside each group of four lanes (features 4a..4a+3):
+    // afterwards lane 4a+r holds, per w, the codes of token 4w+r for the
+    // group's four features, stored as one word
+    const bool b1 = (lane & 2u) != 0, b0 = (lane & 1u) != 0;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      uint32_t v = wd[w];
+      uint32_t r = __shfl_xor_sync(0xffffffffu, v, 2);
+      v = b1 ? __byte_perm(r, v, 0x7632) : __byte_perm(v, r, 0x5410);
+      r = __shfl_xor_sync(0xffffffffu, v, 1);
+      v = b0 ? __byte_perm(r, v, 0x7351) : __byte_perm(v, r, 0x6240);
+      const int32_t row = c0 + 4 * w + (int32_t)(lane & 3u);
+      if (row < tl.rows) *reinterpret_cast<uint32_t*>(yq4 + (int64_t)row * I) = v;
     }
   }
   return true;
@@ -680,7 +743,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     with_blocks([&](auto bc) {
     constexpr int kB = decltype(bc)::value;
     uint32_t acc = 0, acc_phase = 0;
-    uint32_t chunk = 0;  // SwiGLU to E4M3: chunks done, for the exchange barrier's phase
+    uint32_t tile_par = 0;  // SwiGLU to E4M3: parity of tiles done, the exchange barrier's phase
     for (int32_t t = unit; S > 0 && t < total; t += n_units) {
       const Tile tl = decode_tile(t, tpre, cnt, rowbase, E, NB, q, p.masked);
       if (!warp_wait(&sh.acc_full[acc], acc_phase, deadline, &sh.abort_flag, p.status)) break;
@@ -689,7 +752,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool swiglu = false;
       if constexpr (kB == 2 && !kPair) swiglu = p.epi != kEpiPlain;
       if (swiglu) {
-        if (!swiglu_chunks(p, sh, tl, taddr, quad, half, lane, chunk, deadline)) break;
+        if (p.epi == kEpiSwigluBf16) {
+          swiglu_bf16_tile(p, tl, taddr, quad, half, lane);
+        } else if (!swiglu_fp8_tile(p, sh, tl, taddr, quad, half, lane, tile_par, deadline)) {
+          break;
+        }
+        tile_par ^= 1u;
       } else {
         // this thread's output column of block 0; block b is b * kBlockRows further
         const int32_t n = tl.nb * tile_rows + (int32_t)(rank * kCtaRows + quad * 32 + lane);

@@ -262,6 +262,16 @@ WORKLOADS: Dict[str, dict] = {
         form="contiguous", dtype="fp8", E=64, N=4096, K=7168, align_q=128, seed=1004,
         a_std=1.0, b_std=1.0, counts=counts_zipf_prefill,
         second=dict(N=7168, K=2048)),
+    # the same two GEMMs as one expert FFN: GEMM1's SwiGLU epilogue writes the
+    # E4M3 activations (and scales) that GEMM2 reads
+    "prefill_ffn_fp8_e64_t32768_n4096_k7168": dict(
+        form="contiguous", dtype="fp8", E=64, N=4096, K=7168, align_q=128, seed=1004,
+        a_std=1.0, b_std=7168 ** -0.5, counts=counts_zipf_prefill,
+        second=dict(N=7168, K=2048), swiglu=True),
+    "prefill_ffn_fp8_e16_t8192_n4096_k7168": dict(
+        form="contiguous", dtype="fp8", E=16, N=4096, K=7168, align_q=128, seed=1006,
+        a_std=1.0, b_std=7168 ** -0.5, counts=lambda: counts_zipf_prefill(seed=1006, E=16, total=8192),
+        second=dict(N=7168, K=2048), swiglu=True),
     "prefill_bf16_e64_t32768_n4096_k7168": dict(
         form="contiguous", dtype="bf16", E=64, N=4096, K=7168, align_q=128, seed=1004,
         a_std=7168 ** -0.5, b_std=7168 ** -0.5, counts=counts_zipf_prefill,
