@@ -120,3 +120,30 @@ def test_swapped_gate_and_up_is_caught(monkeypatch):
     orig = oe.gate_up_halves
     monkeypatch.setattr(oe, "gate_up_halves", lambda H: orig(H)[::-1])
     assert fails(te.test_gate_up_halves_layout)
+
+
+
+def test_e2m1_wrong_bias_is_caught(monkeypatch):
+    orig = on.decode_e2m1
+    monkeypatch.setattr(on, "decode_e2m1", lambda c: orig(c) * 2.0)
+    assert fails(tn.test_e2m1_all_codes)
+
+
+def test_mx4_nibble_swap_is_caught(monkeypatch):
+    def bad(packed):
+        p = np.asarray(packed, dtype=np.uint8)
+        out = np.empty(p.shape[:-1] + (2 * p.shape[-1],), dtype=np.uint8)
+        out[..., 0::2] = p >> 4
+        out[..., 1::2] = p & 0xF
+        return out
+    monkeypatch.setattr(on, "unpack_e2m1", bad)
+    assert fails(tn.test_unpack_e2m1_nibble_order)
+    assert fails(tn.test_dequant_weight_mx4_brute_force)
+
+
+def test_mx4_scale_granularity_is_caught(monkeypatch):
+    def bad(packed, sf):
+        codes = on.unpack_e2m1(packed)
+        return on.decode_e2m1(codes) * np.repeat(on.decode_ue8m0(sf), 32, axis=1)[:, ::-1]
+    monkeypatch.setattr(on, "dequant_weight_mx4", bad)
+    assert fails(tn.test_dequant_weight_mx4_brute_force)

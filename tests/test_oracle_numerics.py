@@ -80,3 +80,55 @@ def test_power_of_two_scale_shifts_exactly():
     shifted = on.dequant_weight(codes, sf2)
     assert np.array_equal(shifted[:, :128], base[:, :128])
     assert np.array_equal(shifted[:, 128:], base[:, 128:] * 8.0)
+
+
+# ---- FP4 E2M1 with per-32 UE8M0 scales
+def _minifloat(code, ebits, mbits, bias):
+    """Generic sign/exponent/mantissa decoder (no NaN/inf handling), checked
+    against torch on two FP8 formats below and then applied to E2M1."""
+    sign = (code >> (ebits + mbits)) & 1
+    e = (code >> mbits) & ((1 << ebits) - 1)
+    m = code & ((1 << mbits) - 1)
+    if e == 0:
+        v = m * 2.0 ** (1 - bias - mbits)
+    else:
+        v = (1 + m * 2.0 ** -mbits) * 2.0 ** (e - bias)
+    return -v if sign else v
+
+
+def test_generic_minifloat_matches_torch_fp8():
+    for dt, eb, mb_, bias in ((torch.float8_e4m3fn, 4, 3, 7), (torch.float8_e5m2, 5, 2, 15)):
+        codes = np.arange(256, dtype=np.uint8)
+        ref = torch.from_numpy(codes).view(dt).to(torch.float64).numpy()
+        for c in range(256):
+            if np.isfinite(ref[c]):
+                assert _minifloat(c, eb, mb_, bias) == ref[c], (dt, c)
+
+
+def test_e2m1_all_codes():
+    codes = np.arange(16)
+    got = on.decode_e2m1(codes)
+    want = np.array([_minifloat(int(c), 2, 1, 1) for c in codes])
+    assert np.array_equal(got, want)
+    # the published E2M1 value set: largest finite magnitude 6, smallest 0.5
+    assert sorted(set(np.abs(got).tolist())) == [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    assert np.array_equal(got[8:], -got[:8])
+
+
+def test_unpack_e2m1_nibble_order():
+    packed = np.array([[0x21, 0xF3]], dtype=np.uint8)
+    assert on.unpack_e2m1(packed).tolist() == [[0x1, 0x2, 0x3, 0xF]]
+
+
+def test_dequant_weight_mx4_brute_force():
+    rng = np.random.default_rng(12)
+    N, K = 6, 128
+    packed = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    sf = rng.integers(110, 140, (N, K // 32), dtype=np.uint8)
+    got = on.dequant_weight_mx4(packed, sf)
+    for n in range(N):
+        for k in range(K):
+            byte = int(packed[n, k // 2])
+            code = (byte >> 4) if k % 2 else (byte & 0xF)
+            v = _minifloat(code, 2, 1, 1) * 2.0 ** (int(sf[n, k // 32]) - 127)
+            assert got[n, k] == v
