@@ -190,7 +190,8 @@ class Contiguous:
     def __init__(self, name, dev):
         spec = wl.WORKLOADS[name]
         self.name, self.spec, self.dev = name, spec, dev
-        self.fp8 = spec["dtype"] == "fp8"
+        self.fp8 = spec["dtype"] in ("fp8", "fp8xfp4")
+        self.w4 = spec["dtype"] == "fp8xfp4"      # E2M1 weights, one scale per (row, 32 K)
         self.counts = spec["counts"]()
         self.E = spec["E"]
         self.align = spec["align_q"]
@@ -223,7 +224,7 @@ class Contiguous:
         self.offsets = torch.empty(self.E + 1, dtype=torch.int64, device=dev)
         self.stats = torch.empty(48, dtype=torch.uint8, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.dtype = mb.MG_FP8_E4M3_UE8M0 if self.fp8 else mb.MG_BF16
+        self.dtype = mb.MG_FP8_X_FP4_E2M1 if self.w4 else (mb.MG_FP8_E4M3_UE8M0 if self.fp8 else mb.MG_BF16)
         self.elem = 1 if self.fp8 else 2
 
     def flops(self):
@@ -235,9 +236,10 @@ class Contiguous:
         act = sum(1 for t in self.counts if t > 0)
         N, K = g["N"], g["K"]
         out = self.U * (N // 2 + N // 256) if g["swiglu"] else self.U * N * 2   # E4M3 Y + scales, or bf16 D
-        b = act * N * K * self.elem + self.U * K * self.elem + out
+        w = act * (N * K // 2 + N * K // 32) if self.w4 else act * N * K * self.elem
+        b = w + self.U * K * self.elem + out
         if self.fp8:
-            b += act * (K // 128) * (N // 128) + self.U * (K // 128)
+            b += self.U * (K // 128) + (0 if self.w4 else act * (K // 128) * (N // 128))
         return b
 
     def launches_per_step(self):
@@ -306,7 +308,7 @@ class Contiguous:
         d = {"workload": self.name, "form": "contiguous", "experts": self.E, "assignments": self.U,
              "align_q": self.align, "rows_cap": self.rows_cap, "tile_q": "device-selected",
              "gemms": [f"N={g['N']},K={g['K']}" for g in self.gemms],
-             "operands": "e4m3 + ue8m0 per-128 scales" if self.fp8 else "bf16",
+             "operands": operands_label(self.fp8, self.w4),
              "l2": "inputs larger than L2 (no flush)"}
         if self.swiglu:
             d["epilogue"] = "GEMM1: SwiGLU of interleaved gate/up blocks, re-quantised to e4m3 + ue8m0; feeds GEMM2"
@@ -338,7 +340,8 @@ class Contiguous:
                 else:
                     a = on.decode_bf16(h["A"][o:o + t].view(torch.int16).numpy().view(np.uint16))
                 if self.fp8:
-                    b = on.dequant_weight(g["B"][e].cpu().numpy(), g["SFB"][e].cpu().numpy())
+                    deq_w = on.dequant_weight_mx4 if self.w4 else on.dequant_weight
+                    b = deq_w(g["B"][e].cpu().numpy(), g["SFB"][e].cpu().numpy())
                 else:
                     b = on.decode_bf16(g["B"][e].cpu().view(torch.int16).numpy().view(np.uint16))
                 r = og.expert_product(a, b)
@@ -353,7 +356,8 @@ class Masked:
     def __init__(self, name, dev):
         spec = wl.WORKLOADS[name]
         self.name, self.spec = name, spec
-        self.fp8 = spec["dtype"] == "fp8"
+        self.fp8 = spec["dtype"] in ("fp8", "fp8xfp4")
+        self.w4 = spec["dtype"] == "fp8xfp4"      # E2M1 weights, one scale per (row, 32 K)
         self.E, self.M, self.N, self.K = spec["E"], spec["M_max"], spec["N"], spec["K"]
         self.counts = spec["counts"]()
         self.U = sum(self.counts)
@@ -362,7 +366,7 @@ class Masked:
         self.D = torch.empty((self.E, self.M, self.N), dtype=torch.bfloat16, device=dev)
         self.d_counts = torch.tensor(self.counts, dtype=torch.int32, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.dtype = mb.MG_FP8_E4M3_UE8M0 if self.fp8 else mb.MG_BF16
+        self.dtype = mb.MG_FP8_X_FP4_E2M1 if self.w4 else (mb.MG_FP8_E4M3_UE8M0 if self.fp8 else mb.MG_BF16)
         self.elem = 1 if self.fp8 else 2
         self.gemms = [dict(N=self.N, K=self.K)]
 
@@ -374,9 +378,11 @@ class Masked:
 
     def bytes_alg(self):
         act = sum(1 for t in self.counts if t > 0)
-        b = act * self.N * self.K * self.elem + self.U * self.K * self.elem + self.U * self.N * 2
+        N, K = self.N, self.K
+        w = act * (N * K // 2 + N * K // 32) if self.w4 else act * N * K * self.elem
+        b = w + self.U * K * self.elem + self.U * N * 2
         if self.fp8:
-            b += act * (self.K // 128) * (self.N // 128) + self.U * (self.K // 128)
+            b += self.U * (K // 128) + (0 if self.w4 else act * (K // 128) * (N // 128))
         return b
 
     def step(self, lib, stream, ev=None):
@@ -414,7 +420,7 @@ class Masked:
     def config(self):
         return {"workload": self.name, "form": "masked", "experts": self.E, "M_max": self.M,
                 "valid_rows": self.U, "N": self.N, "K": self.K,
-                "operands": "e4m3 + ue8m0 per-128 scales" if self.fp8 else "bf16",
+                "operands": operands_label(self.fp8, self.w4),
                 "l2": "inputs larger than L2 (no flush)"}
 
     def oracle_sample(self, experts):
@@ -428,7 +434,8 @@ class Masked:
                 continue
             if self.fp8:
                 a = on.dequant_rows(self.A[e, :v].cpu().numpy(), self.SFA[e][:, :v].cpu().numpy())
-                b = on.dequant_weight(self.B[e].cpu().numpy(), self.SFB[e].cpu().numpy())
+                deq_w = on.dequant_weight_mx4 if self.w4 else on.dequant_weight
+                b = deq_w(self.B[e].cpu().numpy(), self.SFB[e].cpu().numpy())
             else:
                 a = on.decode_bf16(self.A[e, :v].cpu().view(torch.int16).numpy().view(np.uint16))
                 b = on.decode_bf16(self.B[e].cpu().view(torch.int16).numpy().view(np.uint16))
@@ -529,6 +536,12 @@ def blas_threads():
     except Exception:
         pass
     return len(os.sched_getaffinity(0))
+
+
+def operands_label(fp8, w4):
+    if w4:
+        return "e4m3 + ue8m0 per (row, 128 K) x e2m1 weights + ue8m0 per (row, 32 K)"
+    return "e4m3 + ue8m0 per-128 scales" if fp8 else "bf16"
 
 
 def sample_steps(w):
@@ -633,7 +646,8 @@ def run_ours(args):
         "metric": "effective TFLOPS (valid rows only)",
         "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_max / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "e4m3" if w.fp8 else "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": ("e4m3xe2m1" if getattr(w, "w4", False) else "e4m3") if w.fp8 else "bf16",
+        "data": "synthetic",
         "config": dict(w.config(), kernel_policy=args.kernel_policy),
         "per_gemm_ms": per_gemm,
         "roofline": roof,

@@ -55,7 +55,9 @@ typedef enum {
 
 typedef enum {
   MG_BF16 = 0,             /* bf16 operands, fp32 accumulate                   */
-  MG_FP8_E4M3_UE8M0 = 1    /* E4M3 operands with UE8M0 per-128 block scales    */
+  MG_FP8_E4M3_UE8M0 = 1,   /* E4M3 operands with UE8M0 per-128 block scales    */
+  MG_FP8_X_FP4_E2M1 = 2    /* E4M3 activations as above x E2M1 (FP4) weights
+                              with one UE8M0 scale per (row, 32 K)             */
 } mg_dtype;
 
 /* Padding accounting of one histogram at one token tile q ("MoE GroupGEMM
@@ -170,7 +172,19 @@ mg_status moe_select_tile_host(mg_dtype dt, const int32_t* counts, int32_t E,
  *            on it.
  *
  * Value of an E4M3 element: e4m3(x) * 2^(s-127) with s its block's scale
- * byte.  Device errors: t_e < 0 -> MG_ERR_DEVICE_ARG (expert skipped);
+ * byte.
+ *
+ * FP8 x FP4 (dt = MG_FP8_X_FP4_E2M1; "flops/deepgemm-grouped-masked-moe-
+ * gemm", "Workarounds": FP8xFP4 linear layers; the weight format follows the
+ * OCP Microscaling convention, the pages give none).  A and SFA as for
+ * E4M3.  B is uint8 [E, N, K/2]: two E2M1 codes per byte, element 2i of a
+ * row in the low nibble of byte i, value (-1)^s * {0, 0.5, 1, 1.5, 2, 3, 4,
+ * 6}.  SFB is uint8 [E, N, K/32]: the UE8M0 scale of (weight row, 32
+ * consecutive K).  K must be a multiple of 512 (else MG_ERR_UNSUPPORTED) and
+ * B 32-byte aligned.  Weight bytes read from HBM are half those of E4M3.
+ * The SM-pair kernel families are not used (policies 3 and 4 run 2).
+ *
+ * Device errors: t_e < 0 -> MG_ERR_DEVICE_ARG (expert skipped);
  * aligned segments beyond rows_cap -> MG_ERR_CAPACITY (experts that do not
  * fit are skipped).
  * ------------------------------------------------------------------------ */
@@ -192,8 +206,8 @@ mg_status mgemm_contiguous(mg_dtype dt, const void* A, const uint8_t* SFA,
  * Rows r >= v_e are not written; experts with v_e = 0 load nothing.
  *
  *   A     [E, M_max, K]    bf16 or E4M3 bytes.
- *   SFA   uint8 [E, K/128, M_max] (fp8 only; M_max a multiple of 16).
- *   B, SFB  as for mgemm_contiguous.
+ *   SFA   uint8 [E, K/128, M_max] (fp8 and fp8 x fp4; M_max a multiple of 16).
+ *   B, SFB  as for mgemm_contiguous (all three dtypes).
  *   D     [E, M_max, N]    bf16.
  *   E*M_max must be < 2^31.
  * Device errors: v_e < 0 or v_e > M_max -> MG_ERR_DEVICE_ARG (expert

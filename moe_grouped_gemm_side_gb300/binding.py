@@ -17,7 +17,7 @@ STATUS_NAMES = {
     0: "MG_OK", 1: "MG_ERR_INVALID_ARG", 2: "MG_ERR_UNSUPPORTED", 3: "MG_ERR_CUDA",
     4: "MG_ERR_CAPACITY", 5: "MG_ERR_TIMEOUT", 6: "MG_ERR_DEVICE_ARG",
 }
-MG_BF16, MG_FP8_E4M3_UE8M0 = 0, 1
+MG_BF16, MG_FP8_E4M3_UE8M0, MG_FP8_X_FP4_E2M1 = 0, 1, 2
 MG_SWIGLU_BF16, MG_SWIGLU_FP8_E4M3_UE8M0 = 1, 2
 
 # Every function the header declares, with its ctypes signature.
@@ -110,6 +110,14 @@ def _dtype_of(A):
     raise TypeError(f"unsupported operand dtype {A.dtype}")
 
 
+def _fwd_dtype(A, B, K):
+    """E4M3 activations with packed E2M1 weights ([E, N, K/2]) are FP8 x FP4."""
+    dt = _dtype_of(A)
+    if dt == MG_FP8_E4M3_UE8M0 and 2 * B.shape[-1] == K:
+        return MG_FP8_X_FP4_E2M1
+    return dt
+
+
 def status_str(code: int) -> str:
     return load().mg_status_str(code).decode()
 
@@ -181,7 +189,7 @@ def mgemm_contiguous(A, B, D, d_counts, align_q: int, SFA=None, SFB=None, tile_q
     rows_cap, K = A.shape
     E, N, _ = B.shape
     _check("mgemm_contiguous", lib.mgemm_contiguous(
-        _dtype_of(A), _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(D), _ptr(d_counts), E,
+        _fwd_dtype(A, B, K), _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(D), _ptr(d_counts), E,
         rows_cap, N, K, align_q, tile_q, _ptr(status), _stream(stream)))
 
 
@@ -190,7 +198,7 @@ def mgemm_masked(A, B, D, d_valid_m, SFA=None, SFB=None, status=None, stream=Non
     E, M_max, K = A.shape
     N = B.shape[1]
     _check("mgemm_masked", lib.mgemm_masked(
-        _dtype_of(A), _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(D), _ptr(d_valid_m), E,
+        _fwd_dtype(A, B, K), _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(D), _ptr(d_valid_m), E,
         M_max, N, K, _ptr(status), _stream(stream)))
 
 
@@ -211,7 +219,7 @@ def mgemm_contiguous_swiglu(A, B, Y, d_counts, align_q: int, SFA=None, SFB=None,
     rows_cap, K = A.shape
     E, N, _ = B.shape
     _check("mgemm_contiguous_swiglu", lib.mgemm_contiguous_swiglu(
-        _dtype_of(A), _swiglu_out(Y), _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(Y), _ptr(SFY),
+        _fwd_dtype(A, B, K), _swiglu_out(Y), _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(Y), _ptr(SFY),
         _ptr(d_counts), E, rows_cap, N, K, align_q, tile_q, _ptr(status), _stream(stream)))
 
 
@@ -221,7 +229,7 @@ def mgemm_masked_swiglu(A, B, Y, d_valid_m, SFA=None, SFB=None, SFY=None, status
     E, M_max, K = A.shape
     N = B.shape[1]
     _check("mgemm_masked_swiglu", lib.mgemm_masked_swiglu(
-        _dtype_of(A), _swiglu_out(Y), _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(Y), _ptr(SFY),
+        _fwd_dtype(A, B, K), _swiglu_out(Y), _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(Y), _ptr(SFY),
         _ptr(d_valid_m), E, M_max, N, K, _ptr(status), _stream(stream)))
 
 

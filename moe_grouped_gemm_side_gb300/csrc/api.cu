@@ -27,15 +27,18 @@ std::atomic<int32_t> g_policy{0};
 // block-scaled fp8 path).  Policies 1-4 force single, dual, pair or
 // pair-dual, falling back to the widest family N allows when N is not a
 // multiple of the family's tile rows.
-int fwd_variant(int32_t N) {
+int fwd_variant(int32_t N, bool w4 = false) {
   const int32_t pol = g_policy.load();
   int v = pol == 0 ? kFwdDual : pol == 1 ? kFwdSingle : pol == 2 ? kFwdDual : pol == 3 ? kFwdPair : kFwdPairDual;
+  if (w4 && (v == kFwdPair || v == kFwdPairDual)) v = kFwdDual;  // FP4 weights: single-SM families
   if (v == kFwdPairDual && N % 512 != 0) v = kFwdPair;
   if ((v == kFwdPair || v == kFwdDual) && N % 256 != 0) v = kFwdSingle;
   return v;
 }
 
-cudaError_t launch_fwd_any(const FwdArgs& a, cudaStream_t s) { return launch_fwd(a, s, fwd_variant(a.N)); }
+cudaError_t launch_fwd_any(const FwdArgs& a, cudaStream_t s) {
+  return launch_fwd(a, s, fwd_variant(a.N, a.w4));
+}
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -56,6 +59,22 @@ EncodeTiledFn encode_fn() {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Tensor map over a row-major [outer, inner] matrix, rows `row_bytes` apart.
+mg_status encode_2d_rows(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                         uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                         CUtensorMapSwizzle swz) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return MG_ERR_CUDA;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  const CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MG_OK : MG_ERR_CUDA;
+}
 
 // Tensor map over a row-major [outer, inner] matrix of `elem`-byte elements.
 mg_status encode_2d(CUtensorMap* m, CUtensorMapDataType dt, uint32_t elem, const void* base,
@@ -92,14 +111,17 @@ mg_status encode_sf_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d
 
 mg_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MG_OK : MG_ERR_CUDA; }
 
-bool valid_dtype(mg_dtype dt) { return dt == MG_BF16 || dt == MG_FP8_E4M3_UE8M0; }
+bool valid_dtype(mg_dtype dt) {
+  return dt == MG_BF16 || dt == MG_FP8_E4M3_UE8M0 || dt == MG_FP8_X_FP4_E2M1;
+}
+bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 
 // Operand checks shared by the contiguous and masked forms.
 mg_status check_fwd_common(mg_dtype dt, const void* A, const uint8_t* SFA, const void* B,
                            const uint8_t* SFB, const void* D, const int32_t* counts, int32_t E,
                            int32_t N, int32_t K) {
   if (!valid_dtype(dt)) return MG_ERR_INVALID_ARG;
-  const bool fp8 = dt == MG_FP8_E4M3_UE8M0;
+  const bool fp8 = dt != MG_BF16;
   if (A == nullptr || B == nullptr || D == nullptr || counts == nullptr) return MG_ERR_INVALID_ARG;
   if (fp8 && (SFA == nullptr || SFB == nullptr)) return MG_ERR_INVALID_ARG;
   if (E <= 0 || N <= 0 || K <= 0) return MG_ERR_INVALID_ARG;
@@ -110,6 +132,12 @@ mg_status check_fwd_common(mg_dtype dt, const void* A, const uint8_t* SFA, const
   if (!aligned16(A) || !aligned16(B) || !aligned16(D) || !aligned16(counts))
     return MG_ERR_INVALID_ARG;
   if (fp8 && (!aligned16(SFA) || !aligned16(SFB))) return MG_ERR_INVALID_ARG;
+  if (dt == MG_FP8_X_FP4_E2M1) {
+    // weight-scale rows (K/32 bytes) must be whole 16-byte units for TMA;
+    // packed 4-bit weights need a 32-byte aligned base
+    if (K % 512 != 0) return MG_ERR_UNSUPPORTED;
+    if (!aligned32(B)) return MG_ERR_INVALID_ARG;
+  }
   return MG_OK;
 }
 
@@ -122,8 +150,20 @@ mg_status encode_operands(FwdArgs& a, const void* A, const uint8_t* SFA, const v
   const uint32_t elem = a.fp8 ? 1 : 2;
   const uint32_t box_k = 128 / elem;  // one 128-byte swizzle row
   mg_status st;
-  st = encode_2d(&a.tmW, dt, elem, B, (uint64_t)a.K, (uint64_t)a.E * a.N, box_k, 128,
-                 CU_TENSOR_MAP_SWIZZLE_128B);
+  if (a.w4) {
+    // packed E2M1: TMA spreads each 16 codes (8 bytes) over 16 bytes of
+    // shared memory, the operand layout of kind::mxf8f6f4, so a 128-code box
+    // fills one 128-byte swizzle row like E4M3
+    st = encode_2d_rows(&a.tmW, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, B, (uint64_t)a.K,
+                        (uint64_t)a.E * a.N, (uint64_t)a.K / 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != MG_OK) return st;
+    st = encode_2d_rows(&a.tmSFW, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.sfb, (uint64_t)a.K / 32,
+                        (uint64_t)a.E * a.N, (uint64_t)a.K / 32, 16, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
+  } else {
+    st = encode_2d(&a.tmW, dt, elem, B, (uint64_t)a.K, (uint64_t)a.E * a.N, box_k, 128,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
+    std::memset(&a.tmSFW, 0, sizeof(a.tmSFW));
+  }
   if (st != MG_OK) return st;
   st = encode_2d(&a.tmA64, dt, elem, A, (uint64_t)a.K, (uint64_t)rows_total, box_k, 64,
                  CU_TENSOR_MAP_SWIZZLE_128B);
@@ -150,7 +190,7 @@ mg_status prep_contiguous(FwdArgs& a, mg_dtype dt, const void* A, const uint8_t*
                           int32_t* d_status) {
   mg_status st = check_fwd_common(dt, A, SFA, B, SFB, D, d_counts, E, N, K);
   if (st != MG_OK) return st;
-  const bool fp8 = dt == MG_FP8_E4M3_UE8M0;
+  const bool fp8 = dt != MG_BF16;
   if (rows_cap <= 0 || rows_cap >= (int64_t(1) << 31) || align_q <= 0) return MG_ERR_INVALID_ARG;
   if (fp8 && (align_q % 16 != 0 || rows_cap % 16 != 0)) return MG_ERR_UNSUPPORTED;
   if (tile_q != 0) {
@@ -158,6 +198,7 @@ mg_status prep_contiguous(FwdArgs& a, mg_dtype dt, const void* A, const uint8_t*
     if (fp8 && tile_q > 240 && tile_q != 256) return MG_ERR_INVALID_ARG;
   }
   a.fp8 = fp8;
+  a.w4 = dt == MG_FP8_X_FP4_E2M1;
   a.masked = false;
   a.counts = d_counts;
   a.E = E;
@@ -178,10 +219,11 @@ mg_status prep_masked(FwdArgs& a, mg_dtype dt, const void* A, const uint8_t* SFA
                       int32_t N, int32_t K, int32_t* d_status) {
   mg_status st = check_fwd_common(dt, A, SFA, B, SFB, D, d_valid_m, E, N, K);
   if (st != MG_OK) return st;
-  const bool fp8 = dt == MG_FP8_E4M3_UE8M0;
+  const bool fp8 = dt != MG_BF16;
   if (M_max <= 0 || (int64_t)E * M_max >= (int64_t(1) << 31)) return MG_ERR_INVALID_ARG;
   if (fp8 && M_max % 16 != 0) return MG_ERR_UNSUPPORTED;
   a.fp8 = fp8;
+  a.w4 = dt == MG_FP8_X_FP4_E2M1;
   a.masked = true;
   a.counts = d_valid_m;
   a.E = E;
@@ -283,7 +325,7 @@ mg_status moe_select_tile(mg_dtype dt, const int32_t* d_counts, int32_t E, int32
   if (!valid_dtype(dt) || d_counts == nullptr || d_tile_q == nullptr) return MG_ERR_INVALID_ARG;
   if (E <= 0 || N <= 0 || K <= 0) return MG_ERR_INVALID_ARG;
   if (N % 128 != 0 || K % 128 != 0) return MG_ERR_UNSUPPORTED;
-  return from_cuda(launch_select(dt == MG_FP8_E4M3_UE8M0, fwd_variant(N), d_counts, E, N, K,
+  return from_cuda(launch_select(dt != MG_BF16, fwd_variant(N, dt == MG_FP8_X_FP4_E2M1), d_counts, E, N, K,
                                  d_tile_q, d_status, static_cast<cudaStream_t>(stream)));
 }
 
@@ -292,12 +334,12 @@ mg_status moe_select_tile_host(mg_dtype dt, const int32_t* counts, int32_t E, in
   if (!valid_dtype(dt) || counts == nullptr || tile_q == nullptr) return MG_ERR_INVALID_ARG;
   if (E <= 0 || N <= 0 || K <= 0) return MG_ERR_INVALID_ARG;
   if (N % 128 != 0 || K % 128 != 0) return MG_ERR_UNSUPPORTED;
-  const bool fp8 = dt == MG_FP8_E4M3_UE8M0;
+  const bool fp8 = dt != MG_BF16;
   int64_t tiles[kNumTileCand] = {};
   for (int i = 0; i < kNumTileCand; ++i)
     for (int32_t e = 0; e < E; ++e) tiles[i] += cdiv64(counts[e] > 0 ? counts[e] : 0, tile_candidate(fp8, i));
   const int sms = num_sms > 0 ? num_sms : 152;
-  *tile_q = pick_tile(fp8, tiles, fwd_variant(N), N, sel_kblocks(fp8, K), sms);
+  *tile_q = pick_tile(fp8, tiles, fwd_variant(N, dt == MG_FP8_X_FP4_E2M1), N, sel_kblocks(fp8, K), sms);
   return MG_OK;
 }
 

@@ -61,6 +61,16 @@ constexpr int kSfRaw = kSfRawBytes;              // [4][256] token scale bytes
 // weight words of block 1
 constexpr int kSfStage = kSfStageBytes + 512;
 constexpr int kSfW1 = kSfStageBytes;             // offset of block-1 weight words
+// FP4 weights, per stage after the fp8 scale area: each block's scale box
+// as loaded (128 rows x 16 bytes: K-blocks kb..kb+3 of the stage's group,
+// four 32-K sub-blocks each), then each block's TMEM scale atom for the
+// stage's K-block (32 lanes x 16 bytes: lane i, word j = the four sub-block
+// scales of row i + 32 j), the layout tcgen05.cp.32x128b.warpx4 expects.
+constexpr int kWsfBytes = kCtaRows * 16;
+constexpr int kWsfAtom = 32 * 16;
+constexpr int kWsfArea = 2 * kWsfBytes + 2 * kWsfAtom;
+static_assert(kSfStage % 1024 == 0 && kWsfBytes % 1024 == 0 && kWsfAtom % 16 == 0,
+              "TMA and tcgen05.cp sources stay aligned");
 constexpr int kGroupTiles = 8;                   // token tiles per raster group
 // Token-tile widths the producer publishes for the MMA thread, one slot per
 // tile; more slots than stages, so a slot is rewritten only after the MMA
@@ -150,6 +160,9 @@ __device__ __forceinline__ Tile decode_tile(int32_t t, const int32_t* tpre, cons
   tl.sf_z = masked ? lo : 0;
   return tl;
 }
+
+// kind::mxf8f6f4 instruction-descriptor A format E2M1 (FP4), bits 7-9.
+constexpr uint32_t kIdescAE2M1 = 5u << 7;
 
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
@@ -307,12 +320,14 @@ __device__ __forceinline__ bool swiglu_fp8_tile(const Params& p, Shared& sh, con
   return true;
 }
 
-template <int kBlocks, bool kPair>
+template <int kBlocks, bool kPair, bool kW4>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA64,
                const __grid_constant__ CUtensorMap tmA16, const __grid_constant__ CUtensorMap tmA8,
-               const __grid_constant__ CUtensorMap tmSF, const Params p) {
+               const __grid_constant__ CUtensorMap tmSF, const __grid_constant__ CUtensorMap tmSFW,
+               const Params p) {
   static_assert(kBlocks == 1 || kBlocks == 2, "one or two weight blocks per tile");
+  static_assert(!(kW4 && kPair), "FP4 weights run on single-SM tiles");
   constexpr int kBlockRows = kPair ? 2 * kCtaRows : kCtaRows;  // rows of one weight block (MMA M)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -481,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   // token rows this CTA stages per tile: all of them, or its half of a pair
   const int32_t stage_bytes = nblk * kWTileBytes + (kPair ? sh.qn_max / 2 : sh.qn_max) * kRowBytes;
-  const int32_t sf_bytes = p.fp8 ? kSfStage : 0;
+  const int32_t sf_bytes = p.fp8 ? kSfStage + (kW4 ? kWsfArea : 0) : 0;
   const int32_t avail = kSmemBytes - 1024 - (int32_t)(reinterpret_cast<uintptr_t>(sf_area) -
                                                      reinterpret_cast<uintptr_t>(smem)) - 1024;
   int32_t S = avail / (stage_bytes + sf_bytes);
@@ -501,6 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmA16);
       if (kPair) tma_prefetch_desc(&tmA8);
       if (p.fp8) tma_prefetch_desc(&tmSF);
+      if (kW4) tma_prefetch_desc(&tmSFW);
       uint32_t stage = 0, phase = 0;
       int64_t issued = 0;
       bool ok = true;
@@ -513,7 +529,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int32_t qc = kPair ? tl.qn >> 1 : tl.qn;   // token rows staged here
         const int32_t wy = tl.e * p.N + tl.nb * tile_rows + (int32_t)rank * kCtaRows;
         const int32_t ty = tl.row0 + (int32_t)rank * qc;
-        const uint32_t bytes = (kPair ? 2u : 1u) * (uint32_t)(nblk * kWTileBytes + qc * kRowBytes);
+        // A packed E2M1 box counts its 8 KB of global data toward the barrier,
+        // although it fills 16 KB of shared memory
+        const int32_t w_tx = kW4 ? kWTileBytes / 2 : kWTileBytes;
+        const uint32_t bytes = (kPair ? 2u : 1u) * (uint32_t)(nblk * w_tx + qc * kRowBytes);
         for (int32_t kb = 0; kb < KB; ++kb) {
           const bool group = p.fp8 && (kb % kSfGroup) == 0;
           if (!wait_bounded(&sh.empty[stage], phase ^ 1u, deadline, &sh.abort_flag, p.status)) {
@@ -531,8 +550,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           // first: the 1 KB lands well before the operands, so warp 6 builds
           // the scale words while the operands are still in flight.
           if (p.fp8) {
-            mbar_arrive_expect_tx(&sh.sf_full[stage], group ? (uint32_t)kSfRaw : 0u);
-            if (group) tma_load_3d(sf_area + (size_t)stage * kSfStage, &tmSF, &sh.sf_full[stage], tl.sf_x, kb, tl.sf_z);
+            uint8_t* sfs = sf_area + (size_t)stage * sf_bytes;
+            // FP4 weights: every stage loads each block's scale box of its
+            // group of four K-blocks (16 bytes per row: the TMA minimum)
+            const uint32_t wsf_tx = kW4 ? (uint32_t)(nblk * kWsfBytes) : 0u;
+            mbar_arrive_expect_tx(&sh.sf_full[stage], (group ? (uint32_t)kSfRaw : 0u) + wsf_tx);
+            if (group) tma_load_3d(sfs, &tmSF, &sh.sf_full[stage], tl.sf_x, kb, tl.sf_z);
+            if (kW4)
+              for (int32_t b = 0; b < nblk; ++b)
+                tma_load_2d(sfs + kSfStage + b * kWsfBytes, &tmSFW, &sh.sf_full[stage], (kb & ~3) * 4,
+                            wy + b * kBlockRows);
           }
           const int32_t kx = kb * (p.fp8 ? 128 : 64);
           if constexpr (kPair) {
@@ -585,9 +612,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (leader && lane == 0 && S > 0) {
       // a stage is ready once its operands landed and (fp8) its scale words
       // are built
+      // (FP4 weights: the weight-scale boxes that tcgen05.cp reads land on
+      // sf_full, which the scale warp waited on before sf_ready; the MMA
+      // thread waits on it too, so it observes the copies itself)
       auto ready = [&](uint32_t st, uint32_t ph) {
         return wait_bounded(&sh.full[st], ph, deadline, &sh.abort_flag, p.status) &&
-               (!p.fp8 || wait_bounded(&sh.sf_ready[st], ph, deadline, &sh.abort_flag, p.status));
+               (!p.fp8 || wait_bounded(&sh.sf_ready[st], ph, deadline, &sh.abort_flag, p.status)) &&
+               (!kW4 || wait_bounded(&sh.sf_full[st], ph, deadline, &sh.abort_flag, p.status));
       };
       with_blocks([&](auto bc) {
       constexpr int kB = decltype(bc)::value;
@@ -606,22 +637,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         // barrier: decoding the tile here (a binary search and several
         // divisions) left the tensor pipe idle at every tile boundary.
         const int32_t qn = *reinterpret_cast<volatile int32_t*>(&sh.tile_qn[ti % kInfoRing]);
-        const uint32_t idesc0 = p.fp8 ? idesc_mxf8(kBlockRows, qn) : idesc_bf16(kBlockRows, qn, 0, 0);
+        // FP4 weights (the MMA's A operand): A format E2M1
+        const uint32_t idesc0 = p.fp8 ? (idesc_mxf8(kBlockRows, qn) | (kW4 ? kIdescAE2M1 : 0u))
+                                      : idesc_bf16(kBlockRows, qn, 0, 0);
         for (int32_t kb = 0; kb < KB; ++kb) {
           uint8_t* sw = ring + (size_t)stage * stage_bytes;
           const uint32_t a0 = smem_u32(sw), b0 = smem_u32(sw + kB * kWTileBytes);
           const uint32_t sid = (uint32_t)(kb & 3);
-          const uint32_t idesc = p.fp8 ? (idesc0 | (sid << 4) | (sid << 29)) : idesc0;
+          // scale bytes: tokens use byte kb & 3 of their word, fp8 weights the
+          // same byte of theirs; FP4 weights byte ks of this stage's atom
+          const uint32_t idesc = p.fp8 ? (idesc0 | (sid << 4) | (kW4 ? 0u : (sid << 29))) : idesc0;
+          if constexpr (!kPair) {
+            if (kW4) {
+              const uint32_t atoms = smem_u32(sf_area + (size_t)stage * sf_bytes + kSfStage + 2 * kWsfBytes);
+              tmem_cp_32x128b_x4(tmem + sfa_col, desc_sf_32x16(atoms));
+              if (kB == 2) tmem_cp_32x128b_x4(tmem + sfa_col + 4, desc_sf_32x16(atoms + kWsfAtom));
+            }
+          }
           if (p.fp8 && sid == 0) {
-            const uint32_t sfs = smem_u32(sf_area + (size_t)stage * kSfStage);
+            const uint32_t sfs = smem_u32(sf_area + (size_t)stage * sf_bytes);
             if constexpr (kPair) {
               tmem_cp_32x128b_x4_pair(tmem + sfa_col, desc_sf_32x16(sfs + kSfRaw));
               if (kB == 2) tmem_cp_32x128b_x4_pair(tmem + sfa_col + 4, desc_sf_32x16(sfs + kSfW1));
               tmem_cp_32x128b_x4_pair(tmem + sfb_col, desc_sf_32x16(sfs + kSfRaw + 512));
               if (qn > 128) tmem_cp_32x128b_x4_pair(tmem + sfb_col + 4, desc_sf_32x16(sfs + kSfRaw + 1024));
             } else {
-              tmem_cp_32x128b_x4(tmem + sfa_col, desc_sf_32x16(sfs + kSfRaw));
-              if (kB == 2) tmem_cp_32x128b_x4(tmem + sfa_col + 4, desc_sf_32x16(sfs + kSfW1));
+              if (!kW4) {
+                tmem_cp_32x128b_x4(tmem + sfa_col, desc_sf_32x16(sfs + kSfRaw));
+                if (kB == 2) tmem_cp_32x128b_x4(tmem + sfa_col + 4, desc_sf_32x16(sfs + kSfW1));
+              }
               tmem_cp_32x128b_x4(tmem + sfb_col, desc_sf_32x16(sfs + kSfRaw + 512));
               if (qn > 128) tmem_cp_32x128b_x4(tmem + sfb_col + 4, desc_sf_32x16(sfs + kSfRaw + 1024));
             }
@@ -636,7 +680,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (p.fp8) mma_mxf8_pair(d, ad, bd, idesc, tmem + sfa_col + 4 * b, tmem + sfb_col, accum);
                 else mma_f16_pair(d, ad, bd, idesc, accum);
               } else {
-                if (p.fp8) mma_mxf8(d, ad, bd, idesc, tmem + sfa_col + 4 * b, tmem + sfb_col, accum);
+                if (p.fp8)
+                  mma_mxf8(d, ad, bd, idesc | (kW4 ? (uint32_t)ks << 29 : 0u), tmem + sfa_col + 4 * b,
+                           tmem + sfb_col, accum);
                 else mma_f16(d, ad, bd, idesc, accum);
               }
             }
@@ -699,7 +745,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       };
-      if (unit < total) fetch_wsf(unit, wsf_nxt);
+      if (unit < total && !kW4) fetch_wsf(unit, wsf_nxt);
       for (int32_t t = unit; ok && t < total; t += n_units) {
 #pragma unroll
         for (int b = 0; b < kB; ++b)
@@ -710,22 +756,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
+          uint8_t* sfs = sf_area + (size_t)stage * sf_bytes;
           if ((kb % kSfGroup) == 0) {
-            uint8_t* sfs = sf_area + (size_t)stage * kSfStage;
             // lane l, column c of a word block holds the word of row c*32 + l
-            sf_build_words(sfs, sf_weight_word(wsf[0], kb, KB), lane);
-            if (kB == 2) {
+            // (FP4 weights: only the token words are built here)
+            sf_build_words(sfs, kW4 ? 0u : sf_weight_word(wsf[0], kb, KB), lane);
+            if (kB == 2 && !kW4) {
               const uint32_t w1 = sf_weight_word(wsf[kB - 1], kb, KB);
               *reinterpret_cast<uint4*>(sfs + kSfW1 + lane * 16) = make_uint4(w1, w1, w1, w1);
             }
-            fence_proxy_async_smem();
           }
+          if (kW4) {
+            // this K-block's word of rows lane + 32 j, from the group's box
+#pragma unroll
+            for (int b = 0; b < kB; ++b) {
+              const uint8_t* box = sfs + kSfStage + b * kWsfBytes + 4 * (kb & 3);
+              uint32_t w[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) w[j] = *reinterpret_cast<const uint32_t*>(box + 16 * (lane + 32 * j));
+              *reinterpret_cast<uint4*>(sfs + kSfStage + 2 * kWsfBytes + b * kWsfAtom + lane * 16) =
+                  make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+          if ((kb % kSfGroup) == 0 || kW4) fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
             if constexpr (kPair) mbar_arrive_cluster(ready0 + stage * (uint32_t)sizeof(uint64_t));
             else mbar_arrive(&sh.sf_ready[stage]);
           }
-          if (kb == 0 && t + n_units < total) fetch_wsf(t + n_units, wsf_nxt);
+          if (kb == 0 && t + n_units < total && !kW4) fetch_wsf(t + n_units, wsf_nxt);
           if (++stage == (uint32_t)S) {
             stage = 0;
             phase ^= 1u;
@@ -811,13 +870,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int kBlocks, bool kPair>
+template <int kBlocks, bool kPair, bool kW4>
 cudaError_t launch(const FwdArgs& a, cudaStream_t s) {
   static bool attr_done[64] = {};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
-  auto kernel = fwd_kernel<kBlocks, kPair>;
+  auto kernel = fwd_kernel<kBlocks, kPair, kW4>;
   if (dev < 64 && !attr_done[dev]) {
     err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (err != cudaSuccess) return err;
@@ -825,6 +884,7 @@ cudaError_t launch(const FwdArgs& a, cudaStream_t s) {
   }
   // the SwiGLU epilogue pairs the two blocks of a single-SM tile
   if (a.epi != kEpiPlain && (kBlocks != 2 || kPair)) return cudaErrorInvalidValue;
+  if (a.w4 != kW4) return cudaErrorInvalidValue;
   Params p;
   p.counts = a.counts;
   p.sfb = a.sfb;
@@ -856,17 +916,24 @@ cudaError_t launch(const FwdArgs& a, cudaStream_t s) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = kPair ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kernel, a.tmW, a.tmA64, a.tmA16, a.tmA8, a.tmSF, p);
+  return cudaLaunchKernelEx(&cfg, kernel, a.tmW, a.tmA64, a.tmA16, a.tmA8, a.tmSF, a.tmSFW, p);
 }
 
 }  // namespace fwd
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s, int variant) {
+  if (a.w4) {  // FP4 weights: single-SM families only
+    switch (variant) {
+      case kFwdSingle: return fwd::launch<1, false, true>(a, s);
+      case kFwdDual: return fwd::launch<2, false, true>(a, s);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (variant) {
-    case kFwdSingle: return fwd::launch<1, false>(a, s);
-    case kFwdDual: return fwd::launch<2, false>(a, s);
-    case kFwdPair: return fwd::launch<1, true>(a, s);
-    case kFwdPairDual: return fwd::launch<2, true>(a, s);
+    case kFwdSingle: return fwd::launch<1, false, false>(a, s);
+    case kFwdDual: return fwd::launch<2, false, false>(a, s);
+    case kFwdPair: return fwd::launch<1, true, false>(a, s);
+    case kFwdPairDual: return fwd::launch<2, true, false>(a, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -17,7 +17,8 @@ enum FwdEpilogue { kEpiPlain = 0, kEpiSwigluBf16 = 1, kEpiSwigluFp8 = 2 };
 // token rows at a known row base of a 2-D [rows_total, K] activation view and
 // compute only its first t_e rows.
 struct FwdArgs {
-  bool fp8 = false;
+  bool fp8 = false;                 // E4M3 activations (and weights unless w4)
+  bool w4 = false;                  // E2M1 weights, UE8M0 per (row, 32 K)
   bool masked = false;
   const int32_t* counts = nullptr;  // t_e (contiguous) or valid_m (masked)
   int32_t E = 0, N = 0, K = 0;
@@ -33,6 +34,7 @@ struct FwdArgs {
   int32_t* status = nullptr;
   int64_t wait_ns = 0;
   CUtensorMap tmW{}, tmA64{}, tmA16{}, tmA8{}, tmSF{};
+  CUtensorMap tmSFW{};              // w4: weight scales [E*N, K/32]
 };
 // Contiguous/masked kernel of one family (FwdVariant in sched.cuh).
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s, int variant);

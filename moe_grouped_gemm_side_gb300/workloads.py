@@ -25,6 +25,10 @@ FP8 operands are E4M3 codes with one UE8M0 exponent byte per block: per
 of a block with absolute maximum a is s = clamp(ceil(log2(a / 448)) + 127,
 1, 254) (s = 127 for an all-zero block) and each element is encoded as
 e4m3(x / 2^(s - 127)) rounded to nearest even, which never exceeds 448.
+FP4 weights (dtype "fp8xfp4") are E2M1 codes, two per byte (element 2i in
+the low nibble of byte i), with one UE8M0 byte per (row, 32 K) chosen the
+same way against the largest E2M1 magnitude 6; each element takes the
+nearest E2M1 magnitude (the lower one on a tie).
 """
 
 from dataclasses import dataclass
@@ -34,6 +38,8 @@ import numpy as np
 import torch
 
 E4M3_MAX = 448.0
+E2M1_MAX = 6.0
+E2M1_MAGNITUDES = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)   # codes 0..7
 BF16_NAN_BITS = 0x7FC0
 E4M3_NAN_CODE = 0x7F
 UE8M0_NAN_CODE = 0xFF
@@ -146,8 +152,8 @@ def _ceil_log2(v: torch.Tensor) -> torch.Tensor:
     return torch.where(m == 0.5, e - 1, e)
 
 
-def _scale_bytes(amax: torch.Tensor) -> torch.Tensor:
-    s = _ceil_log2(torch.clamp(amax, min=torch.finfo(torch.float32).tiny) / E4M3_MAX) + 127
+def _scale_bytes(amax: torch.Tensor, fmax: float = E4M3_MAX) -> torch.Tensor:
+    s = _ceil_log2(torch.clamp(amax, min=torch.finfo(torch.float32).tiny) / fmax) + 127
     s = torch.clamp(s, 1, 254)
     s = torch.where(amax == 0, torch.full_like(s, 127), s)
     return s.to(torch.uint8)
@@ -180,6 +186,29 @@ def quantize_weight_fp8(w: torch.Tensor):
     return codes, sf.t().contiguous()
 
 
+def quantize_weight_mx4(w: torch.Tensor):
+    """w float32 [N, K] -> (packed uint8 [N, K/2], sf uint8 [N, K/32])."""
+    N, K = w.shape
+    assert K % 32 == 0
+    wb = w.reshape(N, K // 32, 32)
+    sf = _scale_bytes(wb.abs().amax(dim=2), E2M1_MAX)            # [N, K/32]
+    y = wb / torch.pow(2.0, sf.to(torch.float32) - 127.0)[:, :, None]
+    mags = torch.tensor(E2M1_MAGNITUDES, dtype=torch.float32, device=w.device)
+    code = (y.abs()[..., None] - mags).abs().argmin(dim=-1)      # lowest index on a tie
+    code = (code | torch.where(y < 0, 8, 0)).to(torch.uint8).reshape(N, K)
+    packed = code[:, 0::2] | (code[:, 1::2] << 4)
+    return packed.contiguous(), sf.contiguous()
+
+
+def integer_e2m1_packed(shape, seed: int, device="cpu"):
+    """Packed E2M1 codes [..., K/2] of the values -2..2 (exact in E2M1)."""
+    *lead, K = shape
+    lut = torch.tensor([0xC, 0xA, 0x0, 0x2, 0x4], dtype=torch.uint8)   # -2, -1, 0, 1, 2
+    g = torch.Generator().manual_seed(int(seed))
+    codes = lut[torch.randint(0, 5, tuple(lead) + (K,), generator=g)]
+    return (codes[..., 0::2] | (codes[..., 1::2] << 4)).contiguous().to(device)
+
+
 @dataclass
 class Operands:
     """A grouped-GEMM operand set.  ``A``/``B`` are bf16 tensors for the bf16
@@ -196,6 +225,12 @@ def make_weights(E: int, N: int, K: int, dtype: str, seed: int, device="cpu",
     """Expert weights [E, N, K] (+ SFB [E, K/128, N/128] for fp8)."""
     if dtype == "bf16":
         return normal_bf16((E, N, K), seed, device, std), None
+    if dtype == "fp8xfp4":
+        B = torch.empty((E, N, K // 2), dtype=torch.uint8, device=device)
+        SFB = torch.empty((E, N, K // 32), dtype=torch.uint8, device=device)
+        for e in range(E):
+            B[e], SFB[e] = quantize_weight_mx4(normal_f32((N, K), seed * 1000 + e, device, std))
+        return B, SFB
     B = torch.empty((E, N, K), dtype=torch.uint8, device=device)
     SFB = torch.empty((E, K // 128, N // 128), dtype=torch.uint8, device=device)
     for e in range(E):
@@ -258,6 +293,10 @@ WORKLOADS: Dict[str, dict] = {
     "masked_fp8_e16_m256_n4096_k7168": dict(
         form="masked", dtype="fp8", E=16, M_max=256, N=4096, K=7168, seed=1003,
         a_std=1.0, b_std=1.0, counts=counts_zipf_decode),
+    # the decode case with FP4 weights (half the weight bytes)
+    "masked_fp8xfp4_e16_m256_n4096_k7168": dict(
+        form="masked", dtype="fp8xfp4", E=16, M_max=256, N=4096, K=7168, seed=1003,
+        a_std=1.0, b_std=1.0, counts=counts_zipf_decode),
     "prefill_fp8_e64_t32768_n4096_k7168": dict(
         form="contiguous", dtype="fp8", E=64, N=4096, K=7168, align_q=128, seed=1004,
         a_std=1.0, b_std=1.0, counts=counts_zipf_prefill,
@@ -272,6 +311,10 @@ WORKLOADS: Dict[str, dict] = {
         form="contiguous", dtype="fp8", E=16, N=4096, K=7168, align_q=128, seed=1006,
         a_std=1.0, b_std=7168 ** -0.5, counts=lambda: counts_zipf_prefill(seed=1006, E=16, total=8192),
         second=dict(N=7168, K=2048), swiglu=True),
+    "prefill_fp8xfp4_e64_t32768_n4096_k7168": dict(
+        form="contiguous", dtype="fp8xfp4", E=64, N=4096, K=7168, align_q=128, seed=1004,
+        a_std=1.0, b_std=1.0, counts=counts_zipf_prefill,
+        second=dict(N=7168, K=2048)),
     "prefill_bf16_e64_t32768_n4096_k7168": dict(
         form="contiguous", dtype="bf16", E=64, N=4096, K=7168, align_q=128, seed=1004,
         a_std=7168 ** -0.5, b_std=7168 ** -0.5, counts=counts_zipf_prefill,

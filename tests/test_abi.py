@@ -141,6 +141,10 @@ def test_device_calls_reject_bad_arguments_before_launch(lib):
     assert contig({0: 1}) == 1               # fp8 without scales
     assert contig({0: 1, 2: FAKE, 4: FAKE, 11: 8}) == 2     # fp8 align_q % 16
     assert contig({0: 1, 2: FAKE, 4: FAKE, 12: 248}) == 1   # fp8 tile 248
+    fp4 = {0: mb.MG_FP8_X_FP4_E2M1, 2: FAKE, 4: FAKE, 10: 512}
+    assert contig({**fp4, 10: 640}) == 2                    # FP4 weights need K % 512
+    assert contig({**fp4, 3: ctypes.c_void_p((1 << 20) + 16)}) == 1   # packed FP4 base 32-byte aligned
+    assert contig({**fp4, 4: None}) == 1                    # FP4 without weight scales
     # masked
     m = [mb.MG_BF16, FAKE, None, FAKE, None, FAKE, FAKE, 8, 256, 256, 256, None, None]
     assert L.mgemm_masked(*[None if i == 6 else v for i, v in enumerate(m)]) == 1

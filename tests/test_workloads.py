@@ -61,3 +61,28 @@ def test_fp8_weight_scales_shape():
 def test_masked_sfa_layout():
     ops = wl.make_masked(3, 32, 128, 256, "fp8", seed=5)
     assert ops.A.shape == (3, 32, 256) and ops.SFA.shape == (3, 2, 32) and ops.SFB.shape == (3, 2, 1)
+
+
+def test_mx4_weight_generator_round_trips():
+    """The FP4 weight generator's bytes decode (oracle) to within half an E2M1
+    spacing of the drawn values, with the block maximum inside 6 * scale."""
+    from oracle import numerics as on
+    w = wl.normal_f32((64, 256), 5, "cpu", 0.1)
+    packed, sf = wl.quantize_weight_mx4(w)
+    assert packed.shape == (64, 128) and sf.shape == (64, 8)
+    deq = on.dequant_weight_mx4(packed.numpy(), sf.numpy())
+    x = w.double().numpy()
+    scale = np.repeat(np.exp2(sf.numpy().astype(np.float64) - 127), 32, axis=1)
+    amax = np.repeat(np.abs(x.reshape(64, 8, 32)).max(axis=2), 32, axis=1)
+    assert np.all(amax <= 6 * scale) and np.all(amax > 3 * scale)
+    # E2M1 spacing: 0.5 below 2, 1 in [2, 4), 2 in [4, 6]
+    y = np.abs(x) / scale
+    half = np.where(y < 2, 0.25, np.where(y < 4, 0.5, 1.0))
+    assert np.all(np.abs(deq - x) <= half * scale * (1 + 1e-6))
+
+
+def test_integer_e2m1_values():
+    from oracle import numerics as on
+    p = wl.integer_e2m1_packed((3, 64), 1)
+    vals = on.decode_e2m1(on.unpack_e2m1(p.numpy()))
+    assert set(np.unique(vals).tolist()) <= {-2.0, -1.0, 0.0, 1.0, 2.0}
