@@ -147,3 +147,50 @@ def test_mx4_scale_granularity_is_caught(monkeypatch):
         return on.decode_e2m1(codes) * np.repeat(on.decode_ue8m0(sf), 32, axis=1)[:, ::-1]
     monkeypatch.setattr(on, "dequant_weight_mx4", bad)
     assert fails(tn.test_dequant_weight_mx4_brute_force)
+
+
+# --- exemplar selector (oracle/selector.py) --------------------------------
+import oracle.selector as osel                   # noqa: E402
+from tests import test_oracle_selector as tsel   # noqa: E402
+
+
+def test_ascending_sort_is_caught(monkeypatch):
+    orig = osel.features
+
+    def bad(counts):
+        lu, shares = orig(counts)
+        c = sorted(max(0, int(x)) for x in counts)                  # ascending
+        U = sum(c)
+        if U == 0:
+            return lu, shares
+        E = len(c)
+        return lu, [65536 * sum(c[:-(-k * E // 16)]) // U for k in range(1, 17)]
+    monkeypatch.setattr(osel, "features", bad)
+    assert fails(tsel.test_worked_concentrated_example)
+
+
+def test_floor_expert_count_is_caught(monkeypatch):
+    orig_sorted = sorted
+
+    def bad(counts):
+        c = orig_sorted((max(0, int(x)) for x in counts), reverse=True)
+        U, E = sum(c), len(c)
+        if U == 0:
+            return 0, [0] * 16
+        shares = [65536 * sum(c[:k * E // 16]) // U for k in range(1, 17)]   # floor, not ceil
+        e = U.bit_length() - 1
+        return 16 * e + (16 * (U - (1 << e))) // (1 << e), shares
+    monkeypatch.setattr(osel, "features", bad)
+    assert fails(tsel.test_worked_concentrated_example)
+
+
+def test_hysteresis_inverted_is_caught(monkeypatch):
+    def bad(counts, table, prev=-1, margin=0):
+        feat = osel.features(counts)
+        d = [osel.distance(feat, x) for x in table]
+        best = min(range(len(d)), key=lambda i: (d[i], i))
+        if 0 <= prev < len(table) and d[prev] - d[best] < margin:    # strict: off by one at the margin
+            return prev
+        return best
+    monkeypatch.setattr(osel, "choose", bad)
+    assert fails(tsel.test_choice_ties_and_hysteresis)
