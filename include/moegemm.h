@@ -143,6 +143,52 @@ mg_status moe_select_tile_host(mg_dtype dt, const int32_t* counts, int32_t E,
                                int32_t* tile_q);
 
 /* ------------------------------------------------------------------------
+ * Exemplar selector ("MoE GroupGEMM padding under expert skew", "Adapt
+ * kernels without adding a CPU stall": sort and normalise the per-expert
+ * count vector, match it against exemplars tuned offline on the GPU, and add
+ * guardrails so neighbouring histograms do not switch kernels every layer;
+ * "Padding is not the whole cost model": the table comes from measurement,
+ * not from the padding formula).  The pages give the steps; the integer
+ * definitions below are this library's, so host and device agree exactly.
+ *
+ * Features of counts c[0..E) (negative counts read as 0), U = sum c:
+ *   share[k-1] = floor(65536 * (sum of the m_k largest counts) / U),
+ *                m_k = ceil(k*E/16), k = 1..16  (all 0 when U = 0);
+ *   lu         = 16*e + floor(16*(U - 2^e) / 2^e), e = floor(log2 U)
+ *                (0 when U = 0).
+ * Distance to exemplar x: sum_k |share[k] - x.share[k]| + 2048*|lu - x.lu|.
+ * Choice: the smallest distance, the lowest index on ties.  Hysteresis: with
+ * a state word holding the previous choice p (>= 0), p is kept while
+ * dist(p) - dist(best) <= margin; the state then holds the choice.
+ *
+ * The tactic written for the GEMM calls below: int32 [3] = {tile_q, blocks,
+ * exemplar index}; tile_q a multiple of 16 in [16, 256], blocks 1 or 2
+ * (weight blocks of 128 rows per tile).  A chosen exemplar with other
+ * values writes {0, 0, index} and MG_ERR_DEVICE_ARG.
+ * ------------------------------------------------------------------------ */
+#define MG_EXEMPLAR_SHARES 16
+typedef struct {
+  int32_t lu;
+  int32_t share[MG_EXEMPLAR_SHARES];
+  int32_t tile_q;      /* token tile to use for histograms near this one      */
+  int32_t blocks;      /* weight blocks per tile: 1 or 2                       */
+  int32_t reserved;    /* 0                                                    */
+} mg_exemplar;         /* 80 bytes */
+
+/* Host: the features of one histogram (for building tables); E >= 1. */
+mg_status moe_exemplar_features_host(const int32_t* counts, int32_t E, int32_t* lu,
+                                     int32_t* share /* [16] */);
+/* Host: the choice for one histogram (prev < 0: no history). */
+mg_status moe_select_exemplar_host(const int32_t* counts, int32_t E, const mg_exemplar* table,
+                                   int32_t n, int32_t margin, int32_t prev, int32_t* choice);
+/* Device, one small kernel.  d_table: n entries in device memory (n <= 1024);
+ * E <= 4096; d_state: int32 or NULL (no hysteresis; initialise to -1);
+ * d_tactic: int32 [3] as above. */
+mg_status moe_select_exemplar(const int32_t* d_counts, int32_t E, const mg_exemplar* d_table,
+                              int32_t n, int32_t margin, int32_t* d_state, int32_t* d_tactic,
+                              int32_t* d_status, void* stream);
+
+/* ------------------------------------------------------------------------
  * M-grouped contiguous grouped GEMM ("flops/deepgemm-grouped-masked-moe-
  * gemm", "Workarounds": contiguous layout for prefill/training; "Arithmetic
  * intensity": segments aligned to the M block; "MoE GroupGEMM padding under
@@ -266,6 +312,26 @@ mg_status mgemm_masked_swiglu(mg_dtype dt, mg_swiglu_out out, const void* A, con
                               const void* B, const uint8_t* SFB, void* Y, uint8_t* SFY,
                               const int32_t* d_valid_m, int32_t E, int32_t M_max, int32_t N,
                               int32_t K, int32_t* d_status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * The contiguous and masked forms with the token tile and the blocks per
+ * tile read from a device tactic (int32 [3], e.g. written by
+ * moe_select_exemplar): no host round trip between the choice and the GEMM,
+ * and both launches can be captured in one CUDA graph.  Arguments, results
+ * and errors are those of mgemm_contiguous / mgemm_masked (with tile_q taken
+ * from the tactic; tiles wider than the kernel allows are narrowed, which
+ * does not change the result).  These calls run the single-SM kernel of two
+ * 128-row blocks (N % 256 == 0) or of one block; a tactic that is not valid
+ * is reported as MG_ERR_DEVICE_ARG and the kernel's own choice is used.
+ * ------------------------------------------------------------------------ */
+mg_status mgemm_contiguous_tactic(mg_dtype dt, const void* A, const uint8_t* SFA, const void* B,
+                                  const uint8_t* SFB, void* D, const int32_t* d_counts, int32_t E,
+                                  int64_t rows_cap, int32_t N, int32_t K, int32_t align_q,
+                                  const int32_t* d_tactic, int32_t* d_status, void* stream);
+mg_status mgemm_masked_tactic(mg_dtype dt, const void* A, const uint8_t* SFA, const void* B,
+                              const uint8_t* SFB, void* D, const int32_t* d_valid_m, int32_t E,
+                              int32_t M_max, int32_t N, int32_t K, const int32_t* d_tactic,
+                              int32_t* d_status, void* stream);
 
 /* ------------------------------------------------------------------------
  * K-grouped weight-gradient GEMM ("flops/deepgemm-grouped-masked-moe-gemm",

@@ -46,6 +46,12 @@ SIGNATURES = {
                                        _i32, _i32, _vp, _vp]),
     "mgemm_masked_swiglu": (_i32, [_i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp,
                                    _vp]),
+    "moe_exemplar_features_host": (_i32, [_c_i32p, _i32, _c_i32p, _c_i32p]),
+    "moe_select_exemplar_host": (_i32, [_c_i32p, _i32, _vp, _i32, _i32, _i32, _c_i32p]),
+    "moe_select_exemplar": (_i32, [_vp, _i32, _vp, _i32, _i32, _vp, _vp, _vp, _vp]),
+    "mgemm_contiguous_tactic": (_i32, [_i32, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32, _vp,
+                                       _vp, _vp]),
+    "mgemm_masked_tactic": (_i32, [_i32, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp]),
     "kgemm_grouped": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _vp, _vp]),
     "mg_set_wait_limit_ns": (_i32, [_i64]),
     "mg_get_wait_limit_ns": (_i64, []),
@@ -231,6 +237,74 @@ def mgemm_masked_swiglu(A, B, Y, d_valid_m, SFA=None, SFB=None, SFY=None, status
     _check("mgemm_masked_swiglu", lib.mgemm_masked_swiglu(
         _fwd_dtype(A, B, K), _swiglu_out(Y), _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(Y), _ptr(SFY),
         _ptr(d_valid_m), E, M_max, N, K, _ptr(status), _stream(stream)))
+
+
+# ------------------------------------------------------------ exemplar selector
+EXEMPLAR_DTYPE = np.dtype([("lu", "<i4"), ("share", "<i4", (16,)), ("tile_q", "<i4"), ("blocks", "<i4"),
+                           ("reserved", "<i4")])
+assert EXEMPLAR_DTYPE.itemsize == 80
+
+
+def exemplar_table(entries) -> np.ndarray:
+    """List of {"lu", "shares", "tile_q", "blocks"} -> mg_exemplar array."""
+    t = np.zeros(len(entries), dtype=EXEMPLAR_DTYPE)
+    for i, x in enumerate(entries):
+        t[i]["lu"] = x["lu"]
+        t[i]["share"] = x["shares"]
+        t[i]["tile_q"] = x["tile_q"]
+        t[i]["blocks"] = x["blocks"]
+    return t
+
+
+def exemplar_table_device(table: np.ndarray, device="cuda"):
+    """mg_exemplar array -> uint8 device tensor holding the same bytes."""
+    import torch
+    return torch.from_numpy(np.frombuffer(table.tobytes(), dtype=np.uint8).copy()).to(device)
+
+
+def exemplar_features_host(counts):
+    c = np.ascontiguousarray(np.asarray(counts, dtype=np.int32))
+    lu = ctypes.c_int32(0)
+    share = np.zeros(16, dtype=np.int32)
+    _check("moe_exemplar_features_host", load().moe_exemplar_features_host(
+        c.ctypes.data_as(_c_i32p), len(c), ctypes.byref(lu), share.ctypes.data_as(_c_i32p)))
+    return lu.value, share.tolist()
+
+
+def select_exemplar_host(counts, table: np.ndarray, margin: int = 0, prev: int = -1) -> int:
+    c = np.ascontiguousarray(np.asarray(counts, dtype=np.int32))
+    t = np.ascontiguousarray(table)
+    out = ctypes.c_int32(0)
+    _check("moe_select_exemplar_host", load().moe_select_exemplar_host(
+        c.ctypes.data_as(_c_i32p), len(c), t.ctypes.data, len(t), margin, prev, ctypes.byref(out)))
+    return out.value
+
+
+def select_exemplar(d_counts, d_table, n: int, d_tactic, margin: int = 0, d_state=None, status=None,
+                    stream=None):
+    """moe_select_exemplar: writes {tile_q, blocks, index} to d_tactic (int32 [3])."""
+    _check("moe_select_exemplar", load().moe_select_exemplar(
+        _ptr(d_counts), d_counts.numel(), _ptr(d_table), n, margin, _ptr(d_state), _ptr(d_tactic),
+        _ptr(status), _stream(stream)))
+
+
+def mgemm_contiguous_tactic(A, B, D, d_counts, align_q: int, d_tactic, SFA=None, SFB=None, status=None,
+                            stream=None):
+    lib = load()
+    rows_cap, K = A.shape
+    E, N, _ = B.shape
+    _check("mgemm_contiguous_tactic", lib.mgemm_contiguous_tactic(
+        _fwd_dtype(A, B, K), _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(D), _ptr(d_counts), E,
+        rows_cap, N, K, align_q, _ptr(d_tactic), _ptr(status), _stream(stream)))
+
+
+def mgemm_masked_tactic(A, B, D, d_valid_m, d_tactic, SFA=None, SFB=None, status=None, stream=None):
+    lib = load()
+    E, M_max, K = A.shape
+    N = B.shape[1]
+    _check("mgemm_masked_tactic", lib.mgemm_masked_tactic(
+        _fwd_dtype(A, B, K), _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(D), _ptr(d_valid_m), E,
+        M_max, N, K, _ptr(d_tactic), _ptr(status), _stream(stream)))
 
 
 def kgemm_grouped(dY, X, dW, d_counts, status=None, stream=None):

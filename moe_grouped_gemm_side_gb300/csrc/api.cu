@@ -390,6 +390,55 @@ mg_status mgemm_masked_swiglu(mg_dtype dt, mg_swiglu_out out, const void* A, con
   return from_cuda(launch_fwd(a, static_cast<cudaStream_t>(stream), kFwdDual));
 }
 
+mg_status moe_exemplar_features_host(const int32_t* counts, int32_t E, int32_t* lu, int32_t* share) {
+  if (counts == nullptr || lu == nullptr || share == nullptr || E <= 0) return MG_ERR_INVALID_ARG;
+  exemplar_features_host(counts, E, lu, share);
+  return MG_OK;
+}
+
+mg_status moe_select_exemplar_host(const int32_t* counts, int32_t E, const mg_exemplar* table, int32_t n,
+                                   int32_t margin, int32_t prev, int32_t* choice) {
+  if (counts == nullptr || table == nullptr || choice == nullptr || E <= 0 || n <= 0 || margin < 0)
+    return MG_ERR_INVALID_ARG;
+  *choice = exemplar_choose_host(counts, E, table, n, margin, prev, nullptr);
+  return MG_OK;
+}
+
+mg_status moe_select_exemplar(const int32_t* d_counts, int32_t E, const mg_exemplar* d_table, int32_t n,
+                              int32_t margin, int32_t* d_state, int32_t* d_tactic, int32_t* d_status,
+                              void* stream) {
+  if (d_counts == nullptr || d_table == nullptr || d_tactic == nullptr) return MG_ERR_INVALID_ARG;
+  if (E <= 0 || n <= 0 || margin < 0) return MG_ERR_INVALID_ARG;
+  if (E > kSelMaxExperts || n > kSelMaxExemplars) return MG_ERR_UNSUPPORTED;
+  return from_cuda(launch_exemplar(d_counts, E, d_table, n, margin, d_state, d_tactic, d_status,
+                                   static_cast<cudaStream_t>(stream)));
+}
+
+mg_status mgemm_contiguous_tactic(mg_dtype dt, const void* A, const uint8_t* SFA, const void* B,
+                                  const uint8_t* SFB, void* D, const int32_t* d_counts, int32_t E,
+                                  int64_t rows_cap, int32_t N, int32_t K, int32_t align_q,
+                                  const int32_t* d_tactic, int32_t* d_status, void* stream) {
+  if (d_tactic == nullptr) return MG_ERR_INVALID_ARG;
+  FwdArgs a;
+  const mg_status st = prep_contiguous(a, dt, A, SFA, B, SFB, D, d_counts, E, rows_cap, N, K, align_q, 0,
+                                       d_status);
+  if (st != MG_OK) return st;
+  a.tactic = d_tactic;
+  return from_cuda(launch_fwd(a, static_cast<cudaStream_t>(stream), N % 256 == 0 ? kFwdDual : kFwdSingle));
+}
+
+mg_status mgemm_masked_tactic(mg_dtype dt, const void* A, const uint8_t* SFA, const void* B,
+                              const uint8_t* SFB, void* D, const int32_t* d_valid_m, int32_t E,
+                              int32_t M_max, int32_t N, int32_t K, const int32_t* d_tactic,
+                              int32_t* d_status, void* stream) {
+  if (d_tactic == nullptr) return MG_ERR_INVALID_ARG;
+  FwdArgs a;
+  const mg_status st = prep_masked(a, dt, A, SFA, B, SFB, D, d_valid_m, E, M_max, N, K, d_status);
+  if (st != MG_OK) return st;
+  a.tactic = d_tactic;
+  return from_cuda(launch_fwd(a, static_cast<cudaStream_t>(stream), N % 256 == 0 ? kFwdDual : kFwdSingle));
+}
+
 mg_status kgemm_grouped(const void* dY, const void* X, float* dW, const int32_t* d_counts,
                         int32_t E, int64_t T_cap, int32_t N, int32_t K, int32_t* d_status,
                         void* stream) {

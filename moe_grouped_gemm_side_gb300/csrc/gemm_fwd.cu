@@ -93,6 +93,7 @@ struct Params {
   int32_t rows_total, M_max, align_q, tile_q;
   int32_t epi;       // kEpiPlain, kEpiSwigluBf16 or kEpiSwigluFp8
   int32_t sfy_ld;
+  const int32_t* tactic;  // device {tile_q, blocks} chosen elsewhere on the GPU, or null
 };
 
 struct Shared {
@@ -420,7 +421,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
     int32_t q = p.tile_q;
-    if (p.masked) {
+    int32_t want_blocks = 0;  // 0: decided below from the tile count
+    if (p.tactic != nullptr) {
+      const int32_t tq = p.tactic[0], tb = p.tactic[1];
+      if (tq >= 16 && tq <= 256 && tq % 16 == 0 && (tb == 1 || tb == 2)) {
+        q = tq;
+        want_blocks = min(tb, kBlocks);
+      } else if (lane == 0) {
+        set_status(p.status, MG_ERR_DEVICE_ARG);
+      }
+    }
+    if (q == 0 && p.masked) {
       q = q_cap;
     } else if (q == 0) {
       int64_t tiles[kNumTileCand];
@@ -440,7 +451,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // not fill two waves of workers: with few tiles (decode) the finer
     // split balances the SMs, which all stream weights from DRAM then.
     int32_t nblk = kBlocks;
-    if (kBlocks == 2 && p.epi == kEpiPlain) {  // a SwiGLU epilogue needs gate and up in one tile
+    if (kBlocks == 2 && p.epi == kEpiPlain && want_blocks != 0) {
+      nblk = want_blocks;
+    } else if (kBlocks == 2 && p.epi == kEpiPlain) {  // a SwiGLU epilogue needs gate and up in one tile
       int64_t tt = 0;
       for (int32_t e = lane; e < E; e += 32) tt += cdiv64(cnt[e], q);
 #pragma unroll
@@ -892,6 +905,7 @@ cudaError_t launch(const FwdArgs& a, cudaStream_t s) {
   p.sfy = a.sfy;
   p.epi = a.epi;
   p.sfy_ld = a.sfy_ld;
+  p.tactic = a.tactic;
   p.status = a.status;
   p.wait_ns = a.wait_ns;
   p.E = a.E;

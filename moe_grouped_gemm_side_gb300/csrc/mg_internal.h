@@ -32,6 +32,7 @@ struct FwdArgs {
   uint8_t* sfy = nullptr;           // kEpiSwigluFp8: scales [z][N/256][sfy_ld]
   int32_t sfy_ld = 0;
   int32_t* status = nullptr;
+  const int32_t* tactic = nullptr;  // device {tile_q, blocks} or null
   int64_t wait_ns = 0;
   CUtensorMap tmW{}, tmA64{}, tmA16{}, tmA8{}, tmSF{};
   CUtensorMap tmSFW{};              // w4: weight scales [E*N, K/32]
@@ -56,6 +57,19 @@ cudaError_t launch_plan(const int32_t* counts, int32_t E, int32_t q, int64_t* of
 cudaError_t launch_select(bool fp8, int variant, const int32_t* counts, int32_t E, int32_t N,
                           int32_t K, int32_t* tile_q, int32_t* status, cudaStream_t s);
 cudaError_t launch_wait_selftest(int32_t* status, int64_t limit_ns, cudaStream_t s);
+
+// Exemplar selector: integer features and choice, host and device.
+constexpr int kExemplarShares = MG_EXEMPLAR_SHARES;
+constexpr int32_t kShareOne = 65536;
+constexpr int32_t kLuWeight = 2048;
+constexpr int kSelMaxExperts = 4096;
+constexpr int kSelMaxExemplars = 1024;
+cudaError_t launch_exemplar(const int32_t* counts, int32_t E, const mg_exemplar* table, int32_t n,
+                            int32_t margin, int32_t* state, int32_t* tactic, int32_t* status,
+                            cudaStream_t s);
+void exemplar_features_host(const int32_t* counts, int32_t E, int32_t* lu, int32_t* share);
+int32_t exemplar_choose_host(const int32_t* counts, int32_t E, const mg_exemplar* table, int32_t n,
+                             int32_t margin, int32_t prev, int64_t* dist_out);
 
 int num_sms_current_device();
 

@@ -2,6 +2,11 @@
 // padded token columns" and "Summarize skew without losing the histogram"),
 // the device token-tile selector ("Adapt kernels without adding a CPU
 // stall"), and the bounded-wait self-test.
+#include <algorithm>
+#include <climits>
+#include <cstdlib>
+#include <vector>
+
 #include "common.cuh"
 #include "mg_internal.h"
 #include "sched.cuh"
@@ -122,6 +127,114 @@ __global__ void select_kernel(const int32_t* __restrict__ counts, int32_t E, int
     *tile_q = pick_tile(fp8 != 0, tiles, variant, N, KB, num_sms);
 }
 
+// Exemplar choice ("MoE GroupGEMM padding under expert skew", "Adapt kernels
+// without adding a CPU stall": sort and normalise the count vector, match it
+// against exemplars tuned offline, guard against switching on neighbouring
+// histograms).  One CTA: bitonic sort of the counts (descending), in-place
+// prefix sums, the 16-point cumulative top-share curve and the log2(U)
+// feature (integers, the definitions in moegemm.h), the L1 distance to every
+// exemplar, the smallest distance (lowest index on ties), then the
+// hysteresis rule against the call site's state.
+__global__ void __launch_bounds__(kPlanThreads)
+    exemplar_kernel(const int32_t* __restrict__ counts, int32_t E, const mg_exemplar* __restrict__ table,
+                    int32_t n, int32_t margin, int32_t* state, int32_t* tactic, int32_t* status) {
+  __shared__ int64_t v[kSelMaxExperts];
+  __shared__ int64_t dist[kSelMaxExemplars];
+  __shared__ int64_t scratch[32];
+  __shared__ int32_t feat[kExemplarShares + 1];      // shares, then lu
+  __shared__ int64_t best_d[32];
+  __shared__ int32_t best_i[32];
+  const int tid = threadIdx.x;
+  int32_t P = 2;
+  while (P < E) P <<= 1;
+  for (int32_t i = tid; i < P; i += kPlanThreads) v[i] = i < E ? (int64_t)max(counts[i], 0) : 0;
+  __syncthreads();
+  for (int32_t k = 2; k <= P; k <<= 1) {
+    for (int32_t j = k >> 1; j > 0; j >>= 1) {
+      for (int32_t i = tid; i < P; i += kPlanThreads) {
+        const int32_t ixj = i ^ j;
+        if (ixj > i) {
+          const int64_t a = v[i], b = v[ixj];
+          if ((i & k) == 0 ? (a < b) : (a > b)) {
+            v[i] = b;
+            v[ixj] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  // inclusive prefix sums in place: each thread owns R consecutive values
+  const int32_t R = (P + kPlanThreads - 1) / kPlanThreads;
+  const int32_t lo = tid * R, hi = min(P, lo + R);
+  int64_t own = 0;
+  for (int32_t i = lo; i < hi; ++i) own += v[i];
+  int64_t total;
+  int64_t run = block_exclusive_scan<int64_t>(own, scratch, total);
+  for (int32_t i = lo; i < hi; ++i) {
+    run += v[i];
+    v[i] = run;
+  }
+  __syncthreads();
+  const int64_t U = v[E - 1];
+  if (tid < kExemplarShares) {
+    const int32_t m = ((tid + 1) * E + kExemplarShares - 1) / kExemplarShares;
+    feat[tid] = U > 0 ? (int32_t)((int64_t)kShareOne * v[m - 1] / U) : 0;
+  }
+  if (tid == 0) {
+    int32_t lu = 0;
+    if (U > 0) {
+      const int e = 63 - __clzll(U);
+      lu = 16 * e + (int32_t)((16 * (U - (int64_t(1) << e))) >> e);
+    }
+    feat[kExemplarShares] = lu;
+  }
+  __syncthreads();
+  int64_t bd = INT64_MAX;
+  int32_t bi = 0x7fffffff;
+  for (int32_t i = tid; i < n; i += kPlanThreads) {
+    int64_t d = (int64_t)kLuWeight * llabs((int64_t)feat[kExemplarShares] - table[i].lu);
+#pragma unroll
+    for (int k = 0; k < kExemplarShares; ++k) d += llabs((int64_t)feat[k] - table[i].share[k]);
+    dist[i] = d;
+    if (d < bd) {  // i increases: the first minimum of this thread's subset
+      bd = d;
+      bi = i;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const int64_t od = __shfl_xor_sync(0xffffffffu, bd, o);
+    const int32_t oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (od < bd || (od == bd && oi < bi)) {
+      bd = od;
+      bi = oi;
+    }
+  }
+  if ((tid & 31) == 0) {
+    best_d[tid >> 5] = bd;
+    best_i[tid >> 5] = bi;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    for (int w = 1; w < kPlanThreads / 32; ++w)
+      if (best_d[w] < bd || (best_d[w] == bd && best_i[w] < bi)) {
+        bd = best_d[w];
+        bi = best_i[w];
+      }
+    int32_t c = bi;
+    const int32_t prev = state != nullptr ? *state : -1;
+    if (prev >= 0 && prev < n && dist[prev] - bd <= (int64_t)margin) c = prev;
+    const mg_exemplar& x = table[c];
+    const bool ok = x.tile_q >= 16 && x.tile_q <= 256 && x.tile_q % 16 == 0 && (x.blocks == 1 || x.blocks == 2);
+    if (!ok) set_status(status, MG_ERR_DEVICE_ARG);
+    tactic[0] = ok ? x.tile_q : 0;
+    tactic[1] = ok ? x.blocks : 0;
+    tactic[2] = c;
+    if (state != nullptr) *state = c;
+  }
+}
+
 __global__ void wait_selftest_kernel(int32_t* status, int64_t limit_ns) {
   __shared__ uint64_t bar;
   __shared__ int32_t abort_flag;
@@ -163,6 +276,53 @@ cudaError_t launch_select(bool fp8, int variant, const int32_t* counts, int32_t 
                                  (int32_t)sel_kblocks(fp8, K), num_sms_current_device(), tile_q,
                                  status);
   return cudaGetLastError();
+}
+
+cudaError_t launch_exemplar(const int32_t* counts, int32_t E, const mg_exemplar* table, int32_t n,
+                            int32_t margin, int32_t* state, int32_t* tactic, int32_t* status,
+                            cudaStream_t s) {
+  exemplar_kernel<<<1, kPlanThreads, 0, s>>>(counts, E, table, n, margin, state, tactic, status);
+  return cudaGetLastError();
+}
+
+void exemplar_features_host(const int32_t* counts, int32_t E, int32_t* lu, int32_t* share) {
+  std::vector<int64_t> c((size_t)E);
+  for (int32_t e = 0; e < E; ++e) c[(size_t)e] = counts[e] > 0 ? counts[e] : 0;
+  std::sort(c.begin(), c.end(), [](int64_t a, int64_t b) { return a > b; });
+  std::vector<int64_t> prefix((size_t)E + 1, 0);
+  for (int32_t e = 0; e < E; ++e) prefix[(size_t)e + 1] = prefix[(size_t)e] + c[(size_t)e];
+  const int64_t U = prefix[(size_t)E];
+  *lu = 0;
+  for (int k = 0; k < kExemplarShares; ++k) {
+    const int32_t m = ((k + 1) * E + kExemplarShares - 1) / kExemplarShares;
+    share[k] = U > 0 ? (int32_t)((int64_t)kShareOne * prefix[(size_t)m] / U) : 0;
+  }
+  if (U > 0) {
+    int e = 0;
+    while ((U >> (e + 1)) != 0) ++e;
+    *lu = 16 * e + (int32_t)((16 * (U - (int64_t(1) << e))) >> e);
+  }
+}
+
+int32_t exemplar_choose_host(const int32_t* counts, int32_t E, const mg_exemplar* table, int32_t n,
+                             int32_t margin, int32_t prev, int64_t* dist_out) {
+  int32_t lu, share[kExemplarShares];
+  exemplar_features_host(counts, E, &lu, share);
+  int64_t bd = INT64_MAX;
+  int32_t bi = 0;
+  std::vector<int64_t> d((size_t)n);
+  for (int32_t i = 0; i < n; ++i) {
+    int64_t x = (int64_t)kLuWeight * std::llabs((int64_t)lu - table[i].lu);
+    for (int k = 0; k < kExemplarShares; ++k) x += std::llabs((int64_t)share[k] - table[i].share[k]);
+    d[(size_t)i] = x;
+    if (x < bd) {
+      bd = x;
+      bi = i;
+    }
+  }
+  if (prev >= 0 && prev < n && d[(size_t)prev] - bd <= (int64_t)margin) bi = prev;
+  if (dist_out != nullptr) *dist_out = d[(size_t)bi];
+  return bi;
 }
 
 cudaError_t launch_wait_selftest(int32_t* status, int64_t limit_ns, cudaStream_t s) {

@@ -26,7 +26,7 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for f in ("moe_plan", "moe_plan_host", "mgemm_contiguous", "mgemm_masked", "kgemm_grouped",
+    for f in ("moe_plan", "moe_plan_host", "mgemm_contiguous", "mgemm_masked", "kgemm_grouped", "moe_select_exemplar", "mgemm_contiguous_tactic",
               "moe_select_tile", "mg_status_str", "mgemm_contiguous_swiglu", "mgemm_masked_swiglu"):
         assert f in names
     assert set(names) == set(mb.SIGNATURES), "binding and header disagree"
@@ -205,3 +205,37 @@ def test_kernel_policy_setting(lib):
         assert lib.mg_set_kernel_policy(-1) == 1 and lib.mg_get_kernel_policy() == 0
     finally:
         lib.mg_set_kernel_policy(0)
+
+
+def test_exemplar_features_and_choice_match_the_oracle(lib):
+    """Host features and choice (what table builders and tests use) equal the
+    oracle's integer definitions bit for bit."""
+    from oracle import selector as osel
+    rng = random.Random(11)
+    for _ in range(300):
+        E = rng.choice([1, 3, 8, 16, 33, 64, 256, 1000])
+        c = [rng.choice([0, 0, 1, 5, 17, 300, 9000, 40000]) * rng.randrange(0, 3) for _ in range(E)]
+        assert mb.exemplar_features_host(c) == osel.features(c)
+    for _ in range(200):
+        n = rng.randrange(1, 12)
+        entries = [{"lu": rng.randrange(0, 300), "shares": sorted(rng.randrange(0, 65537) for _ in range(16)),
+                    "tile_q": 16 * rng.randrange(1, 16), "blocks": rng.choice([1, 2])} for _ in range(n)]
+        table = mb.exemplar_table(entries)
+        c = [rng.randrange(0, 2000) for _ in range(rng.randrange(1, 70))]
+        prev = rng.randrange(-1, n)
+        margin = rng.choice([0, 1000, 30000, 10 ** 6])
+        assert mb.select_exemplar_host(c, table, margin, prev) == osel.choose(c, entries, prev, margin)
+
+
+def test_exemplar_calls_reject_bad_arguments(lib):
+    L = lib
+    assert L.moe_select_exemplar(FAKE, 0, FAKE, 1, 0, None, FAKE, None, None) == 1        # E
+    assert L.moe_select_exemplar(FAKE, 8, FAKE, 0, 0, None, FAKE, None, None) == 1        # n
+    assert L.moe_select_exemplar(FAKE, 8, FAKE, 1, -1, None, FAKE, None, None) == 1       # margin
+    assert L.moe_select_exemplar(FAKE, 5000, FAKE, 1, 0, None, FAKE, None, None) == 2     # E > 4096
+    assert L.moe_select_exemplar(FAKE, 8, FAKE, 2000, 0, None, FAKE, None, None) == 2     # n > 1024
+    assert L.moe_select_exemplar(FAKE, 8, FAKE, 1, 0, None, None, None, None) == 1        # tactic NULL
+    t = [mb.MG_BF16, FAKE, None, FAKE, None, FAKE, FAKE, 8, 1024, 256, 256, 16, None, None, None]
+    assert L.mgemm_contiguous_tactic(*t) == 1                                              # tactic NULL
+    assert L.mgemm_masked_tactic(mb.MG_BF16, FAKE, None, FAKE, None, FAKE, FAKE, 8, 64, 256, 256, None,
+                                 None, None) == 1
