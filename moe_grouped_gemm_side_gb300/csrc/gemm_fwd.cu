@@ -361,7 +361,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kMaxStages; ++i) {
-      mbar_init(&sh.full[i], 1);
+      // single SM, fp8: the scale warp's arrival completes the stage's
+      // operand barrier too, so the MMA thread tests one barrier per stage
+      mbar_init(&sh.full[i], (!kPair && p.fp8) ? 2 : 1);
       mbar_init(&sh.empty[i], 1);
       mbar_init(&sh.sf_full[i], 1);
       mbar_init(&sh.sf_ready[i], kPair ? 2 : 1);
@@ -624,14 +626,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================================================= MMA issuer (one thread)
     if (leader && lane == 0 && S > 0) {
       // a stage is ready once its operands landed and (fp8) its scale words
-      // are built
-      // (FP4 weights: the weight-scale boxes that tcgen05.cp reads land on
-      // sf_full, which the scale warp waited on before sf_ready; the MMA
-      // thread waits on it too, so it observes the copies itself)
+      // are built: on one SM both complete the stage's barrier (each test of
+      // a barrier costs the issuing thread ~80 cycles); a pair's scale words
+      // are built in both CTAs and counted on sf_ready
       auto ready = [&](uint32_t st, uint32_t ph) {
         return wait_bounded(&sh.full[st], ph, deadline, &sh.abort_flag, p.status) &&
-               (!p.fp8 || wait_bounded(&sh.sf_ready[st], ph, deadline, &sh.abort_flag, p.status)) &&
-               (!kW4 || wait_bounded(&sh.sf_full[st], ph, deadline, &sh.abort_flag, p.status));
+               (!(kPair && p.fp8) || wait_bounded(&sh.sf_ready[st], ph, deadline, &sh.abort_flag, p.status));
       };
       with_blocks([&](auto bc) {
       constexpr int kB = decltype(bc)::value;
@@ -653,6 +653,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // FP4 weights (the MMA's A operand): A format E2M1
         const uint32_t idesc0 = p.fp8 ? (idesc_mxf8(kBlockRows, qn) | (kW4 ? kIdescAE2M1 : 0u))
                                       : idesc_bf16(kBlockRows, qn, 0, 0);
+        // Unrolled twice: the jump back to the loop top cost the issuing
+        // thread ~200 cycles per iteration (measured with in-kernel clock
+        // stamps), time in which the shallow tensor-pipe queue runs dry.
+#pragma unroll 2
         for (int32_t kb = 0; kb < KB; ++kb) {
           uint8_t* sw = ring + (size_t)stage * stage_bytes;
           const uint32_t a0 = smem_u32(sw), b0 = smem_u32(sw + kB * kWTileBytes);
@@ -795,7 +799,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) {
             if constexpr (kPair) mbar_arrive_cluster(ready0 + stage * (uint32_t)sizeof(uint64_t));
-            else mbar_arrive(&sh.sf_ready[stage]);
+            else mbar_arrive(&sh.full[stage]);
           }
           if (kb == 0 && t + n_units < total && !kW4) fetch_wsf(t + n_units, wsf_nxt);
           if (++stage == (uint32_t)S) {
