@@ -126,7 +126,7 @@ mg_status moe_plan(const int32_t* d_counts, int32_t E, int32_t q,
  * Candidates are priced by padded MMA work, weight/activation traffic and
  * per-tile scheduling cost ("Padding is not the whole cost model"); the
  * constants were measured on GB300.  This is the choice mgemm_contiguous
- * makes when called with tile_q = 0.
+ * makes when called with tile_q = 0, and mgemm_masked always.
  *
  *   dt, N, K      as for mgemm_contiguous.
  *   d_counts      int32 [E] (device) / counts (host).
