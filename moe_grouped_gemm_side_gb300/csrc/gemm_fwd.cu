@@ -162,6 +162,29 @@ __device__ __forceinline__ Tile decode_tile(int32_t t, const int32_t* tpre, cons
   return tl;
 }
 
+// The packed weight scale word of K-block group g (bytes: K-blocks 4g..4g+3,
+// 127 past the end) for g = this lane, from a tile's scales held as lane l
+// owning K-blocks l, l+32, l+64, l+96.  Warp-collective; built once per tile
+// (16 shuffles), after which a group's word is one shuffle away.  Building
+// it per group on the scale warp took ~470 cycles per block and delayed the
+// stage's scale words by ~1100 cycles (in-kernel clock stamps).
+__device__ __forceinline__ uint32_t group_weight_word(const uint32_t (&wsf)[4], uint32_t lane, int32_t KB) {
+  uint32_t w = 0;
+#pragma unroll
+  for (int i = 0; i < kSfGroup; ++i) {
+    const int32_t k = 4 * (int32_t)lane + i;
+    const uint32_t src = (uint32_t)k & 31u;
+    const uint32_t v0 = __shfl_sync(0xffffffffu, wsf[0], src);
+    const uint32_t v1 = __shfl_sync(0xffffffffu, wsf[1], src);
+    const uint32_t v2 = __shfl_sync(0xffffffffu, wsf[2], src);
+    const uint32_t v3 = __shfl_sync(0xffffffffu, wsf[3], src);
+    const int32_t sel = (k >> 5) & 3;
+    const uint32_t v = sel == 1 ? v1 : sel == 2 ? v2 : sel == 3 ? v3 : v0;
+    w |= (k < KB ? (v & 0xFFu) : 127u) << (8 * i);
+  }
+  return w;
+}
+
 // kind::mxf8f6f4 instruction-descriptor A format E2M1 (FP4), bits 7-9.
 constexpr uint32_t kIdescAE2M1 = 5u << 7;
 
@@ -770,6 +793,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int b = 0; b < kB; ++b)
 #pragma unroll
           for (int i = 0; i < 4; ++i) wsf[b][i] = wsf_nxt[b][i];
+        // lane g: the word of group g of each block (K <= 16384: 32 groups)
+        uint32_t gword[kB];
+#pragma unroll
+        for (int b = 0; b < kB; ++b) gword[b] = kW4 ? 0u : group_weight_word(wsf[b], lane, KB);
         for (int32_t kb = 0; kb < KB; ++kb) {
           if (!warp_wait(&sh.sf_full[stage], phase, deadline, &sh.abort_flag, p.status)) {
             ok = false;
@@ -779,9 +806,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if ((kb % kSfGroup) == 0) {
             // lane l, column c of a word block holds the word of row c*32 + l
             // (FP4 weights: only the token words are built here)
-            sf_build_words(sfs, kW4 ? 0u : sf_weight_word(wsf[0], kb, KB), lane);
+            const int32_t g = kb / kSfGroup;
+            sf_build_words(sfs, __shfl_sync(0xffffffffu, gword[0], g), lane);
             if (kB == 2 && !kW4) {
-              const uint32_t w1 = sf_weight_word(wsf[kB - 1], kb, KB);
+              const uint32_t w1 = __shfl_sync(0xffffffffu, gword[kB - 1], g);
               *reinterpret_cast<uint4*>(sfs + kSfW1 + lane * 16) = make_uint4(w1, w1, w1, w1);
             }
           }
