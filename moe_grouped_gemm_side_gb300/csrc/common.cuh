@@ -385,26 +385,6 @@ constexpr int kSfGroup = 4;
 constexpr int kSfRawBytes = kSfGroup * 256;               // [4][256] token scale bytes
 constexpr int kSfStageBytes = kSfRawBytes + 512 + 1024;   // raw + weight words + token words
 
-// Weight scale bytes of K-blocks kb..kb+3 packed into one word (127 past
-// the end).  `wsf` holds a tile's scales, lane l owning K-blocks l, l+32,
-// l+64, l+96.  Warp-collective.
-__device__ __forceinline__ uint32_t sf_weight_word(const uint32_t (&wsf)[4], int32_t kb,
-                                                   int32_t KB) {
-  uint32_t w = 0;
-#pragma unroll
-  for (int i = 0; i < kSfGroup; ++i) {
-    const int32_t k2 = kb + i;
-    uint32_t v = __shfl_sync(0xffffffffu, wsf[0], k2 & 31);
-    const uint32_t v1 = __shfl_sync(0xffffffffu, wsf[1], k2 & 31);
-    const uint32_t v2 = __shfl_sync(0xffffffffu, wsf[2], k2 & 31);
-    const uint32_t v3 = __shfl_sync(0xffffffffu, wsf[3], k2 & 31);
-    const int32_t sel = (k2 >> 5) & 3;
-    v = sel == 1 ? v1 : sel == 2 ? v2 : sel == 3 ? v3 : v;
-    w |= (k2 < KB ? (v & 0xFFu) : 127u) << (8 * i);
-  }
-  return w;
-}
-
 // Scale words of one 4-K-block group, from the raw token scales at `sfs`
 // ([4][256] bytes): weight words (every row the same four bytes) at
 // sfs + 1024 and token words (row t: its scales in the four K-blocks) at
