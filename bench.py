@@ -538,6 +538,24 @@ def blas_threads():
     return len(os.sched_getaffinity(0))
 
 
+def tactic_report(dtype, counts, N, K, ms):
+    """The token tile the kernel picks on the device for this histogram (the
+    same pricing on the host), the pages' padded rows P at that tile, the rows
+    the kernel actually computes (each expert's last tile trimmed to a
+    multiple of 16) and the physical throughput they imply."""
+    q = mb.select_tile_host(dtype, counts, N, K, 0)
+    offs, _, st, code = mb.plan_host(counts, q, max_tiles=0)
+    assert code == 0
+    computed = 0
+    for t in counts:
+        if t > 0:
+            full, last = divmod(t, q)
+            computed += full * q + (-(-last // 16) * 16 if last else 0)
+    return {"N": N, "K": K, "tile_q": q, "P_at_tile": st.P, "U": st.U, "pad_frac_at_tile": st.pad_frac,
+            "rows_computed": computed, "active_experts": st.active, "effective_experts": st.eff_experts,
+            "physical_tflops": 2.0 * computed * N * K / (ms * 1e-3) / 1e12}
+
+
 def operands_label(fp8, w4):
     if w4:
         return "e4m3 + ue8m0 per (row, 128 K) x e2m1 weights + ue8m0 per (row, 32 K)"
@@ -650,6 +668,8 @@ def run_ours(args):
         "data": "synthetic",
         "config": dict(w.config(), kernel_policy=args.kernel_policy),
         "per_gemm_ms": per_gemm,
+        "tactics": ([tactic_report(w.dtype, w.counts, g["N"], g["K"], t) for g, t in zip(w.gemms, per_gemm)]
+                    if hasattr(w, "dtype") else None),
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,
