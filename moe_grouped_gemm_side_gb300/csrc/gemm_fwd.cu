@@ -100,7 +100,6 @@ struct Shared {
   uint64_t full[kMaxStages];      // operand bytes (of both CTAs of a pair) landed
   uint64_t empty[kMaxStages];     // the MMAs reading the stage are done
   uint64_t sf_full[kMaxStages];   // fp8: this CTA's raw scale bytes of the stage landed
-  uint64_t sf_ready[kMaxStages];  // fp8: scale words of the stage built (in every CTA)
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint64_t drain;
@@ -115,6 +114,9 @@ struct Shared {
   // tokens, exchanged between the four epilogue warps of one half
   uint64_t amax_bar[2];
   float amax[4][256];
+  // pairs, fp8: a group of four K-blocks' scale words built in both CTAs
+  // (indexed by group & 3, phase = (group >> 2) & 1)
+  uint64_t sf_grp[4];
 };
 
 struct Tile {
@@ -389,7 +391,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sh.full[i], (!kPair && p.fp8) ? 2 : 1);
       mbar_init(&sh.empty[i], 1);
       mbar_init(&sh.sf_full[i], 1);
-      mbar_init(&sh.sf_ready[i], kPair ? 2 : 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh.acc_full[i], 1);
@@ -397,6 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&sh.drain, 1);
     for (int i = 0; i < 2; ++i) mbar_init(&sh.amax_bar[i], 4 * 32);
+    for (int i = 0; i < 4; ++i) mbar_init(&sh.sf_grp[i], 2);
     sh.abort_flag = 0;
     fence_barrier_init();
   }
@@ -650,14 +652,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ================================================= MMA issuer (one thread)
     if (leader && lane == 0 && S > 0) {
-      // a stage is ready once its operands landed and (fp8) its scale words
-      // are built: on one SM both complete the stage's barrier (each test of
-      // a barrier costs the issuing thread ~80 cycles); a pair's scale words
-      // are built in both CTAs and counted on sf_ready
+      // a stage is ready once its operands landed and (fp8, one SM) its scale
+      // words are built: both complete the stage's barrier (each test of a
+      // barrier costs the issuing thread ~80 cycles).  A pair's scale words
+      // are built in both CTAs and published once per group of four K-blocks
+      // on sf_grp, which the copies below wait for.  (Publishing every stage
+      // with a cluster-scope release cost each scale warp 1300-2800 cycles
+      // per stage: the pairs ran 25 % slower than one SM.)
       auto ready = [&](uint32_t st, uint32_t ph) {
-        return wait_bounded(&sh.full[st], ph, deadline, &sh.abort_flag, p.status) &&
-               (!(kPair && p.fp8) || wait_bounded(&sh.sf_ready[st], ph, deadline, &sh.abort_flag, p.status));
+        return wait_bounded(&sh.full[st], ph, deadline, &sh.abort_flag, p.status);
       };
+      uint32_t grp = 0;  // pairs: groups of scale words consumed
       with_blocks([&](auto bc) {
       constexpr int kB = decltype(bc)::value;
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
@@ -699,6 +704,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (p.fp8 && sid == 0) {
             const uint32_t sfs = smem_u32(sf_area + (size_t)stage * sf_bytes);
             if constexpr (kPair) {
+              if (!wait_bounded(&sh.sf_grp[grp & 3], (grp >> 2) & 1, deadline, &sh.abort_flag, p.status)) {
+                ok = false;
+                break;
+              }
+              ++grp;
               tmem_cp_32x128b_x4_pair(tmem + sfa_col, desc_sf_32x16(sfs + kSfRaw));
               if (kB == 2) tmem_cp_32x128b_x4_pair(tmem + sfa_col + 4, desc_sf_32x16(sfs + kSfW1));
               tmem_cp_32x128b_x4_pair(tmem + sfb_col, desc_sf_32x16(sfs + kSfRaw + 512));
@@ -769,7 +779,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (p.fp8 && S > 0) {
       uint32_t stage = 0, phase = 0;
       bool ok = true;
-      const uint32_t ready0 = mapa_shared(smem_u32(&sh.sf_ready[0]), 0);
+      const uint32_t grp0 = mapa_shared(smem_u32(&sh.sf_grp[0]), 0);
+      uint32_t wgrp = 0;  // groups of words published
       // weight scales of a tile's blocks: lane l holds K-blocks l + 32 i;
       // the next tile's are fetched while the current tile streams
       with_blocks([&](auto bc) {
@@ -798,6 +809,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int b = 0; b < kB; ++b) gword[b] = kW4 ? 0u : group_weight_word(wsf[b], lane, KB);
         for (int32_t kb = 0; kb < KB; ++kb) {
+          // A pair's scale words change only on the first K-block of a
+          // group, and the MMA thread waits for them only there, so the
+          // other stages are skipped: no wait, no arrival.  (Waiting on
+          // them would let this warp fall a whole ring cycle behind, since
+          // nothing holds the ring back for it on those stages.)
+          if (kPair && (kb % kSfGroup) != 0) {
+            if (++stage == (uint32_t)S) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
           if (!warp_wait(&sh.sf_full[stage], phase, deadline, &sh.abort_flag, p.status)) {
             ok = false;
             break;
@@ -828,8 +851,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if ((kb % kSfGroup) == 0 || kW4) fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            if constexpr (kPair) mbar_arrive_cluster(ready0 + stage * (uint32_t)sizeof(uint64_t));
-            else mbar_arrive(&sh.full[stage]);
+            if constexpr (kPair) {
+              if ((kb % kSfGroup) == 0) {
+                mbar_arrive_cluster(grp0 + (wgrp & 3) * (uint32_t)sizeof(uint64_t));
+                ++wgrp;
+              }
+            } else {
+              mbar_arrive(&sh.full[stage]);
+            }
           }
           if (kb == 0 && t + n_units < total && !kW4) fetch_wsf(t + n_units, wsf_nxt);
           if (++stage == (uint32_t)S) {
