@@ -1,0 +1,37 @@
+"""Host-side pieces of bench.py that need no GPU: the tactic report (tile the
+device prices, the pages' P at it, rows the kernel computes) against the
+oracle's plan, and the binding's choice of the FP8 x FP4 dtype from operand
+shapes."""
+import numpy as np
+import pytest
+import torch
+
+import bench
+from moe_grouped_gemm_side_gb300 import binding as mb
+from moe_grouped_gemm_side_gb300 import workloads as wl
+from oracle import plan as op
+
+pytestmark = pytest.mark.cpu
+
+
+@pytest.mark.parametrize("counts", [wl.counts_zipf_decode(), wl.counts_uniformish(), wl.counts_issue32(),
+                                    [0, 0, 0], [1, 15, 16, 17, 239, 240, 241]])
+def test_tactic_report_against_the_oracle_plan(lib, counts):
+    r = bench.tactic_report(mb.MG_FP8_E4M3_UE8M0, counts, 4096, 7168, 1.0)
+    q = r["tile_q"]
+    assert q == mb.select_tile_host(mb.MG_FP8_E4M3_UE8M0, counts, 4096, 7168, 0)
+    ref = op.plan(counts, q)
+    assert (r["P_at_tile"], r["U"], r["active_experts"]) == (ref.P, ref.U, ref.active)
+    # full tiles of q rows, the last tile of each expert trimmed to a multiple of 16
+    rows = sum((t // q) * q + (-(-(t % q) // 16) * 16) for t in counts)
+    assert r["rows_computed"] == rows
+    assert r["U"] <= r["rows_computed"] <= r["P_at_tile"]
+    assert r["physical_tflops"] == pytest.approx(2.0 * rows * 4096 * 7168 / 1e-3 / 1e12)
+
+
+def test_fp4_dtype_is_read_from_the_weight_shape():
+    A = torch.zeros((32, 512), dtype=torch.uint8)
+    assert mb._fwd_dtype(A, torch.zeros((2, 256, 256), dtype=torch.uint8), 512) == mb.MG_FP8_X_FP4_E2M1
+    assert mb._fwd_dtype(A, torch.zeros((2, 256, 512), dtype=torch.uint8), 512) == mb.MG_FP8_E4M3_UE8M0
+    assert mb._fwd_dtype(torch.zeros((32, 512), dtype=torch.bfloat16),
+                         torch.zeros((2, 256, 512), dtype=torch.bfloat16), 512) == mb.MG_BF16
