@@ -79,3 +79,23 @@ def test_choice_brute_force():
         d = [sum(abs(a - b) for a, b in zip(f[1], x["shares"])) + 2048 * abs(f[0] - x["lu"]) for x in table]
         best = min(range(len(table)), key=lambda i: (d[i], i))
         assert osel.choose(c, table) == best
+
+
+def test_committed_exemplar_tables_are_consistent():
+    """The tables tuned on the GPU store, per exemplar, the histogram it was
+    tuned on: its features must be the oracle's, and every tactic must be one
+    the GEMMs accept."""
+    import glob
+    import json
+    import os
+    from tests.conftest import ROOT
+    paths = sorted(glob.glob(os.path.join(ROOT, "moe_grouped_gemm_side_gb300", "exemplars", "*.json")))
+    assert paths
+    for path in paths:
+        with open(path) as f:
+            t = json.load(f)
+        assert t["exemplars"]
+        for x in t["exemplars"]:
+            assert (x["lu"], x["shares"]) == osel.features(x["counts"])
+            assert x["tile_q"] % 16 == 0 and 16 <= x["tile_q"] <= 256 and x["blocks"] in (1, 2)
+            assert f"{x['tile_q']}x{x['blocks']}" in x["times_us"]
