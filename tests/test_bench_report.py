@@ -35,3 +35,23 @@ def test_fp4_dtype_is_read_from_the_weight_shape():
     assert mb._fwd_dtype(A, torch.zeros((2, 256, 512), dtype=torch.uint8), 512) == mb.MG_FP8_E4M3_UE8M0
     assert mb._fwd_dtype(torch.zeros((32, 512), dtype=torch.bfloat16),
                          torch.zeros((2, 256, 512), dtype=torch.bfloat16), 512) == mb.MG_BF16
+
+
+def test_reference_arm_prints_one_contract_line(lib):
+    """`bench.py --impl reference` (the oracle on the host cores) prints one
+    JSON line with the contract's keys, on a small workload."""
+    import json
+    import subprocess
+    import sys
+    from tests.conftest import ROOT
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "contig_bf16_e8_n256_k256",
+                        "--steps", "2", "--warmup", "3"], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for k in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["value"] > 0 and d["config"]["workload"] == "contig_bf16_e8_n256_k256"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
