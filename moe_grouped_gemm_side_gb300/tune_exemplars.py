@@ -99,6 +99,14 @@ class Bench:
         return times, d_counts
 
 
+def pick_tactic(times, dtype, min_gain):
+    """The tactic an exemplar keeps: the default (widest tile, two blocks)
+    unless the fastest candidate beats it by more than min_gain."""
+    best = min(times, key=times.get)
+    default = f"{TILES[dtype][-1]}x2"
+    return best if times[best] < times[default] * (1.0 - min_gain) else default
+
+
 def tune(args):
     bench = Bench(args.dtype, args.E, args.N, args.K, max(U_TUNE))
     exemplars = []
@@ -108,11 +116,11 @@ def tune(args):
             times, _ = bench.sweep(counts)
             best = min(times, key=times.get)
             default = f"{TILES[args.dtype][-1]}x2"
-            pick = best if times[best] < times[default] * (1.0 - args.min_gain) else default
+            pick = pick_tactic(times, args.dtype, args.min_gain)
             tq, blocks = (int(x) for x in pick.split("x"))
             lu, shares = mb.exemplar_features_host(counts)
             exemplars.append({"lu": lu, "shares": shares, "tile_q": tq, "blocks": blocks, "U": U,
-                              "shape": f"{shape}({param})", "times_us": times})
+                              "shape": f"{shape}({param})", "counts": counts, "times_us": times})
             print(f"U={U:6d} {shape}({param}): best {best} {times[best]:.1f} us, default {times[default]:.1f} us"
                   f" -> {pick}", flush=True)
     out = {"dtype": args.dtype, "E": args.E, "N": args.N, "K": args.K, "align_q": bench.align,

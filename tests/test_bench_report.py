@@ -55,3 +55,17 @@ def test_reference_arm_prints_one_contract_line(lib):
         assert k in d, k
     assert d["impl"] == "reference" and d["value"] > 0 and d["config"]["workload"] == "contig_bf16_e8_n256_k256"
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_exemplar_tuner_guardrail():
+    """The tuner keeps the default tactic unless another beats it by more
+    than the margin; its histograms have the stated totals."""
+    from moe_grouped_gemm_side_gb300 import tune_exemplars as te
+    t = {"240x2": 100.0, "16x1": 98.0, "32x2": 101.0}
+    assert te.pick_tactic(t, "fp8", 0.03) == "240x2"           # 2 % better: not enough
+    assert te.pick_tactic(dict(t, **{"16x1": 96.0}), "fp8", 0.03) == "16x1"
+    assert te.pick_tactic({"256x2": 10.0, "64x2": 9.0}, "bf16", 0.03) == "64x2"
+    for U in (32, 1024, 32768):
+        for i, (shape, param) in enumerate(te.SHAPES):
+            c = te.histogram(shape, param, 64, U, seed=2000 + 37 * i + U)
+            assert len(c) == 64 and sum(c) == U and min(c) >= 0
