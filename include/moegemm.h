@@ -175,10 +175,11 @@ typedef struct {
   int32_t reserved;    /* 0                                                    */
 } mg_exemplar;         /* 80 bytes */
 
-/* Host: the features of one histogram (for building tables); E >= 1. */
+/* Host: the features of one histogram (for building tables); 1 <= E <= 4096
+ * (MG_ERR_UNSUPPORTED above, the device call's limit). */
 mg_status moe_exemplar_features_host(const int32_t* counts, int32_t E, int32_t* lu,
                                      int32_t* share /* [16] */);
-/* Host: the choice for one histogram (prev < 0: no history). */
+/* Host: the choice for one histogram (prev < 0: no history); E as above. */
 mg_status moe_select_exemplar_host(const int32_t* counts, int32_t E, const mg_exemplar* table,
                                    int32_t n, int32_t margin, int32_t prev, int32_t* choice);
 /* Device, one small kernel.  d_table: n entries in device memory (n <= 1024);

@@ -392,6 +392,7 @@ mg_status mgemm_masked_swiglu(mg_dtype dt, mg_swiglu_out out, const void* A, con
 
 mg_status moe_exemplar_features_host(const int32_t* counts, int32_t E, int32_t* lu, int32_t* share) {
   if (counts == nullptr || lu == nullptr || share == nullptr || E <= 0) return MG_ERR_INVALID_ARG;
+  if (E > kSelMaxExperts) return MG_ERR_UNSUPPORTED;  // keeps 65536 * (top-m sum) within int64
   exemplar_features_host(counts, E, lu, share);
   return MG_OK;
 }
@@ -400,6 +401,7 @@ mg_status moe_select_exemplar_host(const int32_t* counts, int32_t E, const mg_ex
                                    int32_t margin, int32_t prev, int32_t* choice) {
   if (counts == nullptr || table == nullptr || choice == nullptr || E <= 0 || n <= 0 || margin < 0)
     return MG_ERR_INVALID_ARG;
+  if (E > kSelMaxExperts) return MG_ERR_UNSUPPORTED;
   *choice = exemplar_choose_host(counts, E, table, n, margin, prev, nullptr);
   return MG_OK;
 }

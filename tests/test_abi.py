@@ -227,6 +227,24 @@ def test_exemplar_features_and_choice_match_the_oracle(lib):
         assert mb.select_exemplar_host(c, table, margin, prev) == osel.choose(c, entries, prev, margin)
 
 
+def test_exemplar_host_limits(lib):
+    """The largest histogram the host calls accept (4096 experts, every count
+    at the int32 maximum) stays exact; one expert more is refused, as on the
+    device, instead of overflowing the top-share products."""
+    from oracle import selector as osel
+    top = [2 ** 31 - 1] * 4096
+    assert mb.exemplar_features_host(top) == osel.features(top)
+    skew = [2 ** 31 - 1] * 7 + [1] * 4089
+    assert mb.exemplar_features_host(skew) == osel.features(skew)
+    c = (ctypes.c_int32 * 4097)(*([5] * 4097))
+    lu, share = ctypes.c_int32(0), (ctypes.c_int32 * 16)()
+    assert lib.moe_exemplar_features_host(c, 4097, ctypes.byref(lu), share) == 2
+    table = mb.exemplar_table([{"lu": 0, "shares": [0] * 16, "tile_q": 16, "blocks": 1}])
+    out = ctypes.c_int32(-7)
+    assert lib.moe_select_exemplar_host(c, 4097, table.ctypes.data, 1, 0, -1, ctypes.byref(out)) == 2
+    assert out.value == -7
+
+
 def test_exemplar_calls_reject_bad_arguments(lib):
     L = lib
     assert L.moe_select_exemplar(FAKE, 0, FAKE, 1, 0, None, FAKE, None, None) == 1        # E
