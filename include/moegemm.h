@@ -66,11 +66,13 @@ typedef enum {
 typedef struct {
   int64_t P;           /* padded token rows  sum_e q*ceil(t_e/q)             */
   int64_t U;           /* useful token rows  sum_e t_e                        */
-  int64_t sumsq;       /* sum_e t_e^2                                         */
+  int64_t sumsq;       /* sum_e t_e^2; INT64_MAX when it is 2^63 or more      */
   int32_t active;      /* experts with t_e > 0                                */
   int32_t num_tiles;   /* sum_e ceil(t_e/q)                                   */
   double pad_frac;     /* (double)(P-U) / (double)P; 0.0 when P == 0          */
-  double eff_experts;  /* ((double)U*(double)U) / (double)sumsq; 0.0 if none   */
+  double eff_experts;  /* ((double)U*(double)U) / (double)(exact sum_e t_e^2),
+                          every conversion and operation rounded to nearest;
+                          0.0 if no expert has tokens                         */
 } mg_plan_stats;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -103,9 +105,12 @@ const char* mg_status_str(mg_status s);
  * only tiles whose first row fits are written and the call reports
  * MG_ERR_UNSUPPORTED (offsets and stats stay complete).
  * A negative count is MG_ERR_INVALID_ARG (host) / MG_ERR_DEVICE_ARG (device,
- * that expert counted as 0).  P, U and sumsq are exact in int64 for
- * E <= 2^20 and t_e < 2^31; the two doubles are correctly rounded IEEE
- * operations in the order written above, identical on host and device.
+ * that expert counted as 0).  P and U are exact in int64 for E <= 2^20 and
+ * t_e < 2^31; sum_e t_e^2 is formed exactly in two words, so sumsq is exact
+ * whenever it fits int64 (three experts at 2^31-1 tokens do not: sumsq then
+ * reads INT64_MAX) and eff_experts is correct either way.  The two doubles
+ * are correctly rounded IEEE operations in the order written above,
+ * identical on host and device.
  * ------------------------------------------------------------------------ */
 
 /* Host, synchronous, touches no GPU. */

@@ -11,6 +11,7 @@
 
 #include "mg_internal.h"
 #include "moegemm.h"
+#include "plan_sums.cuh"
 #include "sched.cuh"
 
 using namespace mg;
@@ -278,7 +279,7 @@ mg_status moe_plan_host(const int32_t* counts, int32_t E, int32_t q, int64_t* of
   if (tiles == nullptr && max_tiles > 0) return MG_ERR_INVALID_ARG;
   for (int32_t e = 0; e < E; ++e)
     if (counts[e] < 0) return MG_ERR_INVALID_ARG;
-  int64_t P = 0, U = 0, sumsq = 0, ntiles = 0;
+  int64_t P = 0, U = 0, sq_hi_sum = 0, sq_lo_sum = 0, ntiles = 0;
   int32_t active = 0;
   for (int32_t e = 0; e < E; ++e) {
     const int64_t c = counts[e];
@@ -294,17 +295,19 @@ mg_status moe_plan_host(const int32_t* counts, int32_t E, int32_t q, int64_t* of
     ntiles += nt;
     P += nt * q;
     U += c;
-    sumsq += c * c;
+    sq_hi_sum += sq_hi(c);
+    sq_lo_sum += sq_lo(c);
     active += c > 0;
   }
   offsets[E] = P;
   stats->P = P;
   stats->U = U;
-  stats->sumsq = sumsq;
+  const SumSq sq = sumsq_finish(sq_hi_sum, sq_lo_sum);
+  stats->sumsq = sq.value;
   stats->active = active;
   stats->num_tiles = (int32_t)ntiles;
   stats->pad_frac = plan_pad_frac(P, U);
-  stats->eff_experts = plan_eff_experts(U, sumsq);
+  stats->eff_experts = plan_eff_experts_exact(U, sq.f64);
   if (tiles != nullptr && ntiles > max_tiles) return MG_ERR_CAPACITY;
   if (tiles != nullptr && max_tiles > 0 && P > INT32_MAX) return MG_ERR_UNSUPPORTED;
   return MG_OK;

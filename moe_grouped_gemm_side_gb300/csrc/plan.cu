@@ -9,6 +9,7 @@
 
 #include "common.cuh"
 #include "mg_internal.h"
+#include "plan_sums.cuh"
 #include "sched.cuh"
 
 namespace mg {
@@ -51,7 +52,7 @@ __global__ void __launch_bounds__(kPlanThreads)
                 int64_t* __restrict__ offsets, int32_t* __restrict__ tiles, int32_t max_tiles,
                 mg_plan_stats* __restrict__ stats, int32_t* status) {
   __shared__ int64_t scratch[32];
-  int64_t carry_rows = 0, carry_tiles = 0, U = 0, sumsq = 0, active = 0;
+  int64_t carry_rows = 0, carry_tiles = 0, U = 0, sq_hi_sum = 0, sq_lo_sum = 0, active = 0;
   for (int32_t base = 0; base < E; base += kPlanThreads) {
     const int32_t e = base + threadIdx.x;
     int64_t c = 0;
@@ -82,21 +83,24 @@ __global__ void __launch_bounds__(kPlanThreads)
     carry_tiles += tot_tiles;
     block_exclusive_scan<int64_t>(c, scratch, tot);
     U += tot;
-    block_exclusive_scan<int64_t>(c * c, scratch, tot);
-    sumsq += tot;
+    block_exclusive_scan<int64_t>(sq_hi(c), scratch, tot);
+    sq_hi_sum += tot;
+    block_exclusive_scan<int64_t>(sq_lo(c), scratch, tot);
+    sq_lo_sum += tot;
     block_exclusive_scan<int64_t>(c > 0 ? 1 : 0, scratch, tot);
     active += tot;
   }
   if (threadIdx.x == 0) {
     offsets[E] = carry_rows;
+    const SumSq sq = sumsq_finish(sq_hi_sum, sq_lo_sum);
     mg_plan_stats s;
     s.P = carry_rows;
     s.U = U;
-    s.sumsq = sumsq;
+    s.sumsq = sq.value;
     s.active = (int32_t)active;
     s.num_tiles = (int32_t)carry_tiles;
     s.pad_frac = plan_pad_frac(carry_rows, U);
-    s.eff_experts = plan_eff_experts(U, sumsq);
+    s.eff_experts = plan_eff_experts_exact(U, sq.f64);
     *stats = s;
     if (tiles != nullptr && carry_tiles > max_tiles) set_status(status, MG_ERR_CAPACITY);
     if (tiles != nullptr && max_tiles > 0 && carry_rows > 2147483647LL) set_status(status, MG_ERR_UNSUPPORTED);

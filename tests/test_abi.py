@@ -88,6 +88,26 @@ def test_host_plan_edges(lib):
     _check_plan(list(range(1024)), 7)
 
 
+# Sums of squares around 2^63: just below (exact), just above through the
+# low-half carry, and far above; sumsq saturates, eff_experts stays the
+# correctly rounded ratio of the exact integers.
+SQ = 2 ** 31 - 1
+SQUARE_SUM_EDGES = ([SQ, SQ], [SQ, SQ, 92681], [SQ, SQ, 92681, 65535], [SQ] * 3, [SQ] * 1000 + [0, 7])
+
+
+def test_host_plan_square_sum_past_int64(lib):
+    for counts in SQUARE_SUM_EDGES:
+        offs, _, st, code = mb.plan_host(counts, 1 << 20, max_tiles=0)
+        ref = op.plan(counts, 1 << 20)
+        assert code == 0 and offs.tolist() == ref.offsets
+        assert (st.P, st.U, st.active) == (ref.P, ref.U, ref.active)
+        assert st.sumsq == min(ref.sumsq, 2 ** 63 - 1)
+        assert st.pad_frac.hex() == ref.pad_frac.hex()
+        assert st.eff_experts.hex() == ref.eff_experts.hex()
+    assert sum(c * c for c in SQUARE_SUM_EDGES[1]) == 2 ** 63 - 166829
+    assert sum(c * c for c in SQUARE_SUM_EDGES[2]) > 2 ** 63
+
+
 def test_host_plan_capacity_and_errors(lib):
     offs, tiles, st, code = mb.plan_host([17] * 8, 8, max_tiles=5)
     assert code == 4 and st.P == 192 and st.num_tiles == 24 and offs[-1] == 192

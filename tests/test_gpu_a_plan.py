@@ -63,6 +63,20 @@ def test_device_plan_issue_histogram(lib, cuda):
         _assert_plan(wl.counts_issue32(), q)
 
 
+def test_device_plan_square_sum_past_int64(lib, cuda):
+    """Sums of squares around 2^63 (just below, just above through the
+    low-half carry, far above): sumsq saturates, eff_experts stays the
+    correctly rounded ratio of the exact integers, as on the host."""
+    q = 2 ** 31 - 1
+    for counts in ([q, q], [q, q, 92681], [q, q, 92681, 65535], [q] * 3, [q] * 1000 + [0, 7]):
+        ref, offs, _, st, status = _device_plan(counts, 1 << 20, max_tiles=0)
+        assert status == 0 and offs == ref.offsets
+        assert (st["P"], st["U"], st["active"]) == (ref.P, ref.U, ref.active)
+        assert st["sumsq"] == min(ref.sumsq, 2 ** 63 - 1)
+        assert float(st["pad_frac"]).hex() == ref.pad_frac.hex()
+        assert float(st["eff_experts"]).hex() == ref.eff_experts.hex()
+
+
 def test_device_plan_errors(lib, cuda):
     ref, offs, tiles, st, status = _device_plan([17] * 8, 8, max_tiles=5)
     assert status == 4 and st["P"] == 192 and tiles == ref.tiles[:5] and offs == ref.offsets
