@@ -3,7 +3,10 @@
 Argument marshalling only: every step of the path runs in the library's CUDA
 kernels.  Torch tensors supply device memory and the current stream; nothing
 here computes the method, and every call raises if the library is missing or
-returns an error.
+returns an error.  Because the C ABI receives bare pointers, each device call
+first checks its tensors (on the GPU, contiguous, expected dtype, at least as
+many bytes as the call reaches) and raises ValueError / TypeError before any
+launch.
 """
 import ctypes
 import os
@@ -101,6 +104,51 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+def _on_device(t) -> bool:
+    return t.is_cuda
+
+
+def _need(t, name: str, nbytes: int, dtypes=None):
+    """Checks a tensor the library reaches through a bare pointer: on the GPU,
+    dense row-major, of an accepted dtype and at least `nbytes` long (the C
+    ABI cannot see buffer sizes, so a short buffer would be overrun)."""
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if not _on_device(t):
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtypes is not None and t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}")
+    have = t.numel() * t.element_size()
+    if have < nbytes:
+        raise ValueError(f"{name} holds {have} bytes; the call reaches {nbytes}")
+
+
+def _opt(t, name: str, nbytes: int, dtypes=None):
+    if t is not None:
+        _need(t, name, nbytes, dtypes)
+
+
+def _int32():
+    import torch
+    return (torch.int32,)
+
+
+def _check_fwd(dt, A, B, D, d_counts, SFA, SFB, status, rows_total, rows_sf, sf_groups, N, K, E):
+    """Operands of the contiguous and masked forms: D bf16 [rows_total, N];
+    SFA [sf_groups, K/128, rows_sf]; SFB [E, K/128, N/128] (E4M3 weights) or
+    [E, N, K/32] (E2M1 weights); counts int32 [E]."""
+    import torch
+    _need(A, "A", A.numel() * A.element_size())
+    _need(B, "B", B.numel() * B.element_size())
+    _need(D, "D", rows_total * N * 2, (torch.bfloat16,))
+    _need(d_counts, "counts", E * 4, _int32())
+    _opt(SFA, "SFA", sf_groups * (K // 128) * rows_sf)
+    _opt(SFB, "SFB", E * N * (K // 32) if dt == MG_FP8_X_FP4_E2M1 else E * (K // 128) * (N // 128))
+    _opt(status, "status", 4, _int32())
+
+
 def _stream(stream):
     import torch
     s = stream if stream is not None else torch.cuda.current_stream()
@@ -169,6 +217,8 @@ def plan(d_counts, q: int, max_tiles: int, status=None, stream=None):
     """moe_plan on device tensors; returns (offsets, tiles, stats_bytes)."""
     import torch
     lib = load()
+    _need(d_counts, "counts", 0, _int32())
+    _opt(status, "status", 4, _int32())
     dev = d_counts.device
     E = d_counts.numel()
     offsets = torch.empty(E + 1, dtype=torch.int64, device=dev)
@@ -183,6 +233,8 @@ def plan(d_counts, q: int, max_tiles: int, status=None, stream=None):
 def select_tile(dtype: int, d_counts, N: int, K: int, status=None, stream=None):
     import torch
     lib = load()
+    _need(d_counts, "counts", 0, _int32())
+    _opt(status, "status", 4, _int32())
     out = torch.zeros(1, dtype=torch.int32, device=d_counts.device)
     _check("moe_select_tile", lib.moe_select_tile(dtype, _ptr(d_counts), d_counts.numel(), N, K,
                                                   _ptr(out), _ptr(status), _stream(stream)))
@@ -194,8 +246,10 @@ def mgemm_contiguous(A, B, D, d_counts, align_q: int, SFA=None, SFB=None, tile_q
     lib = load()
     rows_cap, K = A.shape
     E, N, _ = B.shape
+    dt = _fwd_dtype(A, B, K)
+    _check_fwd(dt, A, B, D, d_counts, SFA, SFB, status, rows_cap, rows_cap, 1, N, K, E)
     _check("mgemm_contiguous", lib.mgemm_contiguous(
-        _fwd_dtype(A, B, K), _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(D), _ptr(d_counts), E,
+        dt, _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(D), _ptr(d_counts), E,
         rows_cap, N, K, align_q, tile_q, _ptr(status), _stream(stream)))
 
 
@@ -203,8 +257,10 @@ def mgemm_masked(A, B, D, d_valid_m, SFA=None, SFB=None, status=None, stream=Non
     lib = load()
     E, M_max, K = A.shape
     N = B.shape[1]
+    dt = _fwd_dtype(A, B, K)
+    _check_fwd(dt, A, B, D, d_valid_m, SFA, SFB, status, E * M_max, M_max, E, N, K, E)
     _check("mgemm_masked", lib.mgemm_masked(
-        _fwd_dtype(A, B, K), _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(D), _ptr(d_valid_m), E,
+        dt, _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(D), _ptr(d_valid_m), E,
         M_max, N, K, _ptr(status), _stream(stream)))
 
 
@@ -217,6 +273,20 @@ def _swiglu_out(Y):
     raise TypeError(f"unsupported SwiGLU output dtype {Y.dtype}")
 
 
+def _check_swiglu(dt, out, A, B, Y, SFY, d_counts, SFA, SFB, status, rows_total, rows_sf, sf_groups, N, K, E):
+    """As _check_fwd, with Y [rows_total, N/2] in place of D and, for E4M3
+    output, SFY [sf_groups, N/256, rows_sf]."""
+    _need(A, "A", A.numel() * A.element_size())
+    _need(B, "B", B.numel() * B.element_size())
+    _need(Y, "Y", rows_total * (N // 2) * Y.element_size())
+    _need(d_counts, "counts", E * 4, _int32())
+    _opt(SFA, "SFA", sf_groups * (K // 128) * rows_sf)
+    _opt(SFB, "SFB", E * N * (K // 32) if dt == MG_FP8_X_FP4_E2M1 else E * (K // 128) * (N // 128))
+    if out == MG_SWIGLU_FP8_E4M3_UE8M0:
+        _opt(SFY, "SFY", sf_groups * (N // 256) * rows_sf)
+    _opt(status, "status", 4, _int32())
+
+
 def mgemm_contiguous_swiglu(A, B, Y, d_counts, align_q: int, SFA=None, SFB=None, SFY=None,
                             tile_q: int = 0, status=None, stream=None):
     """GEMM1 with SwiGLU fused into its epilogue; Y bf16 [rows_cap, N/2], or
@@ -224,8 +294,10 @@ def mgemm_contiguous_swiglu(A, B, Y, d_counts, align_q: int, SFA=None, SFB=None,
     lib = load()
     rows_cap, K = A.shape
     E, N, _ = B.shape
+    dt, out = _fwd_dtype(A, B, K), _swiglu_out(Y)
+    _check_swiglu(dt, out, A, B, Y, SFY, d_counts, SFA, SFB, status, rows_cap, rows_cap, 1, N, K, E)
     _check("mgemm_contiguous_swiglu", lib.mgemm_contiguous_swiglu(
-        _fwd_dtype(A, B, K), _swiglu_out(Y), _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(Y), _ptr(SFY),
+        dt, out, _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(Y), _ptr(SFY),
         _ptr(d_counts), E, rows_cap, N, K, align_q, tile_q, _ptr(status), _stream(stream)))
 
 
@@ -234,8 +306,10 @@ def mgemm_masked_swiglu(A, B, Y, d_valid_m, SFA=None, SFB=None, SFY=None, status
     lib = load()
     E, M_max, K = A.shape
     N = B.shape[1]
+    dt, out = _fwd_dtype(A, B, K), _swiglu_out(Y)
+    _check_swiglu(dt, out, A, B, Y, SFY, d_valid_m, SFA, SFB, status, E * M_max, M_max, E, N, K, E)
     _check("mgemm_masked_swiglu", lib.mgemm_masked_swiglu(
-        _fwd_dtype(A, B, K), _swiglu_out(Y), _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(Y), _ptr(SFY),
+        dt, out, _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(Y), _ptr(SFY),
         _ptr(d_valid_m), E, M_max, N, K, _ptr(status), _stream(stream)))
 
 
@@ -283,6 +357,11 @@ def select_exemplar_host(counts, table: np.ndarray, margin: int = 0, prev: int =
 def select_exemplar(d_counts, d_table, n: int, d_tactic, margin: int = 0, d_state=None, status=None,
                     stream=None):
     """moe_select_exemplar: writes {tile_q, blocks, index} to d_tactic (int32 [3])."""
+    _need(d_counts, "counts", 0, _int32())
+    _need(d_table, "table", n * EXEMPLAR_DTYPE.itemsize)
+    _need(d_tactic, "tactic", 12, _int32())
+    _opt(d_state, "state", 4, _int32())
+    _opt(status, "status", 4, _int32())
     _check("moe_select_exemplar", load().moe_select_exemplar(
         _ptr(d_counts), d_counts.numel(), _ptr(d_table), n, margin, _ptr(d_state), _ptr(d_tactic),
         _ptr(status), _stream(stream)))
@@ -293,8 +372,11 @@ def mgemm_contiguous_tactic(A, B, D, d_counts, align_q: int, d_tactic, SFA=None,
     lib = load()
     rows_cap, K = A.shape
     E, N, _ = B.shape
+    dt = _fwd_dtype(A, B, K)
+    _check_fwd(dt, A, B, D, d_counts, SFA, SFB, status, rows_cap, rows_cap, 1, N, K, E)
+    _need(d_tactic, "tactic", 8, _int32())
     _check("mgemm_contiguous_tactic", lib.mgemm_contiguous_tactic(
-        _fwd_dtype(A, B, K), _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(D), _ptr(d_counts), E,
+        dt, _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(D), _ptr(d_counts), E,
         rows_cap, N, K, align_q, _ptr(d_tactic), _ptr(status), _stream(stream)))
 
 
@@ -302,16 +384,25 @@ def mgemm_masked_tactic(A, B, D, d_valid_m, d_tactic, SFA=None, SFB=None, status
     lib = load()
     E, M_max, K = A.shape
     N = B.shape[1]
+    dt = _fwd_dtype(A, B, K)
+    _check_fwd(dt, A, B, D, d_valid_m, SFA, SFB, status, E * M_max, M_max, E, N, K, E)
+    _need(d_tactic, "tactic", 8, _int32())
     _check("mgemm_masked_tactic", lib.mgemm_masked_tactic(
-        _fwd_dtype(A, B, K), _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(D), _ptr(d_valid_m), E,
+        dt, _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(D), _ptr(d_valid_m), E,
         M_max, N, K, _ptr(d_tactic), _ptr(status), _stream(stream)))
 
 
 def kgemm_grouped(dY, X, dW, d_counts, status=None, stream=None):
+    import torch
     lib = load()
     T_cap, N = dY.shape
     K = X.shape[1]
     E = dW.shape[0]
+    _need(dY, "dY", T_cap * N * 2, (torch.bfloat16,))
+    _need(X, "X", T_cap * K * 2, (torch.bfloat16,))
+    _need(dW, "dW", E * N * K * 4, (torch.float32,))
+    _need(d_counts, "counts", E * 4, _int32())
+    _opt(status, "status", 4, _int32())
     _check("kgemm_grouped", lib.kgemm_grouped(_ptr(dY), _ptr(X), _ptr(dW), _ptr(d_counts), E,
                                               T_cap, N, K, _ptr(status), _stream(stream)))
 
@@ -325,6 +416,7 @@ def get_wait_limit_ns() -> int:
 
 
 def wait_selftest(status, limit_ns: int, stream=None):
+    _need(status, "status", 4, _int32())
     _check("mg_wait_selftest", load().mg_wait_selftest(_ptr(status), int(limit_ns), _stream(stream)))
 
 
