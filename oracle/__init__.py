@@ -20,16 +20,23 @@ What it computes, and where each rule comes from:
   UE8M0 power-of-two scale bytes ("flops/deepgemm-grouped-masked-moe-gemm",
   "Workarounds": FP8 with per-group scaling, UE8M0 on SM100), plus the
   block-scale dequantisation of activations (one scale per row and 128 K)
-  and weights (one scale per 128 N x 128 K block).
+  and weights (one scale per 128 N x 128 K block); E2M1 4-bit weights with
+  one UE8M0 scale per (row, 32 K) (same section: FP8 x FP4 MoE GEMMs).
 * ``gemm``      -- the three grouped GEMM forms, in float64 on dequantised
   inputs: M-grouped contiguous, masked, and K-grouped weight gradient
   ("flops/deepgemm-grouped-masked-moe-gemm", "Arithmetic intensity" and
   "Workarounds"; "MoE GroupGEMM padding under expert skew", "Grouped execution
   does not require padded experts").
+* ``epilogue``  -- SwiGLU of GEMM1's gate and up halves and the E4M3 / UE8M0
+  re-quantisation that feeds GEMM2 ("flops/deepgemm-grouped-masked-moe-gemm",
+  "Workarounds": SwiGLU fused between the two grouped GEMMs of the MoE).
+* ``selector``  -- the exemplar choice of a token tile from the count
+  histogram ("MoE GroupGEMM padding under expert skew", "Adapt kernels
+  without adding a CPU stall"), in integers.
 
 Every function is pinned by ``tests/test_oracle_*.py`` against values the
 pages print, closed forms, invariants and brute force; no function here is
 "parity unpinned".
 """
 
-from . import plan, numerics, gemm  # noqa: F401
+from . import plan, numerics, gemm, epilogue, selector  # noqa: F401
