@@ -32,7 +32,9 @@
  *     kernel that cannot make progress writes MG_ERR_TIMEOUT to *d_status,
  *     drains its own in-flight copies, frees its tensor memory and returns.
  *   - Global base addresses must be 16-byte aligned; N and K must be
- *     multiples of 128.
+ *     multiples of 128.  The GEMM calls take at most 1024 experts and
+ *     E * N < 2^31 (weight rows are 32-bit coordinates); FP8 forms take
+ *     K <= 16384.  Beyond these limits a call returns MG_ERR_UNSUPPORTED.
  */
 #ifndef MOEGEMM_H
 #define MOEGEMM_H

@@ -451,6 +451,7 @@ mg_status kgemm_grouped(const void* dY, const void* X, float* dW, const int32_t*
   if (E <= 0 || N <= 0 || K <= 0 || T_cap <= 0 || T_cap >= (int64_t(1) << 31)) return MG_ERR_INVALID_ARG;
   if (E > kMaxExperts) return MG_ERR_UNSUPPORTED;
   if (N % 128 != 0 || K % 128 != 0) return MG_ERR_UNSUPPORTED;
+  if ((int64_t)E * N >= (int64_t(1) << 31)) return MG_ERR_UNSUPPORTED;  // dW rows are int32 coordinates
   if (!aligned16(dY) || !aligned16(X) || !aligned16(dW) || !aligned16(d_counts)) return MG_ERR_INVALID_ARG;
   KgArgs a;
   a.counts = d_counts;

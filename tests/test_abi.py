@@ -205,6 +205,26 @@ def test_device_calls_reject_bad_arguments_before_launch(lib):
     assert L.mg_wait_selftest(None, 1000, None) == 1
 
 
+def test_gemm_shape_limits(lib):
+    """The limits the header states for every GEMM call: 1024 experts,
+    E * N < 2^31, fp8 K <= 16384; all refused before any launch."""
+    L = lib
+    base = [mb.MG_BF16, FAKE, None, FAKE, None, FAKE, FAKE, 8, 1024, 256, 256, 16, 0, None, None]
+
+    def contig(**kw):
+        a = list(base)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return L.mgemm_contiguous(*a)
+    assert contig(a7=1025) == 2
+    assert contig(a7=1024, a9=2 ** 21) == 2                                  # E * N = 2^31
+    assert contig(a0=mb.MG_FP8_E4M3_UE8M0, a2=FAKE, a4=FAKE, a10=16384 + 128) == 2
+    kg = [FAKE, FAKE, FAKE, FAKE, 8, 1024, 256, 256, None, None]
+    assert L.kgemm_grouped(*[1025 if i == 4 else v for i, v in enumerate(kg)]) == 2
+    assert L.kgemm_grouped(*[1024 if i == 4 else 2 ** 21 if i == 6 else v for i, v in enumerate(kg)]) == 2
+    # (every case here is refused on the host: the pointers are fake)
+
+
 def test_wait_limit_setting(lib):
     old = lib.mg_get_wait_limit_ns()
     try:
