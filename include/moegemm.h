@@ -48,7 +48,7 @@ extern "C" {
 typedef enum {
   MG_OK = 0,
   MG_ERR_INVALID_ARG = 1,  /* null pointer, non-positive size, bad value      */
-  MG_ERR_UNSUPPORTED = 2,  /* valid request this build does not handle        */
+  MG_ERR_UNSUPPORTED = 2,  /* valid request this library does not handle      */
   MG_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed               */
   MG_ERR_CAPACITY = 4,     /* output or tile list too small for the counts     */
   MG_ERR_TIMEOUT = 5,      /* a device wait ran past the wait limit            */
