@@ -90,7 +90,8 @@ const char* mg_status_str(mg_status s);
  * each starting on a multiple of q ("flops/deepgemm-grouped-masked-moe-gemm",
  * "Arithmetic intensity").
  *
- *   counts / d_counts  int32 [E], t_e >= 0.
+ *   counts / d_counts  int32 [E], t_e >= 0; 1 <= E <= 2^20 and q >= 1
+ *                      (else MG_ERR_INVALID_ARG).
  *   offsets            int64 [E+1]: offsets[e] = sum_{e'<e} q*ceil(t_e'/q),
  *                      offsets[E] = P.  Expert e's rows: [offsets[e],
  *                      offsets[e] + t_e).

@@ -108,6 +108,15 @@ def test_host_plan_square_sum_past_int64(lib):
     assert sum(c * c for c in SQUARE_SUM_EDGES[2]) > 2 ** 63
 
 
+def test_host_plan_maximum_experts(lib):
+    """2^20 experts, the documented maximum, bit-exact; one more is refused."""
+    rng = random.Random(5)
+    c = [rng.choice([0, 0, 1, 3, 17, 40, 129]) for _ in range(1 << 20)]
+    _check_plan(c, 16)
+    _, _, _, code = mb.plan_host(c + [1], 16, max_tiles=0)
+    assert code == 1
+
+
 def test_host_plan_capacity_and_errors(lib):
     offs, tiles, st, code = mb.plan_host([17] * 8, 8, max_tiles=5)
     assert code == 4 and st.P == 192 and st.num_tiles == 24 and offs[-1] == 192

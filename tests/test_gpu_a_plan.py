@@ -63,6 +63,13 @@ def test_device_plan_issue_histogram(lib, cuda):
         _assert_plan(wl.counts_issue32(), q)
 
 
+def test_device_plan_maximum_experts(lib, cuda):
+    """2^20 experts (the documented maximum: 1024 block-scan passes of the
+    one-CTA plan), offsets, tiles and stats bit-exact."""
+    rng = random.Random(5)
+    _assert_plan([rng.choice([0, 0, 1, 3, 17, 40, 129]) for _ in range(1 << 20)], 16)
+
+
 def test_device_plan_square_sum_past_int64(lib, cuda):
     """Sums of squares around 2^63 (just below, just above through the
     low-half carry, far above): sumsq saturates, eff_experts stays the
