@@ -79,6 +79,22 @@ def poison_rows_(A, rows_mask_np, fp8: bool, SFA=None):
         A.view(torch.int16).index_fill_(0, idx, wl.BF16_NAN_BITS)
 
 
+def poison_experts_(B, dead, fp8: bool, SFB=None):
+    """Fill the weights (and weight scales) of experts that have no rows to
+    compute with NaN.  Such an expert loads no weights, and a tile that took
+    its weights from the wrong expert would carry the NaN into a valid row."""
+    idx = [e for e, d in enumerate(dead) if d]
+    if not idx:
+        return
+    i = torch.tensor(idx, dtype=torch.int64, device=B.device)
+    if fp8:
+        B.index_fill_(0, i, wl.E4M3_NAN_CODE)
+        if SFB is not None:
+            SFB.index_fill_(0, i, wl.UE8M0_NAN_CODE)
+    else:
+        B.view(torch.int16).index_fill_(0, i, wl.BF16_NAN_BITS)
+
+
 def integer_e4m3(shape, seed, device):
     """E4M3 codes of the integers -2..2 (exactly representable)."""
     lut = torch.tensor([0xC0, 0xB8, 0x00, 0x38, 0x40], dtype=torch.uint8)

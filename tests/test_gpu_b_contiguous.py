@@ -52,6 +52,7 @@ def run_contiguous(counts, N, K, dtype, align_q, tile_q=0, seed=1, integer=False
             ops = wl.make_contiguous(E, rows_cap, N, K, "fp8", seed, dev, a_std, b_std)
             A, B, SFA, SFB = ops.A, ops.B, ops.SFA, ops.SFB
     gu.poison_rows_(A, written, dtype == "fp8", SFA)
+    gu.poison_experts_(B, [t <= 0 for t in counts], dtype == "fp8", SFB)
     # oracle on the same bytes
     if dtype == "bf16":
         Ad = gu.deq_bf16(A)

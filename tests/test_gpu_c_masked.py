@@ -50,6 +50,7 @@ def run_masked(valid_m, M_max, N, K, dtype, seed=1, integer=False, dev="cuda"):
             inv = torch.from_numpy(np.nonzero(~valid[e])[0]).to(dev)
             if inv.numel():
                 SFA[e].index_fill_(1, inv, wl.UE8M0_NAN_CODE)
+    gu.poison_experts_(B, [not 0 < v <= M_max for v in valid_m], dtype == "fp8", SFB)
     if dtype == "bf16":
         Ad = gu.deq_bf16(A).reshape(E, M_max, K)
         Bd = gu.deq_bf16(B).reshape(E, N, K)
