@@ -194,3 +194,43 @@ def test_hysteresis_inverted_is_caught(monkeypatch):
         return best
     monkeypatch.setattr(osel, "choose", bad)
     assert fails(tsel.test_choice_ties_and_hysteresis)
+
+
+def test_kgrouped_aligned_token_segments_are_caught(monkeypatch):
+    """K-grouped tokens are packed with no alignment: segments that start on
+    a block boundary (the contiguous form's layout) must fail a pin."""
+    monkeypatch.setattr(og, "token_offsets", lambda counts: op.plan(counts, 4).offsets)
+    assert fails(tg.test_kgrouped_vs_outer_product_sum)
+
+
+def test_kgrouped_segment_shifted_by_one_is_caught(monkeypatch):
+    orig = op.token_offsets
+    monkeypatch.setattr(og, "token_offsets", lambda counts: [0] + [o + 1 for o in orig(counts)[1:]])
+    assert fails(tg.test_kgrouped_vs_outer_product_sum)
+
+
+def test_masked_extra_row_is_caught(monkeypatch):
+    orig = og.masked
+
+    def bad(A, B, valid_m):
+        return orig(A, B, [min(v + 1, A.shape[1]) if v else 0 for v in valid_m])
+    monkeypatch.setattr(og, "masked", bad)
+    assert fails(tg.test_masked_vs_triple_loop)
+
+
+def test_masked_wrong_expert_weights_are_caught(monkeypatch):
+    orig = og.masked
+    monkeypatch.setattr(og, "masked", lambda A, B, v: orig(A, np.roll(B, 1, axis=0), v))
+    assert fails(tg.test_masked_vs_triple_loop)
+
+
+def test_contiguous_dropped_expert_is_caught(monkeypatch):
+    orig = og.contiguous
+
+    def bad(A, B, counts, align_q):
+        c = list(counts)
+        c[-1] = 0
+        R, w = orig(A, B, c, align_q)
+        return R, w
+    monkeypatch.setattr(og, "contiguous", bad)
+    assert fails(tg.test_contiguous_vs_triple_loop, [3, 0, 5, 1], 4)
