@@ -74,6 +74,16 @@ def measured_traffic(workload, kind):
     return rec.get("bytes_per_step")
 
 
+def traffic_fields(workload, kind, alg_bytes_per_step, launches):
+    """The dominant kernel's ncu DRAM bytes beside its algorithmic bytes, per
+    launch (the step's launches averaged, like `achieved`) and per step;
+    traffic is None when no capture matches the current kernel sources."""
+    t = measured_traffic(workload, kind)
+    return {"traffic": None if t is None else t / launches, "traffic_per_step": t,
+            "algorithmic_bytes_per_launch": alg_bytes_per_step / launches,
+            "launches_per_step": launches}
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -294,15 +304,15 @@ class Contiguous:
         tensor_peak = peaks["bf16_tflops"] * (FP8_OVER_BF16 if self.fp8 else 1.0)
         t_compute = flops / (tensor_peak * 1e12)
         t_mem = byts / (peaks["hbm_gbs"] * 1e9)
+        tr = traffic_fields(self.name, "fwd", byts, len(self.gemms))
         if t_compute >= t_mem:
             ach = flops / (ms * 1e-3) / 1e12
             return {"bound": "tensor", "achieved": ach, "peak": tensor_peak, "unit": "TFLOP/s",
-                    "frac": ach / tensor_peak, "traffic": measured_traffic(self.name, "fwd"),
+                    "frac": ach / tensor_peak, **tr,
                     "peak_source": f"{peaks['source']} bf16 burst x{FP8_OVER_BF16 if self.fp8 else 1.0:g}"}
         ach = byts / (ms * 1e-3) / 1e9
         return {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": ach / peaks["hbm_gbs"], "traffic": measured_traffic(self.name, "fwd"),
-                "peak_source": f"{peaks['source']} copy"}
+                "frac": ach / peaks["hbm_gbs"], **tr, "peak_source": f"{peaks['source']} copy"}
 
     def config(self):
         d = {"workload": self.name, "form": "contiguous", "experts": self.E, "assignments": self.U,
@@ -414,7 +424,7 @@ class Masked:
         ms = sum(per_gemm_ms)
         ach = self.bytes_alg() / (ms * 1e-3) / 1e9
         return {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": ach / peaks["hbm_gbs"], "traffic": measured_traffic(self.name, "fwd"),
+                "frac": ach / peaks["hbm_gbs"], **traffic_fields(self.name, "fwd", self.bytes_alg(), 1),
                 "peak_source": f"{peaks['source']} copy"}
 
     def config(self):
@@ -487,10 +497,14 @@ class KGrouped:
         for d, h in self.h_out:
             h.copy_(d, non_blocking=True)
 
+    def bytes_alg(self):
+        """Valid dY and X rows read once, every expert's fp32 dW written once."""
+        return self.U * (self.N + self.K) * 2 + self.E * self.N * self.K * 4
+
     def roofline(self, per_gemm_ms, peaks):
         ach = self.flops() / (sum(per_gemm_ms) * 1e-3) / 1e12
         return {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": ach / peaks["bf16_tflops"], "traffic": measured_traffic(self.name, "kg"),
+                "frac": ach / peaks["bf16_tflops"], **traffic_fields(self.name, "kg", self.bytes_alg(), 1),
                 "peak_source": f"{peaks['source']} bf16 burst"}
 
     def config(self):

@@ -69,3 +69,59 @@ def test_exemplar_tuner_guardrail():
         for i, (shape, param) in enumerate(te.SHAPES):
             c = te.histogram(shape, param, 64, U, seed=2000 + 37 * i + U)
             assert len(c) == 64 and sum(c) == U and min(c) >= 0
+
+
+def _bare(cls, name, **attrs):
+    """A workload object with only what its roofline reads (no device)."""
+    w = object.__new__(cls)
+    spec = wl.WORKLOADS[name]
+    w.name = name
+    w.counts = spec["counts"]()
+    w.U = sum(w.counts)
+    for k, v in attrs.items():
+        setattr(w, k, v)
+    return w
+
+
+PEAKS = {"hbm_gbs": 6789.6, "bf16_tflops": 1869.1, "source": "measured"}
+
+
+@pytest.mark.parametrize("case", ["prefill", "masked", "kgrouped"])
+def test_roofline_traffic_is_per_launch(case):
+    """roofline.traffic is the ncu DRAM bytes of one launch (the step's
+    launches averaged) beside the algorithmic bytes of one launch; the
+    per-step figure and the launch count come with it."""
+    import json
+    import os
+    if case == "prefill":
+        name = "prefill_fp8_e64_t32768_n4096_k7168"
+        w = _bare(bench.Contiguous, name, fp8=True, w4=False, elem=1,
+                  gemms=[dict(N=4096, K=7168, swiglu=False), dict(N=7168, K=2048, swiglu=False)])
+        r, launches, kind = w.roofline([0.84, 0.48], PEAKS), 2, "fwd"
+    elif case == "masked":
+        name = "masked_fp8_e16_m256_n4096_k7168"
+        w = _bare(bench.Masked, name, fp8=True, w4=False, elem=1, E=16, M=256, N=4096, K=7168)
+        r, launches, kind = w.roofline([0.0927], PEAKS), 1, "fwd"
+    else:
+        name = "kgrouped_bf16_e32_t65536_n4096_k2048"
+        w = _bare(bench.KGrouped, name, fp8=False, E=32, N=4096, K=2048)
+        r, launches, kind = w.roofline([0.787], PEAKS), 1, "kg"
+        assert w.bytes_alg() == 65536 * (4096 + 2048) * 2 + 32 * 4096 * 2048 * 4
+    assert r["launches_per_step"] == launches
+    with open(os.path.join(bench.ROOT, "profiles", "dram_traffic.json")) as f:
+        rec = json.load(f)[name]
+    if rec["sources_sha256"] == bench.kernel_sources_sha(kind):
+        assert rec["launches"] == launches
+        assert r["traffic_per_step"] == rec["bytes_per_step"]
+        assert r["traffic"] == pytest.approx(rec["bytes_per_step"] / launches)
+        # operands come from DRAM about once: traffic within 20 % of the algorithmic bytes
+        assert 0.99 <= r["traffic"] / r["algorithmic_bytes_per_launch"] < 1.2
+    else:
+        assert r["traffic"] is None and r["traffic_per_step"] is None
+
+
+def test_traffic_is_null_once_kernel_sources_change(monkeypatch):
+    monkeypatch.setattr(bench, "kernel_sources_sha", lambda kind: "0" * 64)
+    f = bench.traffic_fields("prefill_fp8_e64_t32768_n4096_k7168", "fwd", 3.86e9, 2)
+    assert f["traffic"] is None and f["traffic_per_step"] is None
+    assert f["algorithmic_bytes_per_launch"] == pytest.approx(1.93e9)
