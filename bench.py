@@ -6,8 +6,19 @@ token-tile choice and the grouped GEMMs, all through the C ABI of
 libmoegemm.so.  The headline workload is the skewed FP8 prefill: 64 experts,
 32768 token-expert assignments drawn from a Zipf(1.2) law over a seeded
 expert permutation, GEMM1 N=4096 K=7168 then GEMM2 N=7168 K=2048, E4M3
-operands with UE8M0 per-128 block scales.  Other workloads (--workload) are
-parity cases that can be measured the same way.
+operands with UE8M0 per-128 block scales.
+
+Every other workload of the benchmark set is measured in the same run and
+reported under "configs": the 8-expert near-uniform example, the 32-expert
+issue histogram, the masked FP8 decode, the skewed prefill in FP8 and BF16,
+the K-grouped weight gradient, and the FP8 x FP4 decode and fused-SwiGLU FFN
+variants.  Each config record carries its effective and physical
+throughput, the padding accounting at the chosen tile, the roofline (the
+slower of the useful flops at the dense tensor peak and the algorithmic
+bytes at HBM bandwidth) and the CPU oracle timed on a bounded sample.
+
+Timing: L2 is flushed between timed repetitions by writing a buffer of twice
+the L2 size, outside the CUDA events that bracket each step.
 
 Metric: effective TFLOP/s, counting only valid token rows
 (2 * U * N * K per GEMM), the whole job over all ranks.
@@ -30,11 +41,30 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from moe_grouped_gemm_side_gb300 import binding as mb  # noqa: E402
 from moe_grouped_gemm_side_gb300 import workloads as wl  # noqa: E402
 
 HEADLINE = "prefill_fp8_e64_t32768_n4096_k7168"
+# the benchmark set reported under "configs", in order
+CONFIGS = [
+    "contig_bf16_e8_n256_k256",
+    "contig_bf16_e32_n4096_k2048",
+    "masked_fp8_e16_m256_n4096_k7168",
+    "prefill_fp8_e64_t32768_n4096_k7168",
+    "prefill_bf16_e64_t32768_n4096_k7168",
+    "kgrouped_bf16_e32_t65536_n4096_k2048",
+    "masked_fp8xfp4_e16_m256_n4096_k7168",
+    "prefill_ffn_fp8_e64_t32768_n4096_k7168",
+]
 FP8_OVER_BF16 = 2.0   # nominal dense fp8 : bf16 tensor throughput ratio
+METRIC = "effective TFLOPS (valid rows only)"
+L2_NOTE = "L2 flushed between timed reps: 2 x l2CacheSize bytes written outside the CUDA events"
+
+
+def _binding():
+    """The C-ABI binding; imported only by the GPU arm (the reference arm
+    loads no part of the library)."""
+    from moe_grouped_gemm_side_gb300 import binding
+    return binding
 
 
 # ------------------------------------------------------------------ helpers
@@ -96,11 +126,28 @@ def load_peaks():
             "source": "fallback"}
 
 
+def roofline_record(flops, byts, ms, tensor_peak, peaks, peak_label, tr):
+    """Roofline of one timed launch set: the bound is whichever of the useful
+    flops at the tensor peak and the algorithmic bytes at HBM bandwidth
+    takes longer; `achieved` and `frac` are in that bound's unit."""
+    t_compute = flops / (tensor_peak * 1e12)
+    t_mem = byts / (peaks["hbm_gbs"] * 1e9)
+    common = {"flops": flops, "algorithmic_bytes": byts, "t_compute_us": t_compute * 1e6,
+              "t_mem_us": t_mem * 1e6, **tr}
+    if t_compute >= t_mem:
+        ach = flops / (ms * 1e-3) / 1e12
+        return {"bound": "tensor", "achieved": ach, "peak": tensor_peak, "unit": "TFLOP/s",
+                "frac": ach / tensor_peak, **common, "peak_source": peak_label}
+    ach = byts / (ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": ach / peaks["hbm_gbs"], **common, "peak_source": f"{peaks['source']} copy"}
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle samples with host timestamps."""
     Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,utilization.gpu")
 
     def __init__(self, index):
         self.index = index
@@ -135,21 +182,27 @@ class ClockSampler:
             self.thread.join(timeout=5)
 
     def summary(self, t0, t1):
+        """Median SM clock over the samples of [t0, t1] taken under load
+        (utilisation >= 50 %; all samples of the window if none was), the
+        maximum clock, board power and every throttle reason seen."""
         def num(x):
             try:
                 return float(x)
             except ValueError:
                 return None
-        win = [s for (t, s) in self.samples if t0 - 0.3 <= t <= t1 + 0.3 and len(s) >= 8]
+        win = [s for (t, s) in self.samples if t0 - 0.3 <= t <= t1 + 0.3 and len(s) >= 9]
         if not win:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for s in win for i in range(4) if s[4 + i].lower() == "active"})
-        sm = [v for v in (num(s[0]) for s in win) if v is not None]
+        loaded = [s for s in win if (num(s[8]) or 0.0) >= 50.0]
+        use = loaded or win
+        sm = [v for v in (num(s[0]) for s in use) if v is not None]
         mx = [v for v in (num(s[1]) for s in win) if v is not None]
         pw = [v for v in (num(s[2]) for s in win) if v is not None]
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "power_w_max": max(pw) if pw else None, "reasons": reasons, "samples": len(win)}
+                "power_w_max": max(pw) if pw else None, "reasons": reasons, "samples": len(win),
+                "samples_under_load": len(loaded)}
 
 
 def dist_setup():
@@ -193,352 +246,10 @@ def weak_scaling_value(units_per_rank, ws, ms_max):
     return ws * units_per_rank / (ms_max * 1e-3)
 
 
-# ------------------------------------------------------------------ workloads
-class Contiguous:
-    """Plan + one or two contiguous grouped GEMMs over the same histogram."""
-
-    def __init__(self, name, dev):
-        spec = wl.WORKLOADS[name]
-        self.name, self.spec, self.dev = name, spec, dev
-        self.fp8 = spec["dtype"] in ("fp8", "fp8xfp4")
-        self.w4 = spec["dtype"] == "fp8xfp4"      # E2M1 weights, one scale per (row, 32 K)
-        self.counts = spec["counts"]()
-        self.E = spec["E"]
-        self.align = spec["align_q"]
-        offs, _, st, code = mb.plan_host(self.counts, self.align, max_tiles=0)
-        assert code == 0
-        self.U = st.U
-        self.rows_cap = (st.P + 15) // 16 * 16
-        shapes = [(spec["N"], spec["K"])]
-        if "second" in spec:
-            shapes.append((spec["second"]["N"], spec["second"]["K"]))
-        # swiglu: GEMM1's epilogue applies SwiGLU to interleaved gate/up blocks and
-        # re-quantises (E4M3 + UE8M0), and GEMM2 consumes that output (K = N1/2)
-        self.swiglu = bool(spec.get("swiglu", False))
-        self.gemms = []
-        for i, (N, K) in enumerate(shapes):
-            seed = spec["seed"] + 100 * i
-            ops = wl.make_contiguous(self.E, self.rows_cap, N, K, spec["dtype"], seed, dev,
-                                     spec["a_std"] if i == 0 else 1.0, spec["b_std"] if i == 0 else 1.0)
-            A, SFA = ops.A, ops.SFA
-            if self.swiglu and i == 1:
-                A, SFA = self.gemms[0]["D"], self.gemms[0]["SFD"]      # GEMM1's output
-            if self.swiglu and i == 0:
-                D = torch.empty((self.rows_cap, N // 2), dtype=torch.uint8, device=dev)
-                SFD = torch.empty((N // 256, self.rows_cap), dtype=torch.uint8, device=dev)
-            else:
-                D, SFD = torch.empty((self.rows_cap, N), dtype=torch.bfloat16, device=dev), None
-            self.gemms.append(dict(N=N, K=K, A=A, B=ops.B, SFA=SFA, SFB=ops.SFB, D=D, SFD=SFD,
-                                   swiglu=self.swiglu and i == 0))
-        self.d_counts = torch.tensor(self.counts, dtype=torch.int32, device=dev)
-        self.offsets = torch.empty(self.E + 1, dtype=torch.int64, device=dev)
-        self.stats = torch.empty(48, dtype=torch.uint8, device=dev)
-        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.dtype = mb.MG_FP8_X_FP4_E2M1 if self.w4 else (mb.MG_FP8_E4M3_UE8M0 if self.fp8 else mb.MG_BF16)
-        self.elem = 1 if self.fp8 else 2
-
-    def flops(self):
-        return sum(2.0 * self.U * g["N"] * g["K"] for g in self.gemms)
-
-    def bytes_alg(self, g):
-        """Algorithmic bytes of one GEMM: weights of active experts (+scales),
-        valid activation rows (+scales), valid output rows."""
-        act = sum(1 for t in self.counts if t > 0)
-        N, K = g["N"], g["K"]
-        out = self.U * (N // 2 + N // 256) if g["swiglu"] else self.U * N * 2   # E4M3 Y + scales, or bf16 D
-        w = act * (N * K // 2 + N * K // 32) if self.w4 else act * N * K * self.elem
-        b = w + self.U * K * self.elem + out
-        if self.fp8:
-            b += self.U * (K // 128) + (0 if self.w4 else act * (K // 128) * (N // 128))
-        return b
-
-    def launches_per_step(self):
-        return 1 + len(self.gemms)
-
-    def step(self, lib, stream, ev=None):
-        s = ctypes_stream(stream)
-        rc = lib.moe_plan(ptr(self.d_counts), self.E, self.align, ptr(self.offsets), None, 0,
-                          ptr(self.stats), ptr(self.status), s)
-        assert rc == 0, rc
-        for i, g in enumerate(self.gemms):
-            if ev is not None:
-                ev[i][0].record(stream)
-            if g["swiglu"]:
-                rc = lib.mgemm_contiguous_swiglu(self.dtype, mb.MG_SWIGLU_FP8_E4M3_UE8M0, ptr(g["A"]),
-                                                 ptr(g["SFA"]), ptr(g["B"]), ptr(g["SFB"]), ptr(g["D"]),
-                                                 ptr(g["SFD"]), ptr(self.d_counts), self.E, self.rows_cap,
-                                                 g["N"], g["K"], self.align, 0, ptr(self.status), s)
-            else:
-                rc = lib.mgemm_contiguous(self.dtype, ptr(g["A"]), ptr(g["SFA"]), ptr(g["B"]), ptr(g["SFB"]),
-                                          ptr(g["D"]), ptr(self.d_counts), self.E, self.rows_cap, g["N"], g["K"],
-                                          self.align, 0, ptr(self.status), s)
-            assert rc == 0, rc
-            if ev is not None:
-                ev[i][1].record(stream)
-
-    # end-to-end: inputs from pinned host memory, outputs back to pinned host
-    def e2e_setup(self):
-        self.h_in = [(self.d_counts, self.d_counts.cpu().pin_memory())]
-        for i, g in enumerate(self.gemms):
-            if self.swiglu and i == 1:
-                continue                      # produced on the device by GEMM1
-            for k in ("A", "SFA"):
-                if g[k] is not None:
-                    self.h_in.append((g[k], g[k].cpu().pin_memory()))
-        outs = [self.gemms[-1]] if self.swiglu else self.gemms
-        self.h_out = [(g["D"], torch.empty(g["D"].shape, dtype=g["D"].dtype).pin_memory()) for g in outs]
-        return (sum(h.numel() * h.element_size() for _, h in self.h_in),
-                sum(h.numel() * h.element_size() for _, h in self.h_out))
-
-    def e2e_step(self, lib, stream):
-        for d, h in self.h_in:
-            d.copy_(h, non_blocking=True)
-        self.step(lib, stream)
-        for d, h in self.h_out:
-            h.copy_(d, non_blocking=True)
-
-    def roofline(self, per_gemm_ms, peaks):
-        flops = sum(2.0 * self.U * g["N"] * g["K"] for g in self.gemms)
-        ms = sum(per_gemm_ms)
-        byts = sum(self.bytes_alg(g) for g in self.gemms)
-        tensor_peak = peaks["bf16_tflops"] * (FP8_OVER_BF16 if self.fp8 else 1.0)
-        t_compute = flops / (tensor_peak * 1e12)
-        t_mem = byts / (peaks["hbm_gbs"] * 1e9)
-        tr = traffic_fields(self.name, "fwd", byts, len(self.gemms))
-        if t_compute >= t_mem:
-            ach = flops / (ms * 1e-3) / 1e12
-            return {"bound": "tensor", "achieved": ach, "peak": tensor_peak, "unit": "TFLOP/s",
-                    "frac": ach / tensor_peak, **tr,
-                    "peak_source": f"{peaks['source']} bf16 burst x{FP8_OVER_BF16 if self.fp8 else 1.0:g}"}
-        ach = byts / (ms * 1e-3) / 1e9
-        return {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": ach / peaks["hbm_gbs"], **tr, "peak_source": f"{peaks['source']} copy"}
-
-    def config(self):
-        d = {"workload": self.name, "form": "contiguous", "experts": self.E, "assignments": self.U,
-             "align_q": self.align, "rows_cap": self.rows_cap, "tile_q": "device-selected",
-             "gemms": [f"N={g['N']},K={g['K']}" for g in self.gemms],
-             "operands": operands_label(self.fp8, self.w4),
-             "l2": "inputs larger than L2 (no flush)"}
-        if self.swiglu:
-            d["epilogue"] = "GEMM1: SwiGLU of interleaved gate/up blocks, re-quantised to e4m3 + ue8m0; feeds GEMM2"
-        return d
-
-    # ---- CPU oracle on a bounded sample (experts given by index)
-    def oracle_sample(self, experts):
-        from oracle import gemm as og
-        from oracle import numerics as on
-        from oracle import plan as op
-        from oracle import epilogue as oe
-        host = []
-        for g in self.gemms:
-            host.append({k: (g[k].cpu() if g[k] is not None else None) for k in ("A", "SFA")})
-        t0 = time.perf_counter()
-        p = op.plan(self.counts, self.align)
-        useful = 0.0
-        for e in experts:
-            t = self.counts[e]
-            if t == 0:
-                continue
-            o = p.offsets[e]
-            prev = None
-            for g, h in zip(self.gemms, host):
-                if prev is not None:
-                    a = prev                    # GEMM2 reads GEMM1's re-quantised SwiGLU output
-                elif self.fp8:
-                    a = on.dequant_rows(h["A"][o:o + t].numpy(), h["SFA"][:, o:o + t].numpy())
-                else:
-                    a = on.decode_bf16(h["A"][o:o + t].view(torch.int16).numpy().view(np.uint16))
-                if self.fp8:
-                    deq_w = on.dequant_weight_mx4 if self.w4 else on.dequant_weight
-                    b = deq_w(g["B"][e].cpu().numpy(), g["SFB"][e].cpu().numpy())
-                else:
-                    b = on.decode_bf16(g["B"][e].cpu().view(torch.int16).numpy().view(np.uint16))
-                r = og.expert_product(a, b)
-                if g["swiglu"]:
-                    codes, sf = oe.quantize_blocks(oe.swiglu(*oe.gate_up_halves(r)))
-                    prev = on.dequant_rows(codes, sf)
-                useful += 2.0 * t * g["N"] * g["K"]
-        return useful, time.perf_counter() - t0
-
-
-class Masked:
-    def __init__(self, name, dev):
-        spec = wl.WORKLOADS[name]
-        self.name, self.spec = name, spec
-        self.fp8 = spec["dtype"] in ("fp8", "fp8xfp4")
-        self.w4 = spec["dtype"] == "fp8xfp4"      # E2M1 weights, one scale per (row, 32 K)
-        self.E, self.M, self.N, self.K = spec["E"], spec["M_max"], spec["N"], spec["K"]
-        self.counts = spec["counts"]()
-        self.U = sum(self.counts)
-        ops = wl.make_masked(self.E, self.M, self.N, self.K, spec["dtype"], spec["seed"], dev)
-        self.A, self.B, self.SFA, self.SFB = ops.A, ops.B, ops.SFA, ops.SFB
-        self.D = torch.empty((self.E, self.M, self.N), dtype=torch.bfloat16, device=dev)
-        self.d_counts = torch.tensor(self.counts, dtype=torch.int32, device=dev)
-        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.dtype = mb.MG_FP8_X_FP4_E2M1 if self.w4 else (mb.MG_FP8_E4M3_UE8M0 if self.fp8 else mb.MG_BF16)
-        self.elem = 1 if self.fp8 else 2
-        self.gemms = [dict(N=self.N, K=self.K)]
-
-    def flops(self):
-        return 2.0 * self.U * self.N * self.K
-
-    def launches_per_step(self):
-        return 1
-
-    def bytes_alg(self):
-        act = sum(1 for t in self.counts if t > 0)
-        N, K = self.N, self.K
-        w = act * (N * K // 2 + N * K // 32) if self.w4 else act * N * K * self.elem
-        b = w + self.U * K * self.elem + self.U * N * 2
-        if self.fp8:
-            b += self.U * (K // 128) + (0 if self.w4 else act * (K // 128) * (N // 128))
-        return b
-
-    def step(self, lib, stream, ev=None):
-        if ev is not None:
-            ev[0][0].record(stream)
-        rc = lib.mgemm_masked(self.dtype, ptr(self.A), ptr(self.SFA), ptr(self.B), ptr(self.SFB), ptr(self.D),
-                              ptr(self.d_counts), self.E, self.M, self.N, self.K, ptr(self.status),
-                              ctypes_stream(stream))
-        assert rc == 0, rc
-        if ev is not None:
-            ev[0][1].record(stream)
-
-    def e2e_setup(self):
-        self.h_in = [(self.d_counts, self.d_counts.cpu().pin_memory()), (self.A, self.A.cpu().pin_memory())]
-        if self.SFA is not None:
-            self.h_in.append((self.SFA, self.SFA.cpu().pin_memory()))
-        self.h_out = [(self.D, torch.empty(self.D.shape, dtype=self.D.dtype).pin_memory())]
-        return (sum(h.numel() * h.element_size() for _, h in self.h_in),
-                sum(h.numel() * h.element_size() for _, h in self.h_out))
-
-    def e2e_step(self, lib, stream):
-        for d, h in self.h_in:
-            d.copy_(h, non_blocking=True)
-        self.step(lib, stream)
-        for d, h in self.h_out:
-            h.copy_(d, non_blocking=True)
-
-    def roofline(self, per_gemm_ms, peaks):
-        ms = sum(per_gemm_ms)
-        ach = self.bytes_alg() / (ms * 1e-3) / 1e9
-        return {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": ach / peaks["hbm_gbs"], **traffic_fields(self.name, "fwd", self.bytes_alg(), 1),
-                "peak_source": f"{peaks['source']} copy"}
-
-    def config(self):
-        return {"workload": self.name, "form": "masked", "experts": self.E, "M_max": self.M,
-                "valid_rows": self.U, "N": self.N, "K": self.K,
-                "operands": operands_label(self.fp8, self.w4),
-                "l2": "inputs larger than L2 (no flush)"}
-
-    def oracle_sample(self, experts):
-        from oracle import gemm as og
-        from oracle import numerics as on
-        t0 = time.perf_counter()
-        useful = 0.0
-        for e in experts:
-            v = self.counts[e]
-            if v == 0:
-                continue
-            if self.fp8:
-                a = on.dequant_rows(self.A[e, :v].cpu().numpy(), self.SFA[e][:, :v].cpu().numpy())
-                deq_w = on.dequant_weight_mx4 if self.w4 else on.dequant_weight
-                b = deq_w(self.B[e].cpu().numpy(), self.SFB[e].cpu().numpy())
-            else:
-                a = on.decode_bf16(self.A[e, :v].cpu().view(torch.int16).numpy().view(np.uint16))
-                b = on.decode_bf16(self.B[e].cpu().view(torch.int16).numpy().view(np.uint16))
-            og.expert_product(a, b)
-            useful += 2.0 * v * self.N * self.K
-        return useful, time.perf_counter() - t0
-
-
-class KGrouped:
-    def __init__(self, name, dev):
-        spec = wl.WORKLOADS[name]
-        self.name = name
-        self.E, self.N, self.K, self.T = spec["E"], spec["N"], spec["K"], spec["T"]
-        self.counts = spec["counts"]()
-        self.U = sum(self.counts)
-        self.dY, self.X = wl.make_kgrouped(self.T, self.N, self.K, spec["seed"], dev)
-        self.dW = torch.empty((self.E, self.N, self.K), dtype=torch.float32, device=dev)
-        self.d_counts = torch.tensor(self.counts, dtype=torch.int32, device=dev)
-        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.fp8 = False
-        self.gemms = [dict(N=self.N, K=self.K)]
-
-    def flops(self):
-        return 2.0 * self.U * self.N * self.K
-
-    def launches_per_step(self):
-        return 1
-
-    def step(self, lib, stream, ev=None):
-        if ev is not None:
-            ev[0][0].record(stream)
-        rc = lib.kgemm_grouped(ptr(self.dY), ptr(self.X), ptr(self.dW), ptr(self.d_counts), self.E, self.T,
-                               self.N, self.K, ptr(self.status), ctypes_stream(stream))
-        assert rc == 0, rc
-        if ev is not None:
-            ev[0][1].record(stream)
-
-    def e2e_setup(self):
-        self.h_in = [(self.d_counts, self.d_counts.cpu().pin_memory()), (self.dY, self.dY.cpu().pin_memory()),
-                     (self.X, self.X.cpu().pin_memory())]
-        self.h_out = [(self.dW, torch.empty(self.dW.shape, dtype=self.dW.dtype).pin_memory())]
-        return (sum(h.numel() * h.element_size() for _, h in self.h_in),
-                sum(h.numel() * h.element_size() for _, h in self.h_out))
-
-    def e2e_step(self, lib, stream):
-        for d, h in self.h_in:
-            d.copy_(h, non_blocking=True)
-        self.step(lib, stream)
-        for d, h in self.h_out:
-            h.copy_(d, non_blocking=True)
-
-    def bytes_alg(self):
-        """Valid dY and X rows read once, every expert's fp32 dW written once."""
-        return self.U * (self.N + self.K) * 2 + self.E * self.N * self.K * 4
-
-    def roofline(self, per_gemm_ms, peaks):
-        ach = self.flops() / (sum(per_gemm_ms) * 1e-3) / 1e12
-        return {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": ach / peaks["bf16_tflops"], **traffic_fields(self.name, "kg", self.bytes_alg(), 1),
-                "peak_source": f"{peaks['source']} bf16 burst"}
-
-    def config(self):
-        return {"workload": self.name, "form": "kgrouped", "experts": self.E, "tokens": self.U,
-                "N": self.N, "K": self.K, "operands": "bf16 in, fp32 dW",
-                "l2": "inputs larger than L2 (no flush)"}
-
-    def oracle_sample(self, experts):
-        from oracle import gemm as og
-        from oracle import numerics as on
-        off = np.concatenate([[0], np.cumsum(self.counts)])
-        t0 = time.perf_counter()
-        useful = 0.0
-        for e in experts:
-            a, b = int(off[e]), int(off[e + 1])
-            if b == a:
-                continue
-            cnt = [0] * self.E
-            cnt[e] = b - a
-            dy = on.decode_bf16(self.dY[a:b].cpu().view(torch.int16).numpy().view(np.uint16))
-            x = on.decode_bf16(self.X[a:b].cpu().view(torch.int16).numpy().view(np.uint16))
-            og.kgrouped(dy, x, [b - a])
-            useful += 2.0 * (b - a) * self.N * self.K
-        return useful, time.perf_counter() - t0
-
-
-def make_workload(name, dev):
-    form = wl.WORKLOADS[name]["form"]
-    return {"contiguous": Contiguous, "masked": Masked, "kgrouped": KGrouped}[form](name, dev)
-
-
-def ctypes_stream(stream):
-    import ctypes
-    return ctypes.c_void_p(stream.cuda_stream)
+def operands_label(fp8, w4):
+    if w4:
+        return "e4m3 + ue8m0 per (row, 128 K) x e2m1 weights + ue8m0 per (row, 32 K)"
+    return "e4m3 + ue8m0 per-128 scales" if fp8 else "bf16"
 
 
 def blas_threads():
@@ -552,11 +263,334 @@ def blas_threads():
     return len(os.sched_getaffinity(0))
 
 
-def tactic_report(dtype, counts, N, K, ms):
+# ------------------------------------------------------------------ workloads
+class Workload:
+    """What a workload is (histogram, shapes, dtype), independent of where its
+    operands live.  `attach_gpu` builds the device operands for the library;
+    `attach_cpu` makes the host copies the oracle reads, drawn lazily per
+    expert.  `oracle_sample` times the oracle on some experts either way."""
+
+    def __init__(self, name):
+        spec = wl.WORKLOADS[name]
+        self.name, self.spec = name, spec
+        self.form = spec["form"]
+        self.dtype_name = spec["dtype"]
+        self.fp8 = spec["dtype"] in ("fp8", "fp8xfp4")
+        self.w4 = spec["dtype"] == "fp8xfp4"
+        self.elem = 1 if self.fp8 else 2
+        self.counts = spec["counts"]()
+        self.E = spec["E"]
+        self.U = sum(self.counts)
+        self.active = sum(1 for t in self.counts if t > 0)
+        self.swiglu = bool(spec.get("swiglu", False))
+        shapes = [(spec["N"], spec["K"])]
+        if "second" in spec:
+            shapes.append((spec["second"]["N"], spec["second"]["K"]))
+        self.gemms = [dict(N=N, K=K, swiglu=self.swiglu and i == 0) for i, (N, K) in enumerate(shapes)]
+        self.host = None
+
+    # ---- pure accounting
+    def flops(self):
+        return sum(2.0 * self.U * g["N"] * g["K"] for g in self.gemms)
+
+    def bytes_alg(self, g):
+        """Algorithmic bytes of one GEMM: weights (and scales) of active
+        experts, valid activation rows (and scales), valid output rows."""
+        N, K = g["N"], g["K"]
+        if self.form == "kgrouped":
+            return self.U * (N + K) * 2 + self.E * N * K * 4
+        act = self.active
+        out = self.U * (N // 2 + N // 256) if g["swiglu"] else self.U * N * 2   # E4M3 Y + scales, or bf16 D
+        w = act * (N * K // 2 + N * K // 32) if self.w4 else act * N * K * self.elem
+        b = w + self.U * K * self.elem + out
+        if self.fp8:
+            b += self.U * (K // 128) + (0 if self.w4 else act * (K // 128) * (N // 128))
+        return b
+
+    def bytes_alg_total(self):
+        return sum(self.bytes_alg(g) for g in self.gemms)
+
+    def launches_per_step(self):
+        return (1 if self.form == "contiguous" else 0) + len(self.gemms)
+
+    def tensor_peak(self, peaks):
+        return peaks["bf16_tflops"] * (FP8_OVER_BF16 if self.fp8 else 1.0)
+
+    def roofline(self, per_gemm_ms, peaks):
+        kind = "kg" if self.form == "kgrouped" else "fwd"
+        byts = self.bytes_alg_total()
+        tr = traffic_fields(self.name, kind, byts, len(self.gemms))
+        label = f"{peaks['source']} bf16 burst x{FP8_OVER_BF16 if self.fp8 else 1.0:g}"
+        return roofline_record(self.flops(), byts, sum(per_gemm_ms), self.tensor_peak(peaks), peaks, label, tr)
+
+    def config(self):
+        """The workload's description; identical in both arms."""
+        d = {"workload": self.name, "form": self.form, "experts": self.E,
+             "operands": operands_label(self.fp8, self.w4) if self.form != "kgrouped" else "bf16 in, fp32 dW",
+             "l2": L2_NOTE}
+        if self.form == "contiguous":
+            d.update(assignments=self.U, align_q=self.spec["align_q"], tile_q="device-selected",
+                     gemms=[f"N={g['N']},K={g['K']}" for g in self.gemms])
+        elif self.form == "masked":
+            d.update(M_max=self.spec["M_max"], valid_rows=self.U, N=self.spec["N"], K=self.spec["K"],
+                     tile_q="device-selected")
+        else:
+            d.update(tokens=self.U, N=self.spec["N"], K=self.spec["K"])
+        if self.swiglu:
+            d["epilogue"] = "GEMM1: SwiGLU of interleaved gate/up blocks, re-quantised to e4m3 + ue8m0; feeds GEMM2"
+        return d
+
+    # ---- device operands (GPU arm)
+    def attach_gpu(self, mb, dev):
+        self.mb = mb
+        spec = self.spec
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.d_counts = torch.tensor(self.counts, dtype=torch.int32, device=dev)
+        self.dtype = (mb.MG_FP8_X_FP4_E2M1 if self.w4 else mb.MG_FP8_E4M3_UE8M0) if self.fp8 else mb.MG_BF16
+        if self.form == "contiguous":
+            self.align = spec["align_q"]
+            _, _, st, code = mb.plan_host(self.counts, self.align, max_tiles=0)
+            assert code == 0
+            self.rows_cap = (st.P + 15) // 16 * 16
+            for i, g in enumerate(self.gemms):
+                seed = spec["seed"] + 100 * i
+                ops = wl.make_contiguous(self.E, self.rows_cap, g["N"], g["K"], spec["dtype"], seed, dev,
+                                         spec["a_std"] if i == 0 else 1.0, spec["b_std"] if i == 0 else 1.0)
+                A, SFA = ops.A, ops.SFA
+                if self.swiglu and i == 1:
+                    A, SFA = self.gemms[0]["D"], self.gemms[0]["SFD"]      # GEMM1's output
+                if g["swiglu"]:
+                    D = torch.empty((self.rows_cap, g["N"] // 2), dtype=torch.uint8, device=dev)
+                    SFD = torch.empty((g["N"] // 256, self.rows_cap), dtype=torch.uint8, device=dev)
+                else:
+                    D, SFD = torch.empty((self.rows_cap, g["N"]), dtype=torch.bfloat16, device=dev), None
+                g.update(A=A, B=ops.B, SFA=SFA, SFB=ops.SFB, D=D, SFD=SFD)
+            self.offsets = torch.empty(self.E + 1, dtype=torch.int64, device=dev)
+            self.stats = torch.empty(48, dtype=torch.uint8, device=dev)
+        elif self.form == "masked":
+            M, N, K = spec["M_max"], spec["N"], spec["K"]
+            ops = wl.make_masked(self.E, M, N, K, spec["dtype"], spec["seed"], dev)
+            self.gemms[0].update(A=ops.A, B=ops.B, SFA=ops.SFA, SFB=ops.SFB,
+                                 D=torch.empty((self.E, M, N), dtype=torch.bfloat16, device=dev))
+        else:
+            N, K, T = spec["N"], spec["K"], spec["T"]
+            dY, X = wl.make_kgrouped(T, N, K, spec["seed"], dev)
+            self.gemms[0].update(dY=dY, X=X, dW=torch.empty((self.E, N, K), dtype=torch.float32, device=dev))
+        return self
+
+    def step(self, lib, stream, ev=None):
+        """One pass: (contiguous) the device plan, then each GEMM; ev[i] =
+        (start, end) events around GEMM i."""
+        import ctypes
+        s = ctypes.c_void_p(stream.cuda_stream)
+        mb = self.mb
+        if self.form == "contiguous":
+            rc = lib.moe_plan(ptr(self.d_counts), self.E, self.align, ptr(self.offsets), None, 0,
+                              ptr(self.stats), ptr(self.status), s)
+            assert rc == 0, rc
+        for i, g in enumerate(self.gemms):
+            if ev is not None:
+                ev[i][0].record(stream)
+            if self.form == "kgrouped":
+                rc = lib.kgemm_grouped(ptr(g["dY"]), ptr(g["X"]), ptr(g["dW"]), ptr(self.d_counts), self.E,
+                                       self.spec["T"], g["N"], g["K"], ptr(self.status), s)
+            elif self.form == "masked":
+                rc = lib.mgemm_masked(self.dtype, ptr(g["A"]), ptr(g["SFA"]), ptr(g["B"]), ptr(g["SFB"]),
+                                      ptr(g["D"]), ptr(self.d_counts), self.E, self.spec["M_max"], g["N"], g["K"],
+                                      ptr(self.status), s)
+            elif g["swiglu"]:
+                rc = lib.mgemm_contiguous_swiglu(self.dtype, mb.MG_SWIGLU_FP8_E4M3_UE8M0, ptr(g["A"]),
+                                                 ptr(g["SFA"]), ptr(g["B"]), ptr(g["SFB"]), ptr(g["D"]),
+                                                 ptr(g["SFD"]), ptr(self.d_counts), self.E, self.rows_cap,
+                                                 g["N"], g["K"], self.align, 0, ptr(self.status), s)
+            else:
+                rc = lib.mgemm_contiguous(self.dtype, ptr(g["A"]), ptr(g["SFA"]), ptr(g["B"]), ptr(g["SFB"]),
+                                          ptr(g["D"]), ptr(self.d_counts), self.E, self.rows_cap, g["N"], g["K"],
+                                          self.align, 0, ptr(self.status), s)
+            assert rc == 0, rc
+            if ev is not None:
+                ev[i][1].record(stream)
+
+    def check_status(self):
+        code = int(self.status.item())
+        if code != 0:
+            raise RuntimeError(f"{self.name}: device status " + self.mb.status_str(code))
+
+    # end-to-end: inputs from pinned host memory, outputs back to pinned host
+    def e2e_setup(self):
+        self.h_in = [(self.d_counts, self.d_counts.cpu().pin_memory())]
+        keys = ("dY", "X") if self.form == "kgrouped" else ("A", "SFA")
+        for i, g in enumerate(self.gemms):
+            if self.swiglu and i == 1:
+                continue                      # produced on the device by GEMM1
+            for k in keys:
+                if g.get(k) is not None:
+                    self.h_in.append((g[k], g[k].cpu().pin_memory()))
+        out_key = "dW" if self.form == "kgrouped" else "D"
+        outs = [self.gemms[-1]] if self.swiglu else self.gemms
+        self.h_out = [(g[out_key], torch.empty(g[out_key].shape, dtype=g[out_key].dtype).pin_memory())
+                      for g in outs]
+        return (sum(h.numel() * h.element_size() for _, h in self.h_in),
+                sum(h.numel() * h.element_size() for _, h in self.h_out))
+
+    def e2e_step(self, lib, stream):
+        for d, h in self.h_in:
+            d.copy_(h, non_blocking=True)
+        self.step(lib, stream)
+        for d, h in self.h_out:
+            h.copy_(d, non_blocking=True)
+
+    def tactics(self, per_gemm_ms):
+        if self.form == "kgrouped":
+            return None
+        return [tactic_report(self.mb, self.dtype, self.counts, g["N"], g["K"], t)
+                for g, t in zip(self.gemms, per_gemm_ms)]
+
+    # ---- host operands for the oracle
+    def attach_cpu(self):
+        """Host operands drawn with the workload's own seeded generators on
+        the CPU: activations whole, weights one expert at a time on first
+        use.  (Draws on the CPU and on the GPU follow the same recipe but not
+        the same random stream.)"""
+        from oracle import plan as op
+        spec = self.spec
+        self.host = {"w": {}}
+        if self.form == "contiguous":
+            rows_cap = (op.plan(self.counts, spec["align_q"]).P + 15) // 16 * 16
+            self.host["rows"] = []
+            for i, g in enumerate(self.gemms):
+                if self.swiglu and i == 1:
+                    self.host["rows"].append(None)       # GEMM1's output, made by the oracle
+                    continue
+                A, SFA = wl.make_rows(rows_cap, g["K"], "bf16" if not self.fp8 else "fp8",
+                                      spec["seed"] + 100 * i, "cpu", spec["a_std"] if i == 0 else 1.0)
+                self.host["rows"].append((A, SFA))
+        elif self.form == "masked":
+            M, K = spec["M_max"], spec["K"]
+            A2, SFA2 = wl.make_rows(self.E * M, K, "fp8" if self.fp8 else "bf16", spec["seed"], "cpu")
+            SFA = None if SFA2 is None else SFA2.reshape(K // 128, self.E, M).permute(1, 0, 2).contiguous()
+            self.host["rows"] = [(A2.reshape(self.E, M, K), SFA)]
+        else:
+            self.host["rows"] = [wl.make_kgrouped(spec["T"], spec["N"], spec["K"], spec["seed"], "cpu")]
+        return self
+
+    def _host_weight(self, i, e):
+        key = (i, e)
+        if key not in self.host["w"]:
+            g, spec = self.gemms[i], self.spec
+            seed = (spec["seed"] + 100 * i if self.form == "contiguous" else spec["seed"]) + 1
+            std = spec.get("b_std", 1.0) if i == 0 else 1.0
+            self.host["w"][key] = wl.expert_weight(e, g["N"], g["K"], self.dtype_name, seed, "cpu", std)
+        return self.host["w"][key]
+
+    def _rows(self, i, e, lo, hi):
+        """Activation rows [lo, hi) of GEMM i (expert e for the masked form)
+        and their scale columns, on the host."""
+        if self.host is not None:
+            A, SFA = self.host["rows"][i]
+        else:
+            g = self.gemms[i]
+            A, SFA = g["A"], g["SFA"]
+        if self.form == "masked":
+            a = A[e, lo:hi]
+            sf = None if SFA is None else SFA[e][:, lo:hi]
+        else:
+            a = A[lo:hi]
+            sf = None if SFA is None else SFA[:, lo:hi]
+        return a.cpu(), (None if sf is None else sf.cpu())
+
+    def _weight(self, i, e):
+        if self.host is not None:
+            return self._host_weight(i, e)
+        g = self.gemms[i]
+        return g["B"][e].cpu(), (None if g["SFB"] is None else g["SFB"][e].cpu())
+
+    def oracle_sample(self, experts):
+        """The oracle (plan + fp64 dequantisation + per-expert GEMMs) on the
+        given experts; returns (useful flops, seconds).  Operand copies to
+        the host are made before the clock starts."""
+        from oracle import epilogue as oe
+        from oracle import gemm as og
+        from oracle import numerics as on
+        from oracle import plan as op
+        if self.form == "kgrouped":
+            return self._oracle_sample_kg(experts)
+        align = self.spec.get("align_q", 1)
+        offs = op.plan(self.counts, align).offsets if self.form == "contiguous" else None
+        # host copies first (not timed)
+        staged = []
+        for e in experts:
+            t = self.counts[e]
+            if t == 0:
+                continue
+            lo = offs[e] if offs is not None else 0
+            per = []
+            for i in range(len(self.gemms)):
+                rows = None if (self.swiglu and i == 1) else self._rows(i, e, lo, lo + t)
+                per.append((rows, self._weight(i, e)))
+            staged.append((e, t, per))
+        t0 = time.perf_counter()
+        if self.form == "contiguous":
+            op.plan(self.counts, align)
+        useful = 0.0
+        for e, t, per in staged:
+            prev = None
+            for g, (rows, (b, sfb)) in zip(self.gemms, per):
+                if prev is not None:
+                    a = prev                    # GEMM2 reads GEMM1's re-quantised SwiGLU output
+                elif self.fp8:
+                    a = on.dequant_rows(rows[0].numpy(), rows[1].numpy())
+                else:
+                    a = on.decode_bf16(rows[0].view(torch.int16).numpy().view(np.uint16))
+                if self.fp8:
+                    deq_w = on.dequant_weight_mx4 if self.w4 else on.dequant_weight
+                    bw = deq_w(b.numpy(), sfb.numpy())
+                else:
+                    bw = on.decode_bf16(b.view(torch.int16).numpy().view(np.uint16))
+                r = og.expert_product(a, bw)
+                if g["swiglu"]:
+                    codes, sf = oe.quantize_blocks(oe.swiglu(*oe.gate_up_halves(r)))
+                    prev = on.dequant_rows(codes, sf)
+                useful += 2.0 * t * g["N"] * g["K"]
+        return useful, time.perf_counter() - t0
+
+    def _oracle_sample_kg(self, experts):
+        from oracle import gemm as og
+        from oracle import numerics as on
+        off = np.concatenate([[0], np.cumsum(self.counts)])
+        if self.host is not None:
+            dY, X = self.host["rows"][0]
+        else:
+            dY, X = self.gemms[0]["dY"], self.gemms[0]["X"]
+        staged = []
+        for e in experts:
+            a, b = int(off[e]), int(off[e + 1])
+            if b > a:
+                staged.append((dY[a:b].cpu(), X[a:b].cpu()))
+        t0 = time.perf_counter()
+        useful = 0.0
+        for dy, x in staged:
+            n = dy.shape[0]
+            og.kgrouped(on.decode_bf16(dy.view(torch.int16).numpy().view(np.uint16)),
+                        on.decode_bf16(x.view(torch.int16).numpy().view(np.uint16)), [n])
+            useful += 2.0 * n * self.spec["N"] * self.spec["K"]
+        return useful, time.perf_counter() - t0
+
+    def sample_steps(self):
+        if self.swiglu:
+            return "plan + fp64 dequantise + per-expert GEMM1, SwiGLU, E4M3 re-quantisation, GEMM2"
+        if self.form == "kgrouped":
+            return "fp64 decode + per-expert dY^T X"
+        return "plan + fp64 dequantise + per-expert GEMMs" if self.form == "contiguous" else \
+            "fp64 dequantise + per-expert GEMMs"
+
+
+def tactic_report(mb, dtype, counts, N, K, ms):
     """The token tile the kernel picks on the device for this histogram (the
     same pricing on the host), the pages' padded rows P at that tile, the rows
     the kernel actually computes (each expert's last tile trimmed to a
-    multiple of 16) and the physical throughput they imply."""
+    multiple of 16) and the physical throughput they imply: the pages'
+    (2 P N K / t) and the computed rows' (2 R N K / t)."""
     q = mb.select_tile_host(dtype, counts, N, K, 0)
     offs, _, st, code = mb.plan_host(counts, q, max_tiles=0)
     assert code == 0
@@ -567,19 +601,8 @@ def tactic_report(dtype, counts, N, K, ms):
             computed += full * q + (-(-last // 16) * 16 if last else 0)
     return {"N": N, "K": K, "tile_q": q, "P_at_tile": st.P, "U": st.U, "pad_frac_at_tile": st.pad_frac,
             "rows_computed": computed, "active_experts": st.active, "effective_experts": st.eff_experts,
-            "physical_tflops": 2.0 * computed * N * K / (ms * 1e-3) / 1e12}
-
-
-def operands_label(fp8, w4):
-    if w4:
-        return "e4m3 + ue8m0 per (row, 128 K) x e2m1 weights + ue8m0 per (row, 32 K)"
-    return "e4m3 + ue8m0 per-128 scales" if fp8 else "bf16"
-
-
-def sample_steps(w):
-    if getattr(w, "swiglu", False):
-        return "plan + fp64 dequantise + per-expert GEMM1, SwiGLU, E4M3 re-quantisation, GEMM2"
-    return "plan + fp64 dequantise + per-expert GEMMs"
+            "physical_tflops": 2.0 * st.P * N * K / (ms * 1e-3) / 1e12,
+            "computed_rows_tflops": 2.0 * computed * N * K / (ms * 1e-3) / 1e12}
 
 
 def oracle_sample_bounded(w, budget_s):
@@ -599,49 +622,114 @@ def oracle_sample_bounded(w, budget_s):
     return experts, useful, secs
 
 
+def cpu_baseline(w, budget_s):
+    experts, useful, secs = oracle_sample_bounded(w, budget_s)
+    return {"value": useful / secs / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"experts {experts} of {w.name}: {w.sample_steps()}, "
+                      f"{useful / 1e9:.2f} useful GFLOP in {secs:.2f} s"}
+
+
+class L2Flush:
+    """Writes 2 x l2CacheSize bytes between timed repetitions, so every rep
+    reads its operands from HBM."""
+
+    def __init__(self, dev):
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        self.bytes = 2 * int(l2)
+        self.buf = torch.empty(self.bytes, dtype=torch.uint8, device=dev)
+
+    def __call__(self):
+        self.buf.fill_(1)
+
+
+def timed_reps(w, lib, stream, flush, reps):
+    """`reps` steps, each after an L2 flush, each GEMM bracketed by CUDA
+    events; returns per-rep lists of per-GEMM milliseconds."""
+    n_g = len(w.gemms)
+    evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(n_g)]
+           for _ in range(reps)]
+    for i in range(reps):
+        flush()
+        w.step(lib, stream, evs[i])
+    torch.cuda.synchronize()
+    return [[evs[i][g][0].elapsed_time(evs[i][g][1]) for g in range(n_g)] for i in range(reps)]
+
+
+def config_record(w, lib, stream, flush, peaks, args, cpu=None):
+    """One entry of "configs": warm-up, then the median of `reps` L2-flushed
+    steps (each GEMM between its own events), with the roofline, the tactic
+    and padding accounting, and the oracle's CPU baseline."""
+    for _ in range(5):
+        flush()
+        w.step(lib, stream)
+    torch.cuda.synchronize()
+    w.check_status()
+    per_rep = timed_reps(w, lib, stream, flush, args.reps)
+    w.check_status()
+    tot = [sum(r) for r in per_rep]
+    med_i = sorted(range(len(tot)), key=lambda i: tot[i])[len(tot) // 2]
+    per_gemm = per_rep[med_i]
+    ms = tot[med_i]
+    tac = w.tactics(per_gemm)
+    rec = {"value": w.flops() / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
+           "ms_mean": sum(tot) / len(tot), "ms_min": min(tot), "reps": args.reps,
+           "per_gemm_ms": per_gemm, "useful_flops": w.flops(), "U": w.U,
+           "active_experts": w.active, "config": w.config(), "l2": L2_NOTE,
+           "roofline": w.roofline(per_gemm, peaks), "tactics": tac}
+    if tac:
+        rec["physical_tflops"] = sum(2.0 * t["P_at_tile"] * t["N"] * t["K"] for t in tac) / (ms * 1e-3) / 1e12
+        rec["computed_rows_tflops"] = sum(2.0 * t["rows_computed"] * t["N"] * t["K"] for t in tac) / (ms * 1e-3) / 1e12
+        rec["P_at_tile"] = [t["P_at_tile"] for t in tac]
+        rec["pad_frac_at_tile"] = [t["pad_frac_at_tile"] for t in tac]
+        rec["effective_experts"] = tac[0]["effective_experts"]
+    if cpu is None and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, args.config_cpu_budget)
+    rec["cpu_baseline"] = cpu
+    return rec
+
+
 # ------------------------------------------------------------------ arms
 def run_ours(args):
     ws, rank, local = dist_setup()
     dev = torch.device("cuda", local)
+    mb = _binding()
     lib = mb.load()
     mb.set_kernel_policy(mb.POLICIES[args.kernel_policy])
-    w = make_workload(args.workload, dev)
+    w = Workload(args.workload).attach_gpu(mb, dev)
     stream = torch.cuda.current_stream()
     peaks = load_peaks()
+    flush = L2Flush(dev)
 
     for _ in range(args.warmup):
+        flush()
         w.step(lib, stream)
     torch.cuda.synchronize()
-    if int(w.status.item()) != 0:
-        raise RuntimeError("device status " + mb.status_str(int(w.status.item())))
+    w.check_status()
 
     n_g = len(w.gemms)
     evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(n_g)]
            for _ in range(args.steps)]
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.6)
     for _ in range(max(3, args.warmup)):
+        flush()
         w.step(lib, stream)
     barrier(ws)
     torch.cuda.synchronize()
     t_host0 = time.time()
-    start.record(stream)
     for i in range(args.steps):
+        flush()
         w.step(lib, stream, evs[i])
-    end.record(stream)
     torch.cuda.synchronize()
     t_host1 = time.time()
     barrier(ws)
-    time.sleep(0.3)
-    sampler.stop()
-    ms = start.elapsed_time(end)
+    per_step = [sum(evs[i][g][0].elapsed_time(evs[i][g][1]) for g in range(n_g)) for i in range(args.steps)]
+    ms = sum(per_step)
     ms_max = max_over_ranks(ms, ws)
     per_gemm = [sum(evs[i][g][0].elapsed_time(evs[i][g][1]) for i in range(args.steps)) / args.steps
                 for g in range(n_g)]
-    if int(w.status.item()) != 0:
-        raise RuntimeError("device status " + mb.status_str(int(w.status.item())))
+    w.check_status()
     value = weak_scaling_value(w.flops() * args.steps, ws, ms_max) / 1e12
 
     # end to end: host buffers in, results back to host, same step count
@@ -664,60 +752,80 @@ def run_ours(args):
         e2e = {"value": weak_scaling_value(w.flops() * n2, ws, ms2) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": n2,
                "ms_per_step": ms2 / n2}
+        w.h_in = w.h_out = None
 
     roof = w.roofline(per_gemm, peaks)
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, args.cpu_budget)
+
+    configs, t_cfg0, t_cfg1 = None, None, None
+    if rank == 0 and not args.no_configs:
+        configs = {}
+        t_cfg0 = time.time()
+        for name in CONFIGS:
+            if name == w.name:
+                cw = w
+            else:
+                cw = Workload(name).attach_gpu(mb, dev)
+            configs[name] = config_record(cw, lib, stream, flush, peaks, args,
+                                          cpu=cpu if cw is w else None)
+            if cw is not w:
+                del cw
+                torch.cuda.empty_cache()
+        t_cfg1 = time.time()
+    time.sleep(0.3)
+    sampler.stop()
     if rank != 0:
         return
-    cpu = None
-    if ws == 1 and not args.no_cpu_baseline:
-        experts, useful, secs = oracle_sample_bounded(w, args.cpu_budget)
-        cpu = {"value": useful / secs / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
-               "sample": f"experts {experts} of {args.workload}: {sample_steps(w)}, "
-                         f"{useful / 1e9:.1f} useful GFLOP in {secs:.1f} s"}
     line = {
-        "metric": "effective TFLOPS (valid rows only)",
+        "metric": METRIC,
         "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_max / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": ("e4m3xe2m1" if getattr(w, "w4", False) else "e4m3") if w.fp8 else "bf16",
+        "vs_baseline": None, "dtype": ("e4m3xe2m1" if w.w4 else "e4m3") if w.fp8 else "bf16",
         "data": "synthetic",
-        "config": dict(w.config(), kernel_policy=args.kernel_policy),
+        "config": w.config(),
+        "kernel_policy": args.kernel_policy,
         "per_gemm_ms": per_gemm,
-        "tactics": ([tactic_report(w.dtype, w.counts, g["N"], g["K"], t) for g, t in zip(w.gemms, per_gemm)]
-                    if hasattr(w, "dtype") else None),
+        "tactics": w.tactics(per_gemm),
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": w.launches_per_step() * args.steps,
         "clocks": sampler.summary(t_host0, t_host1),
     }
+    if configs is not None:
+        line["configs"] = configs
+        line["clocks_configs"] = sampler.summary(t_cfg0, t_cfg1)
     print(json.dumps(line))
 
 
 def run_reference(args):
+    """The oracle on the host cores, one rotating active expert per step of
+    the same workload and config as the GPU arm; loads no part of the
+    CUDA library."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
-    w = make_workload(args.workload, dev)
+    w = Workload(args.workload).attach_cpu()
     active = [e for e, t in enumerate(w.counts) if t]
     total_u, total_s = 0.0, 0.0
-    per_step = 1
     for i in range(args.warmup + args.steps):
-        experts = [active[(i * per_step + j) % len(active)] for j in range(per_step)]
-        u, s = w.oracle_sample(experts)
+        u, s = w.oracle_sample([active[i % len(active)]])
         if i >= args.warmup:
             total_u += u
             total_s += s
     value = total_u / total_s / 1e12
     cores = blas_threads()
     line = {
-        "impl": "reference", "metric": "effective TFLOPS (valid rows only)", "value": value, "unit": "TFLOP/s",
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": total_s * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": w.config(),
+        "kernel_policy": args.kernel_policy,
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": f"one active expert per step (rotating) of {args.workload}: "
-                                   f"{sample_steps(w)}"},
+                                   f"{w.sample_steps()}"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -732,9 +840,13 @@ def main():
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(wl.WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-config records")
+    ap.add_argument("--reps", type=int, default=20, help="timed L2-flushed reps per config record")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--config-cpu-budget", type=float, default=5.0,
+                    help="seconds of oracle work for each config record's cpu_baseline")
     ap.add_argument("--kernel-policy", choices=["auto", "single", "dual", "pair", "pair_dual"], default="auto",
-                    help="grouped GEMM kernel family (auto: two 128-row weight blocks per SM when N %% 256 == 0)")
+                    help="grouped GEMM kernel family (auto: the library's default per shape)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

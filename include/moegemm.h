@@ -70,7 +70,7 @@ typedef struct {
   int64_t U;           /* useful token rows  sum_e t_e                        */
   int64_t sumsq;       /* sum_e t_e^2; INT64_MAX when it is 2^63 or more      */
   int32_t active;      /* experts with t_e > 0                                */
-  int32_t num_tiles;   /* sum_e ceil(t_e/q)                                   */
+  int32_t num_tiles;   /* sum_e ceil(t_e/q); 2^31-1 when it is that or more   */
   double pad_frac;     /* (double)(P-U) / (double)P; 0.0 when P == 0          */
   double eff_experts;  /* ((double)U*(double)U) / (double)(exact sum_e t_e^2),
                           every conversion and operation rounded to nearest;
@@ -101,6 +101,10 @@ const char* mg_status_str(mg_status s);
  *                      min(q, t_e - j*q)).  Experts with t_e = 0 get none.
  *   max_tiles          capacity of `tiles` in triples.
  *   stats              the accounting above.
+ *
+ * A caller that does not know how many tiles to expect calls once with
+ * tiles = NULL and max_tiles = 0 (only offsets and stats are written) and
+ * sizes the list from stats.num_tiles.
  *
  * If there are more than max_tiles tiles, the first max_tiles are written,
  * offsets and stats are complete, and the call reports MG_ERR_CAPACITY.
@@ -253,8 +257,9 @@ mg_status mgemm_contiguous(mg_dtype dt, const void* A, const uint8_t* SFA,
 /* ------------------------------------------------------------------------
  * Masked grouped GEMM ("flops/deepgemm-grouped-masked-moe-gemm",
  * "Workarounds": masked grouped GEMM for decode under CUDA graphs;
- * "Arithmetic intensity": the kernel takes a mask and computes only the
- * valid portions, so no CPU sync sits on the critical path).
+ * "Arithmetic intensity": each expert owns a fixed-size buffer and a
+ * per-expert row count on the device tells the kernel how many of its rows
+ * to compute, so the host never waits for the routing result).
  *
  * For every e and every r < v_e = d_valid_m[e]:
  *     D[e, r, :] = A[e, r, :] * B[e]^T

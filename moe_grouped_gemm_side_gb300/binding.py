@@ -178,15 +178,26 @@ def status_str(code: int) -> str:
 
 # ------------------------------------------------------------------ host plan
 def plan_host(counts, q: int, max_tiles: int = None):
-    """moe_plan_host: returns (offsets int64 [E+1], tiles int32 [T,3], PlanStats, status)."""
+    """moe_plan_host: returns (offsets int64 [E+1], tiles int32 [T,3], PlanStats, status).
+
+    With max_tiles None the tile list is sized by the library: a first call
+    without a list reports the tile count in its stats."""
     lib = load()
     c = np.ascontiguousarray(np.asarray(counts, dtype=np.int32))
     E = len(c)
     offsets = np.zeros(E + 1, dtype=np.int64)
-    if max_tiles is None:
-        max_tiles = int(sum(-(-int(t) // q) for t in c if t > 0)) if q > 0 else 0
-    tiles = np.zeros((max(max_tiles, 1), 3), dtype=np.int32)
     st = PlanStats()
+    if max_tiles is None:
+        code = lib.moe_plan_host(c.ctypes.data_as(_c_i32p), E, q, offsets.ctypes.data_as(_c_i64p),
+                                 None, 0, ctypes.byref(st))
+        if code != MG_OK:
+            return offsets, np.zeros((0, 3), dtype=np.int32), st, code
+        if st.num_tiles == 2 ** 31 - 1:
+            # saturated count: rows of such a list would pass 2^31 - 1, which
+            # an int32 tile list refuses anyway
+            return offsets, np.zeros((0, 3), dtype=np.int32), st, 2
+        max_tiles = st.num_tiles
+    tiles = np.zeros((max(max_tiles, 1), 3), dtype=np.int32)
     code = lib.moe_plan_host(c.ctypes.data_as(_c_i32p), E, q, offsets.ctypes.data_as(_c_i64p),
                              tiles.ctypes.data_as(_c_i32p) if max_tiles > 0 else None,
                              max_tiles, ctypes.byref(st))

@@ -305,7 +305,7 @@ mg_status moe_plan_host(const int32_t* counts, int32_t E, int32_t q, int64_t* of
   const SumSq sq = sumsq_finish(sq_hi_sum, sq_lo_sum);
   stats->sumsq = sq.value;
   stats->active = active;
-  stats->num_tiles = (int32_t)ntiles;
+  stats->num_tiles = ntiles > INT32_MAX ? INT32_MAX : (int32_t)ntiles;  // saturates
   stats->pad_frac = plan_pad_frac(P, U);
   stats->eff_experts = plan_eff_experts_exact(U, sq.f64);
   if (tiles != nullptr && ntiles > max_tiles) return MG_ERR_CAPACITY;

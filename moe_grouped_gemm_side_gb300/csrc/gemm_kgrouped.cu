@@ -56,7 +56,7 @@ struct Params {
 struct Shared {
   uint64_t full[kMaxStages];
   uint64_t fixed[kMaxStages];  // warp 6 has zeroed the stage's tail rows (if any)
-  uint64_t empty[kMaxStages];
+  uint64_t empty[kMaxStages];  // the MMAs reading the stage are done and warp 6 is past it
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint64_t drain;
@@ -130,7 +130,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kMaxStages; ++i) {
       mbar_init(&sh.full[i], 1);
       mbar_init(&sh.fixed[i], 1);
-      mbar_init(&sh.empty[i], 1);
+      // two arrivals free a stage: the MMA commit and warp 6, so the ring
+      // never runs a whole cycle ahead of warp 6 (a warp that fell that far
+      // behind would test a barrier phase that has already come round again)
+      mbar_init(&sh.empty[i], 2);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh.acc_full[i], 1);
@@ -254,9 +257,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // A stage is ready once its operands landed; a stage holding an
       // expert's last, partial token block must also have its rows past the
       // expert zeroed by warp 6.  Testing `fixed` only there saves the
-      // issuing thread a barrier test (~80 cycles) on every other stage;
-      // warp 6 still arrives on every stage, and it can run at most one ring
-      // cycle ahead, so the parity of a later wait stays unambiguous.
+      // issuing thread a barrier test (~80 cycles) on every other stage.
+      // Warp 6 arrives on `fixed` and `empty` for every stage: it cannot be
+      // a cycle ahead of this thread (the stage's refill waits for this
+      // thread's commit) nor a cycle behind it (the refill waits for warp 6
+      // too), so the parity of each wait is unambiguous.
       auto ready = [&](uint32_t st, uint32_t ph, int32_t rem) {
         const bool fix = rem < kBlockT && (rem & 15) != 0;
         return wait_bounded(&sh.full[st], ph, deadline, &sh.abort_flag, p.status) &&
@@ -321,7 +326,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================================================= tail rows
     // Every stage, in order: once it has landed, zero the rows of a partial
     // token block that belong to no token of the expert (up to the next
-    // multiple of 16, the last rows an MMA step reads), then mark it fixed.
+    // multiple of 16, the last rows an MMA step reads), then mark it fixed
+    // and give the producer this warp's half of the stage's release.
     if (S > 0) {
       uint32_t stage = 0, phase = 0;
       bool ok = true;
@@ -352,7 +358,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           __syncwarp();
-          if (lane == 0) mbar_arrive(&sh.fixed[stage]);
+          if (lane == 0) {
+            mbar_arrive(&sh.fixed[stage]);
+            mbar_arrive(&sh.empty[stage]);
+          }
           next_stage(stage, phase);
         }
       }

@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(kPlanThreads)
     s.U = U;
     s.sumsq = sq.value;
     s.active = (int32_t)active;
-    s.num_tiles = (int32_t)carry_tiles;
+    s.num_tiles = carry_tiles > 2147483647LL ? 2147483647 : (int32_t)carry_tiles;  // saturates
     s.pad_frac = plan_pad_frac(carry_rows, U);
     s.eff_experts = plan_eff_experts_exact(U, sq.f64);
     *stats = s;

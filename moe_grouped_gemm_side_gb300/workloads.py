@@ -220,22 +220,33 @@ class Operands:
     SFB: Optional[torch.Tensor] = None
 
 
+def expert_weight(e: int, N: int, K: int, dtype: str, seed: int, device="cpu",
+                  std: float = 1.0):
+    """The weights of expert e alone, exactly as make_weights draws them on
+    the same device: (bf16 values, None) or (codes, scales)."""
+    if dtype == "bf16":
+        return normal_bf16((N, K), seed * 1000 + e, device, std), None
+    w = normal_f32((N, K), seed * 1000 + e, device, std)
+    return quantize_weight_mx4(w) if dtype == "fp8xfp4" else quantize_weight_fp8(w)
+
+
 def make_weights(E: int, N: int, K: int, dtype: str, seed: int, device="cpu",
                  std: float = 1.0):
-    """Expert weights [E, N, K] (+ SFB [E, K/128, N/128] for fp8)."""
+    """Expert weights [E, N, K] (+ SFB [E, K/128, N/128] for fp8), one seeded
+    draw per expert."""
     if dtype == "bf16":
-        return normal_bf16((E, N, K), seed, device, std), None
+        B = torch.empty((E, N, K), dtype=torch.bfloat16, device=device)
+        for e in range(E):
+            B[e] = expert_weight(e, N, K, dtype, seed, device, std)[0]
+        return B, None
     if dtype == "fp8xfp4":
         B = torch.empty((E, N, K // 2), dtype=torch.uint8, device=device)
         SFB = torch.empty((E, N, K // 32), dtype=torch.uint8, device=device)
-        for e in range(E):
-            B[e], SFB[e] = quantize_weight_mx4(normal_f32((N, K), seed * 1000 + e, device, std))
-        return B, SFB
-    B = torch.empty((E, N, K), dtype=torch.uint8, device=device)
-    SFB = torch.empty((E, K // 128, N // 128), dtype=torch.uint8, device=device)
+    else:
+        B = torch.empty((E, N, K), dtype=torch.uint8, device=device)
+        SFB = torch.empty((E, K // 128, N // 128), dtype=torch.uint8, device=device)
     for e in range(E):
-        w = normal_f32((N, K), seed * 1000 + e, device, std)
-        B[e], SFB[e] = quantize_weight_fp8(w)
+        B[e], SFB[e] = expert_weight(e, N, K, dtype, seed, device, std)
     return B, SFB
 
 

@@ -61,8 +61,8 @@ def contiguous(A: np.ndarray, B: np.ndarray, counts, align_q: int):
 
 def masked(A: np.ndarray, B: np.ndarray, valid_m):
     """Masked form ("Workarounds": masked grouped GEMM for decode under CUDA
-    graphs; "Arithmetic intensity": the kernel takes a mask and computes only
-    the valid portions).
+    graphs; "Arithmetic intensity": fixed per-expert buffers, of which only
+    the first valid_m[e] rows of expert e are computed).
 
     A: float64 [E, M_max, K]; B: float64 [E, N, K]; valid_m [E].
     R[e, r] = A[e, r] @ B[e]^T for r < valid_m[e]; other rows are untouched.

@@ -117,6 +117,30 @@ def test_host_plan_maximum_experts(lib):
     assert code == 1
 
 
+def test_host_plan_tile_count_saturates(lib):
+    """sum_e ceil(t_e/q) past 2^31-1 reads 2^31-1 (a closed form, no list)."""
+    huge = [2 ** 31 - 1, 2 ** 31 - 1]
+    offs, _, st, code = mb.plan_host(huge, 1, max_tiles=0)
+    assert code == 0 and st.P == 2 * (2 ** 31 - 1) and st.num_tiles == 2 ** 31 - 1
+    _, _, st, code = mb.plan_host([2 ** 31 - 1], 1, max_tiles=0)
+    assert code == 0 and st.num_tiles == 2 ** 31 - 1
+    _, _, st, code = mb.plan_host([2 ** 31 - 2, 0], 1, max_tiles=0)
+    assert code == 0 and st.num_tiles == 2 ** 31 - 2
+    # the binding sizes a list from that count and refuses one that cannot exist
+    _, tiles, st, code = mb.plan_host(huge, 1)
+    assert code == 2 and tiles.shape == (0, 3)
+
+
+def test_host_plan_sizing_call_matches_list(lib):
+    """A call without a tile list reports the count the list then holds."""
+    counts = [4, 1026, 0, 17, 255, 256, 257]
+    for q in (1, 7, 16, 128):
+        _, _, st0, code0 = mb.plan_host(counts, q, max_tiles=0)
+        offs, tiles, st, code = mb.plan_host(counts, q)
+        assert code0 == 0 and code == 0 and len(tiles) == st0.num_tiles == st.num_tiles
+        assert [tuple(t) for t in tiles.tolist()] == op.plan(counts, q).tiles
+
+
 def test_host_plan_capacity_and_errors(lib):
     offs, tiles, st, code = mb.plan_host([17] * 8, 8, max_tiles=5)
     assert code == 4 and st.P == 192 and st.num_tiles == 24 and offs[-1] == 192

@@ -17,7 +17,7 @@ pytestmark = pytest.mark.cpu
 @pytest.mark.parametrize("counts", [wl.counts_zipf_decode(), wl.counts_uniformish(), wl.counts_issue32(),
                                     [0, 0, 0], [1, 15, 16, 17, 239, 240, 241]])
 def test_tactic_report_against_the_oracle_plan(lib, counts):
-    r = bench.tactic_report(mb.MG_FP8_E4M3_UE8M0, counts, 4096, 7168, 1.0)
+    r = bench.tactic_report(mb, mb.MG_FP8_E4M3_UE8M0, counts, 4096, 7168, 1.0)
     q = r["tile_q"]
     assert q == mb.select_tile_host(mb.MG_FP8_E4M3_UE8M0, counts, 4096, 7168, 0)
     ref = op.plan(counts, q)
@@ -26,7 +26,9 @@ def test_tactic_report_against_the_oracle_plan(lib, counts):
     rows = sum((t // q) * q + (-(-(t % q) // 16) * 16) for t in counts)
     assert r["rows_computed"] == rows
     assert r["U"] <= r["rows_computed"] <= r["P_at_tile"]
-    assert r["physical_tflops"] == pytest.approx(2.0 * rows * 4096 * 7168 / 1e-3 / 1e12)
+    # physical throughput as the pages define it (padded rows P), and of the rows computed
+    assert r["physical_tflops"] == pytest.approx(2.0 * ref.P * 4096 * 7168 / 1e-3 / 1e12)
+    assert r["computed_rows_tflops"] == pytest.approx(2.0 * rows * 4096 * 7168 / 1e-3 / 1e12)
 
 
 def test_fp4_dtype_is_read_from_the_weight_shape():
@@ -37,15 +39,22 @@ def test_fp4_dtype_is_read_from_the_weight_shape():
                          torch.zeros((2, 256, 512), dtype=torch.bfloat16), 512) == mb.MG_BF16
 
 
-def test_reference_arm_prints_one_contract_line(lib):
+def test_reference_arm_prints_one_contract_line():
     """`bench.py --impl reference` (the oracle on the host cores) prints one
-    JSON line with the contract's keys, on a small workload."""
+    JSON line with the contract's keys and the GPU arm's config, on a small
+    workload, without loading any part of the CUDA library."""
     import json
     import subprocess
     import sys
     from tests.conftest import ROOT
-    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "contig_bf16_e8_n256_k256",
-                        "--steps", "2", "--warmup", "3"], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    probe = (
+        "import runpy, sys\n"
+        "sys.argv = ['bench.py', '--impl', 'reference', '--workload', 'contig_bf16_e8_n256_k256',"
+        " '--steps', '2', '--warmup', '3']\n"
+        "runpy.run_path('bench.py', run_name='__main__')\n"
+        "maps = open('/proc/self/maps').read()\n"
+        "print('LOADED', 'libmoegemm' in maps, 'moe_grouped_gemm_side_gb300.binding' in sys.modules)\n")
+    r = subprocess.run([sys.executable, "-c", probe], cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
     assert len(lines) == 1
@@ -55,6 +64,32 @@ def test_reference_arm_prints_one_contract_line(lib):
         assert k in d, k
     assert d["impl"] == "reference" and d["value"] > 0 and d["config"]["workload"] == "contig_bf16_e8_n256_k256"
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
+    assert d["config"] == bench.Workload("contig_bf16_e8_n256_k256").config()
+    assert "LOADED False False" in r.stdout
+
+
+@pytest.mark.parametrize("name", bench.CONFIGS)
+def test_host_operands_follow_the_workload_recipe(name):
+    """The reference arm's host operands have the shapes and dtypes of the
+    GPU arm's, and its per-expert weights are the same draws the full
+    weight tensor makes (one seeded draw per expert)."""
+    w = bench.Workload(name)
+    spec = wl.WORKLOADS[name]
+    if w.form == "kgrouped":
+        w.spec = dict(spec, T=300, N=256, K=128)
+        w.counts = [100, 0, 200]
+        w.attach_cpu()
+        dY, X = w.host["rows"][0]
+        assert dY.shape == (300, 256) and X.shape == (300, 128) and dY.dtype == torch.bfloat16
+        return
+    e = next(i for i, t in enumerate(w.counts) if t)
+    w.gemms[0].update(N=256, K=512)          # small shapes, same recipe
+    w.host = {"w": {}}
+    b, sfb = w._host_weight(0, e)
+    full_b, full_sfb = wl.make_weights(e + 1, 256, 512, w.dtype_name, spec["seed"] + 1, "cpu",
+                                       spec.get("b_std", 1.0))
+    assert torch.equal(b, full_b[e])
+    assert (sfb is None and full_sfb is None) or torch.equal(sfb, full_sfb[e])
 
 
 def test_exemplar_tuner_guardrail():
@@ -71,18 +106,6 @@ def test_exemplar_tuner_guardrail():
             assert len(c) == 64 and sum(c) == U and min(c) >= 0
 
 
-def _bare(cls, name, **attrs):
-    """A workload object with only what its roofline reads (no device)."""
-    w = object.__new__(cls)
-    spec = wl.WORKLOADS[name]
-    w.name = name
-    w.counts = spec["counts"]()
-    w.U = sum(w.counts)
-    for k, v in attrs.items():
-        setattr(w, k, v)
-    return w
-
-
 PEAKS = {"hbm_gbs": 6789.6, "bf16_tflops": 1869.1, "source": "measured"}
 
 
@@ -95,22 +118,19 @@ def test_roofline_traffic_is_per_launch(case):
     import os
     if case == "prefill":
         name = "prefill_fp8_e64_t32768_n4096_k7168"
-        w = _bare(bench.Contiguous, name, fp8=True, w4=False, elem=1,
-                  gemms=[dict(N=4096, K=7168, swiglu=False), dict(N=7168, K=2048, swiglu=False)])
-        r, launches, kind = w.roofline([0.84, 0.48], PEAKS), 2, "fwd"
+        r, launches, kind = bench.Workload(name).roofline([0.84, 0.48], PEAKS), 2, "fwd"
     elif case == "masked":
         name = "masked_fp8_e16_m256_n4096_k7168"
-        w = _bare(bench.Masked, name, fp8=True, w4=False, elem=1, E=16, M=256, N=4096, K=7168)
-        r, launches, kind = w.roofline([0.0927], PEAKS), 1, "fwd"
+        r, launches, kind = bench.Workload(name).roofline([0.0927], PEAKS), 1, "fwd"
     else:
         name = "kgrouped_bf16_e32_t65536_n4096_k2048"
-        w = _bare(bench.KGrouped, name, fp8=False, E=32, N=4096, K=2048)
+        w = bench.Workload(name)
         r, launches, kind = w.roofline([0.787], PEAKS), 1, "kg"
-        assert w.bytes_alg() == 65536 * (4096 + 2048) * 2 + 32 * 4096 * 2048 * 4
+        assert w.bytes_alg_total() == 65536 * (4096 + 2048) * 2 + 32 * 4096 * 2048 * 4
     assert r["launches_per_step"] == launches
     with open(os.path.join(bench.ROOT, "profiles", "dram_traffic.json")) as f:
-        rec = json.load(f)[name]
-    if rec["sources_sha256"] == bench.kernel_sources_sha(kind):
+        rec = json.load(f).get(name)
+    if rec and rec["sources_sha256"] == bench.kernel_sources_sha(kind):
         assert rec["launches"] == launches
         assert r["traffic_per_step"] == rec["bytes_per_step"]
         assert r["traffic"] == pytest.approx(rec["bytes_per_step"] / launches)
@@ -118,6 +138,32 @@ def test_roofline_traffic_is_per_launch(case):
         assert 0.99 <= r["traffic"] / r["algorithmic_bytes_per_launch"] < 1.2
     else:
         assert r["traffic"] is None and r["traffic_per_step"] is None
+
+
+@pytest.mark.parametrize("name", bench.CONFIGS)
+def test_roofline_bound_is_the_slower_of_compute_and_memory(name):
+    """Every form, the masked one included, is scored against whichever of
+    the useful flops at the tensor peak and the algorithmic bytes at HBM
+    bandwidth takes longer, and frac = that time / the measured time."""
+    w = bench.Workload(name)
+    ms = 1.0
+    r = w.roofline([ms / len(w.gemms)] * len(w.gemms), PEAKS)
+    peak = PEAKS["bf16_tflops"] * (2.0 if w.fp8 else 1.0)
+    t_c = w.flops() / (peak * 1e12)
+    t_m = w.bytes_alg_total() / (PEAKS["hbm_gbs"] * 1e9)
+    assert r["bound"] == ("tensor" if t_c >= t_m else "hbm")
+    assert r["frac"] == pytest.approx(max(t_c, t_m) / (ms * 1e-3))
+
+
+def test_masked_roofline_turns_tensor_bound_when_rows_fill_the_buffers():
+    """A masked decode whose buffers are full does enough work per weight
+    byte to be bound by the tensor peak, not by HBM."""
+    w = bench.Workload("masked_fp8_e16_m256_n4096_k7168")
+    assert w.roofline([0.1], PEAKS)["bound"] == "hbm"
+    w.counts = [256] * 16
+    w.U, w.active = 4096, 16
+    peaks = dict(PEAKS, hbm_gbs=20000.0)
+    assert w.roofline([0.1], peaks)["bound"] == "tensor"
 
 
 def test_traffic_is_null_once_kernel_sources_change(monkeypatch):

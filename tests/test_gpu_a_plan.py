@@ -84,6 +84,20 @@ def test_device_plan_square_sum_past_int64(lib, cuda):
         assert float(st["eff_experts"]).hex() == ref.eff_experts.hex()
 
 
+def test_device_plan_tile_count_saturates(lib, cuda):
+    """sum_e ceil(t_e/q) past 2^31-1 reads 2^31-1, as on the host."""
+    m = 2 ** 31 - 1
+    for counts, want in (([m, m], m), ([m], m), ([m - 1, 0], m - 1)):
+        d = torch.tensor(counts, dtype=torch.int32, device=cuda)
+        status = torch.zeros(1, dtype=torch.int32, device=cuda)
+        _, _, stats = mb.plan(d, 1, 0, status=status)
+        torch.cuda.synchronize()
+        st = mb.decode_stats(stats)
+        assert int(status.item()) == 0 and st["num_tiles"] == want and st["P"] == sum(counts)
+        _, _, hst, _ = mb.plan_host(counts, 1, max_tiles=0)
+        assert hst.num_tiles == want
+
+
 def test_device_plan_errors(lib, cuda):
     ref, offs, tiles, st, status = _device_plan([17] * 8, 8, max_tiles=5)
     assert status == 4 and st["P"] == 192 and tiles == ref.tiles[:5] and offs == ref.offsets

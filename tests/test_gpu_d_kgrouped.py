@@ -101,3 +101,14 @@ def test_max_experts(lib, cuda):
     got, ref, status = run_kgrouped(counts, 256, 128, integer=True, T_extra=5)
     assert status == 0
     assert np.array_equal(got, ref)
+
+
+def test_long_experts_with_tails(lib, cuda):
+    """Experts of 2^15+ tokens ending in a partial token block: hundreds of
+    full stages go by before the one whose tail rows need zeroing, so the
+    tail-zeroing warp must stay in step with the ring all the way.  Integer
+    operands keep every fp32 sum exact (|sum| <= 4 * 40037 < 2^24)."""
+    counts = [40037, 0, 3, 33005]
+    got, ref, status = run_kgrouped(counts, 256, 256, integer=True, T_extra=7)
+    assert status == 0
+    assert np.array_equal(got, ref)
