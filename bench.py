@@ -712,9 +712,16 @@ def run_ours(args):
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.6)
-    for _ in range(max(3, args.warmup)):
-        flush()
-        w.step(lib, stream)
+    # soak: the same steps back to back for `--soak` seconds right before the
+    # timed region, so the clock record holds samples taken under this load
+    t_soak0 = time.time()
+    while True:
+        for _ in range(max(3, args.warmup)):
+            flush()
+            w.step(lib, stream)
+        torch.cuda.synchronize()
+        if time.time() - t_soak0 >= args.soak:
+            break
     barrier(ws)
     torch.cuda.synchronize()
     t_host0 = time.time()
@@ -792,7 +799,8 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": w.launches_per_step() * args.steps,
-        "clocks": sampler.summary(t_host0, t_host1),
+        "clocks": dict(sampler.summary(t_soak0, t_host1), window="soak of the same steps + timed region",
+                       soak_s=round(t_host0 - t_soak0, 2), timed_s=round(t_host1 - t_host0, 3)),
     }
     if configs is not None:
         line["configs"] = configs
@@ -842,6 +850,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-config records")
     ap.add_argument("--reps", type=int, default=20, help="timed L2-flushed reps per config record")
+    ap.add_argument("--soak", type=float, default=2.0,
+                    help="seconds of back-to-back steps right before the timed region (clock record)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--config-cpu-budget", type=float, default=5.0,
                     help="seconds of oracle work for each config record's cpu_baseline")

@@ -69,6 +69,41 @@ def test_prefill_fp8_sampled_experts(lib, cuda, gemm_index):
         gu.check_frobenius(Dbits[o:o + t], og.expert_product(a, b))
 
 
+def _row_sample(t, q, rng, extra=8):
+    """Rows of an expert to check: its first rows, the rows of its last
+    token tile (trimmed to a multiple of 16 by the kernel, capped at 48),
+    and a few random rows."""
+    last0 = (t // q) * q if t % q else max(0, t - q)
+    rows = set(range(min(t, 8))) | set(range(last0, min(t, last0 + 48)))
+    rows |= set(int(r) for r in rng.integers(0, t, size=min(extra, t)))
+    return np.array(sorted(rows))
+
+
+@pytest.mark.parametrize("gemm_index", [0, 1])
+def test_prefill_fp8_every_expert_row_sample(lib, cuda, gemm_index):
+    """Skewed FP8 prefill, both GEMMs: every expert, on a row sample that
+    holds the rows of its last token tile at the tile the device chose (the
+    one the kernel trims), the first rows and random rows; the per-expert
+    Frobenius rule applies to the sampled rows, all columns."""
+    name = "prefill_fp8_e64_t32768_n4096_k7168"
+    counts, p, ops, Dbits = _contiguous_full(name, cuda, gemm_index)
+    N, K = ops.B.shape[1], ops.B.shape[2]
+    q = mb.select_tile_host(mb.MG_FP8_E4M3_UE8M0, counts, N, K, torch.cuda.get_device_properties(0).multi_processor_count)
+    rng = np.random.default_rng(11 + gemm_index)
+    partial = 0
+    for e, t in enumerate(counts):
+        if t == 0:
+            continue
+        partial += t % q != 0
+        o = p.offsets[e]
+        rows = _row_sample(t, q, rng)
+        idx = torch.from_numpy(o + rows).to(ops.A.device)
+        a = on.dequant_rows(ops.A[idx].cpu().numpy(), ops.SFA[:, idx].cpu().numpy())
+        b = on.dequant_weight(ops.B[e].cpu().numpy(), ops.SFB[e].cpu().numpy())
+        gu.check_frobenius(Dbits[o + rows], og.expert_product(a, b))
+    assert partial > 0
+
+
 def test_prefill_bf16_sampled_experts(lib, cuda):
     counts, p, ops, Dbits = _contiguous_full("prefill_bf16_e64_t32768_n4096_k7168", cuda)
     order = np.argsort(counts)
