@@ -26,19 +26,32 @@
 // moves ~94 KB through an SM's shared memory for 3.9 M fp8 multiply-adds and
 // the tensor pipe waits.  Two blocks against the same token tile, and the
 // pair's split of the token operand, cut the bytes per multiply-add.  Two
-// 240/256-column fp32 accumulators fill TMEM, so two-block tiles run one at
-// a time (the epilogue is not overlapped); one-block tiles keep two
-// accumulators and overlap the epilogue with the next main loop.
+// 240/256-column fp32 accumulators fill TMEM, so a tile's epilogue is not
+// overlapped with the next tile's main loop.
 //
-// CTA = 11 warps: warp 0 issues TMA; warp 1 owns TMEM and one of its threads
-// (of the pair's first CTA) issues every tcgen05.mma and tcgen05.cp; warps
-// 2-5 and 7-10 drain the fp32 accumulators from TMEM (two warps per 32-lane
-// quadrant, alternate 16-token chunks) and store bf16 rows; warp 6 (fp8
-// only) turns each stage's raw UE8M0 bytes into the TMEM scale-word layout,
-// four K-blocks per word.  The tensor pipe queues only a few MMAs, so the
-// issuing thread does nothing between MMAs but wait for the next stage: any
-// other work there (warp-wide synchronisation, building scale words,
-// decoding tiles) left the pipe idle.
+// CTA = 12 warps: warp 0 issues TMA; warps 1 and 11 issue the tcgen05.mma
+// and tcgen05.cp on one SM (below), warp 1 alone for a CTA pair (the pair's
+// first CTA); warps 2-5 and 7-10 drain the fp32 accumulators from TMEM (two
+// warps per 32-lane quadrant, alternate 16-token chunks) and store bf16 rows;
+// warp 6 (fp8 only) turns each stage's raw UE8M0 bytes into the TMEM
+// scale-word layout, four K-blocks per word.
+//
+// MMA issue.  The tensor pipe queues only about two MMAs, so whatever the
+// issuing thread does between MMAs (a barrier test ~90 cycles, a commit ~60,
+// address arithmetic) shows up as idle pipe time: with one issuing thread a
+// stage of eight 128 x 240 x 32 block-scaled MMAs took ~1530 cycles against
+// ~1300 of MMA work (in-kernel clock stamps).  So on one SM two warps issue,
+// each into a 256-column TMEM allocation of its own holding its accumulator
+// and its copy of the scale words: for two-block tiles warp 1 issues block
+// 0's MMAs and warp 11 block 1's; for one-block tiles each issues two of
+// every stage's four K-steps into its own accumulator, and the epilogue adds
+// the two partial sums (one fp32 addition, then the single bf16 rounding).
+// One thread's barrier tests and commits then overlap the other's queued
+// MMAs.  The issuing warps run their loops with all 32 lanes and lane 0
+// alone executes each tcgen05 instruction: descriptors and addresses stay
+// warp-uniform, which made issue cheaper again (FP8 GEMM1 of the skewed
+// prefill: 0.844 ms with one single-lane issuer, 0.811 with two, 0.788 with
+// two warp-wide; BF16 GEMM2: 0.841, 0.797, 0.743).
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -49,8 +62,10 @@
 namespace mg {
 namespace fwd {
 
-constexpr int kThreads = 352;
+constexpr int kThreads = 384;
 constexpr int kSfWarp = 6;
+// Second MMA-issuing warp of single-SM two-block tiles (block 1's MMAs).
+constexpr int kMma2Warp = 11;
 constexpr int kEpiWarps = 8;                     // warps 2-5 and 7-10: two per TMEM lane quadrant
 constexpr int kMaxStages = 16;
 constexpr int kCtaRows = 128;                    // weight rows of one block on one SM
@@ -104,6 +119,7 @@ struct Shared {
   uint64_t acc_empty[2];
   uint64_t drain;
   uint32_t tmem_base;
+  uint32_t tmem_base2;  // two issuers: block 1's own TMEM allocation
   int32_t abort_flag;
   int32_t q;         // token tile of full tiles
   int32_t qn_max;    // widest tile of this launch
@@ -187,6 +203,64 @@ __device__ __forceinline__ uint32_t group_weight_word(const uint32_t (&wsf)[4], 
   return w;
 }
 
+// Predicated issue: the whole warp runs the issue loop (descriptors and
+// addresses stay warp-uniform); lane 0 alone executes the tcgen05 op.
+__device__ __forceinline__ void mma_f16_e(uint32_t e, uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+      "@q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(e));
+}
+__device__ __forceinline__ void mma_mxf8_e(uint32_t e, uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %6, 0;\n\tsetp.ne.b32 q, %7, 0;\n\t"
+      "@q tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
+      " [%0], %1, %2, %3, [%4], [%5], p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate), "r"(e));
+}
+__device__ __forceinline__ void mma_f16_pair_e(uint32_t e, uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+      "@q tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(e));
+}
+__device__ __forceinline__ void mma_mxf8_pair_e(uint32_t e, uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %6, 0;\n\tsetp.ne.b32 q, %7, 0;\n\t"
+      "@q tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X"
+      " [%0], %1, %2, %3, [%4], [%5], p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate), "r"(e));
+}
+__device__ __forceinline__ void mma_commit_e(uint32_t e, uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %1, 0;\n\t"
+      "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}\n" ::"r"(
+          smem_u32(bar)), "r"(e)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit_pair_e(uint32_t e, uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t"
+      "@q tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;\n\t}\n" ::"r"(smem_u32(bar)), "h"(mask), "r"(e)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_cp_32x128b_x4_e(uint32_t e, uint32_t taddr, uint64_t sdesc) {
+  asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t"
+               "@q tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n\t}\n" ::"r"(taddr), "l"(sdesc), "r"(e)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_cp_32x128b_x4_pair_e(uint32_t e, uint32_t taddr, uint64_t sdesc) {
+  asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t"
+               "@q tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;\n\t}\n" ::"r"(taddr), "l"(sdesc), "r"(e)
+               : "memory");
+}
 // kind::mxf8f6f4 instruction-descriptor A format E2M1 (FP4), bits 7-9.
 constexpr uint32_t kIdescAE2M1 = 5u << 7;
 
@@ -218,7 +292,8 @@ __device__ __forceinline__ float swiglu_f32(uint32_t g, uint32_t u) {
 
 // To bf16: lane pairs exchange so each store writes two features.
 __device__ __forceinline__ void swiglu_bf16_tile(const Params& p, const Tile& tl, uint32_t taddr,
-                                                 uint32_t quad, int32_t half, uint32_t lane) {
+                                                 uint32_t taddr_up, uint32_t quad, int32_t half,
+                                                 uint32_t lane) {
   const int32_t I = p.N >> 1;
   const int32_t f = tl.nb * kCtaRows + (int32_t)(quad * 32u + lane);  // this thread's feature
   const bool odd = (lane & 1u) != 0;
@@ -226,7 +301,7 @@ __device__ __forceinline__ void swiglu_bf16_tile(const Params& p, const Tile& tl
   for (int32_t c0 = 16 * half; c0 < tl.qn; c0 += 32) {
     uint32_t g[16], u[16];
     tmem_ld16(taddr + (uint32_t)c0, g);
-    tmem_ld16(taddr + kAccStride + (uint32_t)c0, u);
+    tmem_ld16(taddr_up + (uint32_t)c0, u);
     tmem_ld_wait();
     tmem_regs_ready(g);
     tmem_regs_ready(u);
@@ -259,8 +334,9 @@ __device__ __forceinline__ void swiglu_bf16_tile(const Params& p, const Tile& tl
 // tile's accumulator, so one buffer of maxima suffices.  Returns false if
 // the wait gave up.
 __device__ __forceinline__ bool swiglu_fp8_tile(const Params& p, Shared& sh, const Tile& tl,
-                                                uint32_t taddr, uint32_t quad, int32_t half,
-                                                uint32_t lane, uint32_t tile_par, uint64_t deadline) {
+                                                uint32_t taddr, uint32_t taddr_up, uint32_t quad,
+                                                int32_t half, uint32_t lane, uint32_t tile_par,
+                                                uint64_t deadline) {
   const int32_t I = p.N >> 1;
   const int32_t f = tl.nb * kCtaRows + (int32_t)(quad * 32u + lane);
   const bool odd = (lane & 1u) != 0;
@@ -268,7 +344,7 @@ __device__ __forceinline__ bool swiglu_fp8_tile(const Params& p, Shared& sh, con
   for (int32_t c0 = 16 * half; c0 < tl.qn; c0 += 32) {
     uint32_t g[16], u[16];
     tmem_ld16(taddr + (uint32_t)c0, g);
-    tmem_ld16(taddr + kAccStride + (uint32_t)c0, u);
+    tmem_ld16(taddr_up + (uint32_t)c0, u);
     tmem_ld_wait();
     tmem_regs_ready(g);
     tmem_regs_ready(u);
@@ -380,31 +456,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   // token words (8 columns).
   const uint32_t sfa_col = 496u;
   // (sfb_col: after the block-1 weight words when tiles have two blocks)
-  // widest token tile: 256, but 240 where two fp8 accumulators must leave
-  // room for the scale words
-  const int32_t q_cap = (kBlocks == 2 && p.fp8) ? 240 : 256;
+  // widest token tile: 256, but 240 for fp8 wherever an accumulator shares
+  // its 256 TMEM columns with the scale words
+  const int32_t q_cap = (p.fp8 && (kBlocks == 2 || !kPair)) ? 240 : 256;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kMaxStages; ++i) {
       // single SM, fp8: the scale warp's arrival completes the stage's
       // operand barrier too, so the MMA thread tests one barrier per stage
       mbar_init(&sh.full[i], (!kPair && p.fp8) ? 2 : 1);
-      mbar_init(&sh.empty[i], 1);
       mbar_init(&sh.sf_full[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&sh.acc_full[i], 1);
+    for (int i = 0; i < 2; ++i)
       mbar_init(&sh.acc_empty[i], kEpiWarps * (kPair ? 2 : 1));  // one arrival per epilogue warp
-    }
-    mbar_init(&sh.drain, 1);
+    // (empty, acc_full and drain count one commit per MMA-issuing thread:
+    // initialised once the block count of the launch is known)
     for (int i = 0; i < 2; ++i) mbar_init(&sh.amax_bar[i], 4 * 32);
     for (int i = 0; i < 4; ++i) mbar_init(&sh.sf_grp[i], 2);
     sh.abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 1) {
-    if constexpr (kPair) tmem_alloc_pair(&sh.tmem_base, kTmemCols);
-    else tmem_alloc(&sh.tmem_base, kTmemCols);
+  if constexpr (kPair) {
+    if (warp == 1) tmem_alloc_pair(&sh.tmem_base, kTmemCols);
   }
 
   // ---- validated counts
@@ -513,9 +586,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       sh.q = q;
       sh.qn_max = max(qmax, 16);
       sh.nblk = nblk;
+      // one commit per MMA-issuing thread frees a stage, fills an
+      // accumulator and drains the CTA's tensor work
+      const uint32_t issuers = !kPair ? 2u : 1u;
+      for (int i = 0; i < kMaxStages; ++i) mbar_init(&sh.empty[i], issuers);
+      for (int i = 0; i < 2; ++i) mbar_init(&sh.acc_full[i], issuers);
+      mbar_init(&sh.drain, issuers);
+      fence_barrier_init();
     }
   }
   __syncthreads();
+  // On one SM two warps issue the MMAs (of block 0 and block 1 for
+  // two-block tiles, of the first and the last two K-steps of every stage
+  // for one-block tiles), each into a 256-column TMEM allocation of its own:
+  // its accumulator at columns 0-239 (bf16: 0-255) and the scale words its
+  // MMAs read at 240-251.  A CTA pair keeps one 512-column allocation.
+  const bool two_issuers = !kPair;
+  if constexpr (!kPair) {
+    if (warp == 1) tmem_alloc_keep_permit(&sh.tmem_base, two_issuers ? 256u : kTmemCols);
+    if (two_issuers && warp == kMma2Warp) tmem_alloc_keep_permit(&sh.tmem_base2, 256u);
+    __syncthreads();
+    if (warp == 1) tmem_relinquish();
+  }
   tc_fence_after();
   // barriers of both CTAs are initialised before any cross-CTA traffic
   if constexpr (kPair) cluster_sync();
@@ -547,8 +639,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(sf_area) + (uintptr_t)S * sf_bytes + 1023) & ~uintptr_t(1023));
   // accumulator sets: two (double buffered) with one block, unless fp8 scale
   // words need the columns; one with two blocks
-  const uint32_t n_acc = (nblk == 1 && (!p.fp8 || sh.qn_max <= 240)) ? 2u : 1u;
+  const uint32_t n_acc = (!two_issuers && nblk == 1 && (!p.fp8 || sh.qn_max <= 240)) ? 2u : 1u;
   const uint32_t tmem = sh.tmem_base;
+  // block b's accumulator for accumulator set 0 (set a adds a * kAccStride
+  // where a tile has one block)
+  const uint32_t tacc1 = two_issuers ? sh.tmem_base2 : tmem + kAccStride;
 
   if (warp == 0) {
     // ================================================= TMA producer
@@ -649,9 +744,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp == 1) {
-    // ================================================= MMA issuer (one thread)
-    if (leader && lane == 0 && S > 0) {
+  } else if (warp == 1 || (two_issuers && warp == kMma2Warp)) {
+    // ================================================= MMA issuers
+    // Warps 1 and 11 on one SM (two-block tiles: block 0 and block 1;
+    // one-block tiles: K-steps 0-1 and 2-3 of every stage), warp 1 of the
+    // first CTA for a pair.  All lanes run the loop; lane 0 (e0) executes the
+    // tcgen05 instructions.
+    const int32_t me = warp == 1 ? 0 : 1;   // issuer index
+    const uint32_t e0 = lane == 0 ? 1u : 0u;
+    if (leader && S > 0) {
       // a stage is ready once its operands landed and (fp8, one SM) its scale
       // words are built: both complete the stage's barrier (each test of a
       // barrier costs the issuing thread ~80 cycles).  A pair's scale words
@@ -662,15 +763,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto ready = [&](uint32_t st, uint32_t ph) {
         return wait_bounded(&sh.full[st], ph, deadline, &sh.abort_flag, p.status);
       };
+      // this thread's TMEM: its accumulator(s) and scale-word columns
+      const uint32_t my_tmem = me == 0 ? tmem : tacc1;
+      const uint32_t my_sfa = two_issuers ? my_tmem + 240u : tmem + sfa_col;  // + 4 b: block b's words
+      const uint32_t my_sfb = two_issuers ? my_tmem + 244u : tmem + sfb_col;
       uint32_t grp = 0;  // pairs: groups of scale words consumed
       with_blocks([&](auto bc) {
       constexpr int kB = decltype(bc)::value;
+      // blocks this thread issues: all kB, or block `me` alone
+      const int b_lo = (two_issuers && kB == 2) ? me : 0, b_hi = (two_issuers && kB == 2) ? me + 1 : kB;
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       for (int32_t t = unit, ti = 0; ok && t < total; t += n_units, ++ti) {
         if (!wait_bounded(&sh.acc_empty[acc], acc_phase ^ 1u, deadline, &sh.abort_flag, p.status)) break;
         tc_fence_after();
-        const uint32_t d0 = tmem + acc * kAccStride;   // block b accumulates at d0 + b * 256
+        // block b accumulates at d0 + b * kAccStride (one allocation), or at
+        // the start of this thread's own allocation (two issuers)
+        const uint32_t d0 = tmem + acc * kAccStride;
         // The wait for stage kb+1 sits between the third and the fourth
         // K-step of stage kb, so the tensor pipe holds queued work while the
         // thread waits.  No tcgen05 fence follows the stage waits: the
@@ -697,8 +806,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if constexpr (!kPair) {
             if (kW4) {
               const uint32_t atoms = smem_u32(sf_area + (size_t)stage * sf_bytes + kSfStage + 2 * kWsfBytes);
-              tmem_cp_32x128b_x4(tmem + sfa_col, desc_sf_32x16(atoms));
-              if (kB == 2) tmem_cp_32x128b_x4(tmem + sfa_col + 4, desc_sf_32x16(atoms + kWsfAtom));
+              for (int b = b_lo; b < b_hi; ++b)
+                tmem_cp_32x128b_x4_e(e0, my_sfa + 4 * (b - b_lo), desc_sf_32x16(atoms + b * kWsfAtom));
             }
           }
           if (p.fp8 && sid == 0) {
@@ -709,52 +818,62 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
               }
               ++grp;
-              tmem_cp_32x128b_x4_pair(tmem + sfa_col, desc_sf_32x16(sfs + kSfRaw));
-              if (kB == 2) tmem_cp_32x128b_x4_pair(tmem + sfa_col + 4, desc_sf_32x16(sfs + kSfW1));
-              tmem_cp_32x128b_x4_pair(tmem + sfb_col, desc_sf_32x16(sfs + kSfRaw + 512));
-              if (qn > 128) tmem_cp_32x128b_x4_pair(tmem + sfb_col + 4, desc_sf_32x16(sfs + kSfRaw + 1024));
+              tmem_cp_32x128b_x4_pair_e(e0, tmem + sfa_col, desc_sf_32x16(sfs + kSfRaw));
+              if (kB == 2) tmem_cp_32x128b_x4_pair_e(e0, tmem + sfa_col + 4, desc_sf_32x16(sfs + kSfW1));
+              tmem_cp_32x128b_x4_pair_e(e0, tmem + sfb_col, desc_sf_32x16(sfs + kSfRaw + 512));
+              if (qn > 128) tmem_cp_32x128b_x4_pair_e(e0, tmem + sfb_col + 4, desc_sf_32x16(sfs + kSfRaw + 1024));
             } else {
               if (!kW4) {
-                tmem_cp_32x128b_x4(tmem + sfa_col, desc_sf_32x16(sfs + kSfRaw));
-                if (kB == 2) tmem_cp_32x128b_x4(tmem + sfa_col + 4, desc_sf_32x16(sfs + kSfW1));
+                // weight words of block b: at kSfRaw (block 0) or kSfW1 (block 1)
+                for (int b = b_lo; b < b_hi; ++b)
+                  tmem_cp_32x128b_x4_e(e0, my_sfa + 4 * (b - b_lo), desc_sf_32x16(sfs + (b == 0 ? kSfRaw : kSfW1)));
               }
-              tmem_cp_32x128b_x4(tmem + sfb_col, desc_sf_32x16(sfs + kSfRaw + 512));
-              if (qn > 128) tmem_cp_32x128b_x4(tmem + sfb_col + 4, desc_sf_32x16(sfs + kSfRaw + 1024));
+              tmem_cp_32x128b_x4_e(e0, my_sfb, desc_sf_32x16(sfs + kSfRaw + 512));
+              if (qn > 128) tmem_cp_32x128b_x4_e(e0, my_sfb + 4, desc_sf_32x16(sfs + kSfRaw + 1024));
             }
           }
           auto kstep = [&](int ks, uint32_t accum) {
             const uint64_t bd = desc_kmajor_sw128(b0 + ks * 32);
 #pragma unroll
             for (int b = 0; b < kB; ++b) {
+              if (b < b_lo || b >= b_hi) continue;
               const uint64_t ad = desc_kmajor_sw128(a0 + b * kWTileBytes + ks * 32);
-              const uint32_t d = d0 + b * kAccStride;
+              const uint32_t d = two_issuers ? my_tmem : d0 + b * kAccStride;
               if constexpr (kPair) {
-                if (p.fp8) mma_mxf8_pair(d, ad, bd, idesc, tmem + sfa_col + 4 * b, tmem + sfb_col, accum);
-                else mma_f16_pair(d, ad, bd, idesc, accum);
+                if (p.fp8) mma_mxf8_pair_e(e0, d, ad, bd, idesc, tmem + sfa_col + 4 * b, tmem + sfb_col, accum);
+                else mma_f16_pair_e(e0, d, ad, bd, idesc, accum);
               } else {
                 if (p.fp8)
-                  mma_mxf8(d, ad, bd, idesc | (kW4 ? (uint32_t)ks << 29 : 0u), tmem + sfa_col + 4 * b,
-                           tmem + sfb_col, accum);
-                else mma_f16(d, ad, bd, idesc, accum);
+                  mma_mxf8_e(e0, d, ad, bd, idesc | (kW4 ? (uint32_t)ks << 29 : 0u), my_sfa + 4 * (b - b_lo),
+                           my_sfb, accum);
+                else mma_f16_e(e0, d, ad, bd, idesc, accum);
               }
             }
           };
-#pragma unroll
-          for (int ks = 0; ks < 3; ++ks) kstep(ks, (kb | ks) != 0 ? 1u : 0u);
           const uint32_t nstage = stage + 1 == (uint32_t)S ? 0u : stage + 1;
           const uint32_t nphase = stage + 1 == (uint32_t)S ? phase ^ 1u : phase;
-          if (kb + 1 < KB && !ready(nstage, nphase))
-            ok = false;
-          kstep(3, 1u);
-          if constexpr (kPair) mma_commit_pair(&sh.empty[stage], 0x3);
-          else mma_commit(&sh.empty[stage]);
+          if constexpr (kB == 1 && !kPair) {
+            // one-block tiles: this thread's two K-steps of the stage
+            kstep(2 * me, kb != 0 ? 1u : 0u);
+            if (kb + 1 < KB && !ready(nstage, nphase))
+              ok = false;
+            kstep(2 * me + 1, 1u);
+          } else {
+#pragma unroll
+            for (int ks = 0; ks < 3; ++ks) kstep(ks, (kb | ks) != 0 ? 1u : 0u);
+            if (kb + 1 < KB && !ready(nstage, nphase))
+              ok = false;
+            kstep(3, 1u);
+          }
+          if constexpr (kPair) mma_commit_pair_e(e0, &sh.empty[stage], 0x3);
+          else mma_commit_e(e0, &sh.empty[stage]);
           stage = nstage;
           phase = nphase;
           if (!ok) break;
         }
         if (!ok) break;
-        if constexpr (kPair) mma_commit_pair(&sh.acc_full[acc], 0x3);
-        else mma_commit(&sh.acc_full[acc]);
+        if constexpr (kPair) mma_commit_pair_e(e0, &sh.acc_full[acc], 0x3);
+        else mma_commit_e(e0, &sh.acc_full[acc]);
         if (++acc == n_acc) {
           acc = 0;
           acc_phase ^= 1u;
@@ -762,10 +881,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       });
       // all tcgen05 work of the CTA (pair) completes before TMEM is released
-      if constexpr (kPair) mma_commit_pair(&sh.drain, 0x3);
-      else mma_commit(&sh.drain);
+      if constexpr (kPair) mma_commit_pair_e(e0, &sh.drain, 0x3);
+      else mma_commit_e(e0, &sh.drain);
     }
-    if (lane == 0 && S > 0) wait_drain(&sh.drain, 0, globaltimer_ns() + kDrainNs);
+    if (warp == 1 && lane == 0 && S > 0) wait_drain(&sh.drain, 0, globaltimer_ns() + kDrainNs);
     __syncwarp();
   } else if (warp == kSfWarp) {
     // ================================================= fp8 scale words
@@ -869,6 +988,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       });
     }
+  } else if (warp == kMma2Warp) {
+    // second MMA issuer: idle in a CTA pair
   } else {
     // ================================================= epilogue
     const uint32_t quad = warp & 3u;  // TMEM lanes this warp may access
@@ -884,12 +1005,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!warp_wait(&sh.acc_full[acc], acc_phase, deadline, &sh.abort_flag, p.status)) break;
       tc_fence_after();
       const uint32_t taddr = tmem + ((quad * 32u) << 16) + acc * kAccStride;
+      // block 1's accumulator (the up half of a SwiGLU tile)
+      const uint32_t taddr1 = two_issuers ? tacc1 + ((quad * 32u) << 16) : taddr + kAccStride;
+      bool released = false;  // this warp's arrival on acc_empty is made
       bool swiglu = false;
       if constexpr (kB == 2 && !kPair) swiglu = p.epi != kEpiPlain;
       if (swiglu) {
         if (p.epi == kEpiSwigluBf16) {
-          swiglu_bf16_tile(p, tl, taddr, quad, half, lane);
-        } else if (!swiglu_fp8_tile(p, sh, tl, taddr, quad, half, lane, tile_par, deadline)) {
+          swiglu_bf16_tile(p, tl, taddr, taddr1, quad, half, lane);
+        } else if (!swiglu_fp8_tile(p, sh, tl, taddr, taddr1, quad, half, lane, tile_par, deadline)) {
           break;
         }
         tile_par ^= 1u;
@@ -901,8 +1025,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int32_t c0 = 16 * half; c0 < tl.qn; c0 += 32) {
           uint32_t r[kB][16];
 #pragma unroll
-          for (int b = 0; b < kB; ++b) tmem_ld16(taddr + b * kAccStride + (uint32_t)c0, r[b]);
-          tmem_ld_wait();
+          for (int b = 0; b < kB; ++b) tmem_ld16((b == 0 ? taddr : taddr1) + (uint32_t)c0, r[b]);
+          if constexpr (kB == 1 && !kPair) {
+            // the two issuers' partial sums (K-steps 0-1 and 2-3 of every stage)
+            uint32_t r2[16];
+            tmem_ld16(taddr1 + (uint32_t)c0, r2);
+            tmem_ld_wait();
+            tmem_regs_ready(r[0]);
+            tmem_regs_ready(r2);
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              r[0][i] = __float_as_uint(__uint_as_float(r[0][i]) + __uint_as_float(r2[i]));
+          } else {
+            tmem_ld_wait();
+          }
 #pragma unroll
           for (int b = 0; b < kB; ++b) tmem_regs_ready(r[b]);
           // Lanes 2j and 2j+1 hold adjacent output columns.  One exchange per
@@ -922,11 +1058,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if constexpr (kPair) mbar_arrive_cluster(acc_empty0 + acc * (uint32_t)sizeof(uint64_t));
-        else mbar_arrive(&sh.acc_empty[acc]);
+      if (!released) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (kPair) mbar_arrive_cluster(acc_empty0 + acc * (uint32_t)sizeof(uint64_t));
+          else mbar_arrive(&sh.acc_empty[acc]);
+        }
       }
       if (++acc == n_acc) {
         acc = 0;
@@ -942,7 +1080,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     if constexpr (kPair) tmem_dealloc_pair(tmem, kTmemCols);
-    else tmem_dealloc(tmem, kTmemCols);
+    else tmem_dealloc(tmem, two_issuers ? 256u : kTmemCols);
+  }
+  if (two_issuers && warp == kMma2Warp) {
+    tc_fence_after();
+    tmem_dealloc(tacc1, 256u);
   }
 }
 
