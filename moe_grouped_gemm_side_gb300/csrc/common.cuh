@@ -388,6 +388,66 @@ __device__ __forceinline__ void tmem_cp_32x128b_x4_pair(uint32_t taddr, uint64_t
                : "memory");
 }
 
+// ------------------------------------------------------- predicated issue
+// The same tcgen05 instructions executed only where `e` is non-zero: a whole
+// warp runs an issue loop (its descriptors and addresses stay warp-uniform)
+// and one lane issues.
+__device__ __forceinline__ void mma_f16_e(uint32_t e, uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+      "@q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(e));
+}
+__device__ __forceinline__ void mma_mxf8_e(uint32_t e, uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %6, 0;\n\tsetp.ne.b32 q, %7, 0;\n\t"
+      "@q tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
+      " [%0], %1, %2, %3, [%4], [%5], p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate), "r"(e));
+}
+__device__ __forceinline__ void mma_f16_pair_e(uint32_t e, uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+      "@q tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(e));
+}
+__device__ __forceinline__ void mma_mxf8_pair_e(uint32_t e, uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %6, 0;\n\tsetp.ne.b32 q, %7, 0;\n\t"
+      "@q tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X"
+      " [%0], %1, %2, %3, [%4], [%5], p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate), "r"(e));
+}
+__device__ __forceinline__ void mma_commit_e(uint32_t e, uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %1, 0;\n\t"
+      "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}\n" ::"r"(
+          smem_u32(bar)), "r"(e)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit_pair_e(uint32_t e, uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t"
+      "@q tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;\n\t}\n" ::"r"(smem_u32(bar)), "h"(mask), "r"(e)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_cp_32x128b_x4_e(uint32_t e, uint32_t taddr, uint64_t sdesc) {
+  asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t"
+               "@q tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n\t}\n" ::"r"(taddr), "l"(sdesc), "r"(e)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_cp_32x128b_x4_pair_e(uint32_t e, uint32_t taddr, uint64_t sdesc) {
+  asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t"
+               "@q tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;\n\t}\n" ::"r"(taddr), "l"(sdesc), "r"(e)
+               : "memory");
+}
 // ------------------------------------------------ packed FP8 block scales
 // One 32-bit TMEM scale word per row carries the UE8M0 scales of four
 // consecutive 128-wide K-blocks (byte i = K-block kb0 + i); the MMA picks
