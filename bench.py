@@ -850,7 +850,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-config records")
     ap.add_argument("--reps", type=int, default=20, help="timed L2-flushed reps per config record")
-    ap.add_argument("--soak", type=float, default=2.0,
+    ap.add_argument("--soak", type=float, default=1.0,
                     help="seconds of back-to-back steps right before the timed region (clock record)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--config-cpu-budget", type=float, default=5.0,

@@ -380,14 +380,20 @@ int64_t mg_get_wait_limit_ns(void);
  * Kernel family for the contiguous and masked forms.  A tile is one or two
  * weight blocks against one token tile; a block is 128 weight rows on one SM
  * or 256 rows on the two SMs of a cluster sharing each MMA (cta_group::2).
- *   0 (default): single SM, two blocks when N % 256 == 0, one otherwise
- *      (the fastest family measured on GB300);
+ * Families 1-4 put the tokens on the MMA's N axis (token tiles up to 240
+ * rows for E4M3, 256 for bf16); family 5 puts them on its M axis (token
+ * tiles of up to 128 rows against 256 weight rows per MMA).
+ *   0 (default): contiguous form: SM pair, two blocks when N % 512 == 0,
+ *      else as 2; masked form and E2M1 weights: as 2 (the fastest families
+ *      measured on GB300 for prefill and decode shapes);
  *   1: single SM, one block (128 rows);
  *   2: single SM, two blocks (256 rows; needs N % 256 == 0);
  *   3: SM pair, one block (256 rows; needs N % 256 == 0);
- *   4: SM pair, two blocks (512 rows; needs N % 512 == 0).
+ *   4: SM pair, two blocks (512 rows; needs N % 512 == 0);
+ *   5: single SM, tokens on M, 256 weight rows (needs N % 256 == 0).
  * A family whose tile does not divide N falls back to the next narrower one
- * (4 -> 3 -> 1, 2 -> 1, 0 -> 1).  Results are identical up to fp32 summation order.
+ * (4 -> 3 -> 1, 2 -> 1, 5 -> 1, 0 -> 1).  Results are identical up to fp32
+ * summation order.
  * Process-wide.  Returns MG_ERR_INVALID_ARG for other values.
  * ------------------------------------------------------------------------ */
 mg_status mg_set_kernel_policy(int32_t policy);

@@ -64,9 +64,9 @@ SIGNATURES = {
 }
 
 # Kernel families of the contiguous and masked forms (mg_set_kernel_policy).
-POLICY_AUTO, POLICY_SINGLE, POLICY_DUAL, POLICY_PAIR, POLICY_PAIR_DUAL = 0, 1, 2, 3, 4
+POLICY_AUTO, POLICY_SINGLE, POLICY_DUAL, POLICY_PAIR, POLICY_PAIR_DUAL, POLICY_TOKM = 0, 1, 2, 3, 4, 5
 POLICIES = {"auto": POLICY_AUTO, "single": POLICY_SINGLE, "dual": POLICY_DUAL,
-            "pair": POLICY_PAIR, "pair_dual": POLICY_PAIR_DUAL}
+            "pair": POLICY_PAIR, "pair_dual": POLICY_PAIR_DUAL, "tokm": POLICY_TOKM}
 
 _LIB = None
 

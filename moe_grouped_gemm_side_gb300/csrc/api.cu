@@ -22,23 +22,30 @@ constexpr int64_t kDefaultWaitNs = 2000000000LL;
 std::atomic<int64_t> g_wait_ns{kDefaultWaitNs};
 std::atomic<int32_t> g_policy{0};
 
-// Kernel family for N.  Policy 0 (default) takes two 128-row weight blocks
-// per SM when N allows it: measured on GB300 it is the fastest family for
-// prefill and decode shapes alike (the SM-pair families lose on the
-// block-scaled fp8 path).  Policies 1-4 force single, dual, pair or
-// pair-dual, falling back to the widest family N allows when N is not a
-// multiple of the family's tile rows.
-int fwd_variant(int32_t N, bool w4 = false) {
+// Kernel family for N.  Policy 0 (default): for the contiguous form two
+// 256-row weight blocks per CTA pair (cta_group::2) when N % 512 == 0, else
+// two 128-row blocks on one SM; for the masked form two 128-row blocks on
+// one SM (their one-block split for decode-sized histograms).  Measured on
+// GB300 these are the fastest families for prefill and decode shapes; FP4
+// weights run on one SM.  (Tokens on the MMA's M axis halve the MMAs per
+// weight byte, but on the 16-expert decode its 224 tiles leave half the SMs
+// with two tiles and the others with one: no faster end to end.)  Policies
+// 1-5 force single, dual, pair, pair-dual or tokens-on-M, falling back to
+// the widest family N allows when N is not a multiple of the family's tile
+// rows.
+int fwd_variant(int32_t N, bool w4 = false, bool masked = false) {
   const int32_t pol = g_policy.load();
-  int v = pol == 0 ? kFwdDual : pol == 1 ? kFwdSingle : pol == 2 ? kFwdDual : pol == 3 ? kFwdPair : kFwdPairDual;
+  const int dflt = (!masked && !w4 && N % 512 == 0) ? kFwdPairDual : kFwdDual;
+  int v = pol == 0 ? dflt
+        : pol == 1 ? kFwdSingle : pol == 2 ? kFwdDual : pol == 3 ? kFwdPair : pol == 4 ? kFwdPairDual : kFwdTokM;
   if (w4 && (v == kFwdPair || v == kFwdPairDual)) v = kFwdDual;  // FP4 weights: single-SM families
   if (v == kFwdPairDual && N % 512 != 0) v = kFwdPair;
-  if ((v == kFwdPair || v == kFwdDual) && N % 256 != 0) v = kFwdSingle;
+  if ((v == kFwdPair || v == kFwdDual || v == kFwdTokM) && N % 256 != 0) v = kFwdSingle;
   return v;
 }
 
 cudaError_t launch_fwd_any(const FwdArgs& a, cudaStream_t s) {
-  return launch_fwd(a, s, fwd_variant(a.N, a.w4));
+  return launch_fwd(a, s, fwd_variant(a.N, a.w4, a.masked));
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -46,17 +53,26 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// The driver's tensor-map encoder, looked up once.  A failed lookup is not
+// cached: the first call of a process may come before this library's CUDA
+// runtime has a context, so the context is made current first (cudaFree of
+// nothing creates the device's primary context when there is none).
 EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = []() -> EncodeTiledFn {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      return nullptr;
-    return reinterpret_cast<EncodeTiledFn>(p);
-  }();
-  return fn;
+  static std::atomic<EncodeTiledFn> fn{nullptr};
+  EncodeTiledFn f = fn.load();
+  if (f != nullptr) return f;
+  (void)cudaFree(nullptr);
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+          cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || p == nullptr) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  f = reinterpret_cast<EncodeTiledFn>(p);
+  fn.store(f);
+  return f;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -483,7 +499,7 @@ mg_status mg_set_wait_limit_ns(int64_t ns) {
 int64_t mg_get_wait_limit_ns(void) { return g_wait_ns.load(); }
 
 mg_status mg_set_kernel_policy(int32_t policy) {
-  if (policy < 0 || policy > 4) return MG_ERR_INVALID_ARG;
+  if (policy < 0 || policy > 5) return MG_ERR_INVALID_ARG;
   g_policy.store(policy);
   return MG_OK;
 }

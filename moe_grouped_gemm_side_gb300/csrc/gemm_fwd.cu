@@ -240,8 +240,9 @@ __device__ __forceinline__ uint32_t group_weight_word(const uint32_t (&wsf)[4], 
   return w;
 }
 
-// kind::mxf8f6f4 instruction-descriptor A format E2M1 (FP4), bits 7-9.
+// kind::mxf8f6f4 instruction-descriptor A / B format E2M1 (FP4), bits 7-9 / 10-12.
 constexpr uint32_t kIdescAE2M1 = 5u << 7;
+constexpr uint32_t kIdescBE2M1 = 5u << 10;
 
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
@@ -401,7 +402,7 @@ __device__ __forceinline__ bool swiglu_fp8_tile(const Params& p, Shared& sh, con
   return true;
 }
 
-template <int kBlocks, bool kPair, bool kW4>
+template <int kBlocks, bool kPair, bool kW4, bool kTokM>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA64,
                const __grid_constant__ CUtensorMap tmA16, const __grid_constant__ CUtensorMap tmA8,
@@ -409,6 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                const Params p) {
   static_assert(kBlocks == 1 || kBlocks == 2, "one or two weight blocks per tile");
   static_assert(!(kW4 && kPair), "FP4 weights run on single-SM tiles");
+  static_assert(!kTokM || (kBlocks == 2 && !kPair), "tokens-on-M tiles: two blocks on one SM");
   constexpr int kBlockRows = kPair ? 2 * kCtaRows : kCtaRows;  // rows of one weight block (MMA M)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -438,7 +440,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // (sfb_col: after the block-1 weight words when tiles have two blocks)
   // widest token tile: 256, but 240 for fp8 wherever an accumulator shares
   // its 256 TMEM columns with the scale words
-  const int32_t q_cap = (p.fp8 && (kBlocks == 2 || !kPair)) ? 240 : 256;
+  // (tokens on M: the MMA's M, 128 rows)
+  const int32_t q_cap = kTokM ? 128 : (p.fp8 ? 240 : 256);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kMaxStages; ++i) {
@@ -455,9 +458,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 4; ++i) mbar_init(&sh.sf_grp[i], 2);
     sh.abort_flag = 0;
     fence_barrier_init();
-  }
-  if constexpr (kPair) {
-    if (warp == 1) tmem_alloc_pair(&sh.tmem_base, kTmemCols);
   }
 
   // ---- validated counts
@@ -515,6 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // decode case took the widest tile before; the priced choice, 128 on the
     // decode histogram, measured 8 % faster: the widest expert splits and
     // the narrower ring stages leave room for more of them).
+    if (kTokM && q == 0) q = 128;  // the MMA computes 128 token rows whatever the tile
     if (q == 0) {
       int64_t tiles[kNumTileCand];
 #pragma unroll
@@ -533,7 +534,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // not fill two waves of workers: with few tiles (decode) the finer
     // split balances the SMs, which all stream weights from DRAM then.
     int32_t nblk = kBlocks;
-    if (kBlocks == 2 && p.epi == kEpiPlain && want_blocks != 0) {
+    if (kTokM) {
+      // tokens on M: a tile is always 256 weight rows (the MMA's N)
+    } else if (kBlocks == 2 && p.epi == kEpiPlain && want_blocks != 0) {
       nblk = want_blocks;
     } else if (kBlocks == 2 && p.epi == kEpiPlain) {  // a SwiGLU epilogue needs gate and up in one tile
       int64_t tt = 0;
@@ -565,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // by decreasing width (ties: lower expert first).  Built the same way
     // in every CTA (warp scans and ballots, no atomics).
     const int32_t T_tok = carry / NB;
-    const int32_t bal = (nblk == 1 && T_tok <= kBalMax) ? 1 : 0;
+    const int32_t bal = ((nblk == 1 || kTokM) && T_tok <= kBalMax) ? 1 : 0;
     if (bal) {
       int32_t fcarry = 0;
       for (int32_t b = 0; b < E; b += 32) {
@@ -605,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       sh.nblk = nblk;
       // one commit per MMA-issuing thread frees a stage, fills an
       // accumulator and drains the CTA's tensor work
-      const uint32_t issuers = !kPair ? 2u : 1u;
+      const uint32_t issuers = kTokM ? 1u : 2u;
       for (int i = 0; i < kMaxStages; ++i) mbar_init(&sh.empty[i], issuers);
       for (int i = 0; i < 2; ++i) mbar_init(&sh.acc_full[i], issuers);
       mbar_init(&sh.drain, issuers);
@@ -618,12 +621,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   // for one-block tiles), each into a 256-column TMEM allocation of its own:
   // its accumulator at columns 0-239 (bf16: 0-255) and the scale words its
   // MMAs read at 240-251.  A CTA pair keeps one 512-column allocation.
-  const bool two_issuers = !kPair;
+  // Tokens on M: one issuer; its accumulator fills 256 columns and the scale
+  // words follow at 256-267.
+  const bool two_issuers = !kTokM;
   if constexpr (!kPair) {
     if (warp == 1) tmem_alloc_keep_permit(&sh.tmem_base, two_issuers ? 256u : kTmemCols);
     if (two_issuers && warp == kMma2Warp) tmem_alloc_keep_permit(&sh.tmem_base2, 256u);
     __syncthreads();
     if (warp == 1) tmem_relinquish();
+  } else {
+    // pair allocations are made by one warp in each CTA; one at a time, so
+    // both CTAs pair up the same two requests
+    cluster_sync();
+    if (warp == 1) tmem_alloc_pair_keep_permit(&sh.tmem_base, 256u);
+    cluster_sync();
+    if (warp == kMma2Warp) tmem_alloc_pair_keep_permit(&sh.tmem_base2, 256u);
+    cluster_sync();
+    if (warp == 1) tmem_relinquish_pair();
   }
   tc_fence_after();
   // barriers of both CTAs are initialised before any cross-CTA traffic
@@ -647,7 +661,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   };
   // token rows this CTA stages per tile: all of them, or its half of a pair
-  const int32_t stage_bytes = nblk * kWTileBytes + (kPair ? sh.qn_max / 2 : sh.qn_max) * kRowBytes;
+  const int32_t stage_bytes =
+      nblk * kWTileBytes + (kTokM ? 128 : (kPair ? sh.qn_max / 2 : sh.qn_max)) * kRowBytes;
   const int32_t sf_bytes = p.fp8 ? kSfStage + (kW4 ? kWsfArea : 0) : 0;
   const int32_t avail = kSmemBytes - 1024 - (int32_t)(reinterpret_cast<uintptr_t>(sf_area) -
                                                      reinterpret_cast<uintptr_t>(smem)) - 1024;
@@ -781,6 +796,67 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto ready = [&](uint32_t st, uint32_t ph) {
         return wait_bounded(&sh.full[st], ph, deadline, &sh.abort_flag, p.status);
       };
+      if constexpr (kTokM) {
+        // Tokens on M (one issuer): D[token, weight row] += A[token, k] W[row, k]
+        // with M = 128 token rows (rows past the tile's tokens hold stale
+        // data; their output rows are never stored) and N = 256 weight rows,
+        // so one MMA covers both weight blocks: half the MMAs per weight
+        // byte of the swapped layout, which on decode-sized token tiles is
+        // bound by MMA issue, not by the narrow token dimension.  Scale
+        // words: tokens at column 256 (A), weights at 260-267 (B: block 0,
+        // then block 1).
+        const uint32_t sf_tok = tmem + 256u, sf_w = tmem + 260u;
+        uint32_t stage = 0, phase = 0, acc_phase = 0;
+        bool ok = true;
+        const uint32_t idesc0 = p.fp8 ? (idesc_mxf8(128, 256) | (kW4 ? kIdescBE2M1 : 0u)) : idesc_bf16(128, 256, 0, 0);
+        for (int32_t t = unit; ok && t < total; t += n_units) {
+          if (!wait_bounded(&sh.acc_empty[0], acc_phase ^ 1u, deadline, &sh.abort_flag, p.status)) break;
+          tc_fence_after();
+          if (!ready(stage, phase)) break;
+#pragma unroll 2
+          for (int32_t kb = 0; kb < KB; ++kb) {
+            uint8_t* sw = ring + (size_t)stage * stage_bytes;
+            const uint32_t w0 = smem_u32(sw), a0 = smem_u32(sw + 2 * kWTileBytes);
+            const uint32_t sid = (uint32_t)(kb & 3);
+            // token scales: byte kb & 3 of their word (A scale id); E4M3
+            // weights the same byte of theirs, E2M1 weights byte ks of the
+            // stage's atom (B scale id)
+            const uint32_t idesc = p.fp8 ? (idesc0 | (sid << 29) | (kW4 ? 0u : (sid << 4))) : idesc0;
+            if (kW4) {
+              const uint32_t atoms = smem_u32(sf_area + (size_t)stage * sf_bytes + kSfStage + 2 * kWsfBytes);
+              tmem_cp_32x128b_x4_e(e0, sf_w, desc_sf_32x16(atoms));
+              tmem_cp_32x128b_x4_e(e0, sf_w + 4, desc_sf_32x16(atoms + kWsfAtom));
+            }
+            if (p.fp8 && sid == 0) {
+              const uint32_t sfs = smem_u32(sf_area + (size_t)stage * sf_bytes);
+              tmem_cp_32x128b_x4_e(e0, sf_tok, desc_sf_32x16(sfs + kSfRaw + 512));
+              if (!kW4) {
+                tmem_cp_32x128b_x4_e(e0, sf_w, desc_sf_32x16(sfs + kSfRaw));
+                tmem_cp_32x128b_x4_e(e0, sf_w + 4, desc_sf_32x16(sfs + kSfW1));
+              }
+            }
+            auto kstep = [&](int ks, uint32_t accum) {
+              const uint64_t ad = desc_kmajor_sw128(a0 + ks * 32), bd = desc_kmajor_sw128(w0 + ks * 32);
+              if (p.fp8) mma_mxf8_e(e0, tmem, ad, bd, idesc | (kW4 ? (uint32_t)ks << 4 : 0u), sf_tok, sf_w, accum);
+              else mma_f16_e(e0, tmem, ad, bd, idesc, accum);
+            };
+#pragma unroll
+            for (int ks = 0; ks < 3; ++ks) kstep(ks, (kb | ks) != 0 ? 1u : 0u);
+            const uint32_t nstage = stage + 1 == (uint32_t)S ? 0u : stage + 1;
+            const uint32_t nphase = stage + 1 == (uint32_t)S ? phase ^ 1u : phase;
+            if (kb + 1 < KB && !ready(nstage, nphase)) ok = false;
+            kstep(3, 1u);
+            mma_commit_e(e0, &sh.empty[stage]);
+            stage = nstage;
+            phase = nphase;
+            if (!ok) break;
+          }
+          if (!ok) break;
+          mma_commit_e(e0, &sh.acc_full[0]);
+          acc_phase ^= 1u;
+        }
+        mma_commit_e(e0, &sh.drain);
+      } else {
       // this thread's TMEM: its accumulator(s) and scale-word columns
       const uint32_t my_tmem = me == 0 ? tmem : tacc1;
       const uint32_t my_sfa = two_issuers ? my_tmem + 240u : tmem + sfa_col;  // + 4 b: block b's words
@@ -836,10 +912,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
               }
               ++grp;
-              tmem_cp_32x128b_x4_pair_e(e0, tmem + sfa_col, desc_sf_32x16(sfs + kSfRaw));
-              if (kB == 2) tmem_cp_32x128b_x4_pair_e(e0, tmem + sfa_col + 4, desc_sf_32x16(sfs + kSfW1));
-              tmem_cp_32x128b_x4_pair_e(e0, tmem + sfb_col, desc_sf_32x16(sfs + kSfRaw + 512));
-              if (qn > 128) tmem_cp_32x128b_x4_pair_e(e0, tmem + sfb_col + 4, desc_sf_32x16(sfs + kSfRaw + 1024));
+              for (int b = b_lo; b < b_hi; ++b)
+                tmem_cp_32x128b_x4_pair_e(e0, my_sfa + 4 * (b - b_lo), desc_sf_32x16(sfs + (b == 0 ? kSfRaw : kSfW1)));
+              tmem_cp_32x128b_x4_pair_e(e0, my_sfb, desc_sf_32x16(sfs + kSfRaw + 512));
+              if (qn > 128) tmem_cp_32x128b_x4_pair_e(e0, my_sfb + 4, desc_sf_32x16(sfs + kSfRaw + 1024));
             } else {
               if (!kW4) {
                 // weight words of block b: at kSfRaw (block 0) or kSfW1 (block 1)
@@ -858,7 +934,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint64_t ad = desc_kmajor_sw128(a0 + b * kWTileBytes + ks * 32);
               const uint32_t d = two_issuers ? my_tmem : d0 + b * kAccStride;
               if constexpr (kPair) {
-                if (p.fp8) mma_mxf8_pair_e(e0, d, ad, bd, idesc, tmem + sfa_col + 4 * b, tmem + sfb_col, accum);
+                if (p.fp8) mma_mxf8_pair_e(e0, d, ad, bd, idesc, my_sfa + 4 * (b - b_lo), my_sfb, accum);
                 else mma_f16_pair_e(e0, d, ad, bd, idesc, accum);
               } else {
                 if (p.fp8)
@@ -870,7 +946,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           };
           const uint32_t nstage = stage + 1 == (uint32_t)S ? 0u : stage + 1;
           const uint32_t nphase = stage + 1 == (uint32_t)S ? phase ^ 1u : phase;
-          if constexpr (kB == 1 && !kPair) {
+          if constexpr (kB == 1) {
             // one-block tiles: this thread's two K-steps of the stage
             kstep(2 * me, kb != 0 ? 1u : 0u);
             if (kb + 1 < KB && !ready(nstage, nphase))
@@ -901,6 +977,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // all tcgen05 work of the CTA (pair) completes before TMEM is released
       if constexpr (kPair) mma_commit_pair_e(e0, &sh.drain, 0x3);
       else mma_commit_e(e0, &sh.drain);
+      }
     }
     if (warp == 1 && lane == 0 && S > 0) wait_drain(&sh.drain, 0, globaltimer_ns() + kDrainNs);
     __syncwarp();
@@ -1027,8 +1104,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t taddr1 = two_issuers ? tacc1 + ((quad * 32u) << 16) : taddr + kAccStride;
       bool released = false;  // this warp's arrival on acc_empty is made
       bool swiglu = false;
-      if constexpr (kB == 2 && !kPair) swiglu = p.epi != kEpiPlain;
-      if (swiglu) {
+      if constexpr (kB == 2 && !kPair && !kTokM) swiglu = p.epi != kEpiPlain;
+      if constexpr (kTokM) {
+        // Tokens on M: TMEM lane = the tile's token, column = weight row, so
+        // each thread holds one output row; the two warps of a lane quadrant
+        // take 128 of the 256 columns each and store 16 bytes at a time.
+        const int32_t tok = (int32_t)(quad * 32u + lane);
+        const int32_t c_lo = 128 * half;
+        __nv_bfloat16* drow = static_cast<__nv_bfloat16*>(p.D) + (int64_t)(tl.row0 + tok) * p.N +
+                              tl.nb * (2 * kCtaRows) + c_lo;
+#pragma unroll
+        for (int c = 0; c < 128; c += 32) {
+          uint32_t r0[16], r1[16];
+          tmem_ld16(taddr + (uint32_t)(c_lo + c), r0);
+          tmem_ld16(taddr + (uint32_t)(c_lo + c + 16), r1);
+          tmem_ld_wait();
+          tmem_regs_ready(r0);
+          tmem_regs_ready(r1);
+          uint32_t v[16];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const __nv_bfloat162 a = __floats2bfloat162_rn(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]));
+            const __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1]));
+            v[i] = *reinterpret_cast<const uint32_t*>(&a);
+            v[8 + i] = *reinterpret_cast<const uint32_t*>(&b);
+          }
+          if (tok < tl.rows) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              *reinterpret_cast<uint4*>(drow + c + 8 * j) = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          }
+        }
+      } else if (swiglu) {
         if (p.epi == kEpiSwigluBf16) {
           swiglu_bf16_tile(p, tl, taddr, taddr1, quad, half, lane);
         } else if (!swiglu_fp8_tile(p, sh, tl, taddr, taddr1, quad, half, lane, tile_par, deadline)) {
@@ -1044,7 +1151,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t r[kB][16];
 #pragma unroll
           for (int b = 0; b < kB; ++b) tmem_ld16((b == 0 ? taddr : taddr1) + (uint32_t)c0, r[b]);
-          if constexpr (kB == 1 && !kPair) {
+          if constexpr (kB == 1) {
             // the two issuers' partial sums (K-steps 0-1 and 2-3 of every stage)
             uint32_t r2[16];
             tmem_ld16(taddr1 + (uint32_t)c0, r2);
@@ -1097,29 +1204,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   if constexpr (kPair) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    if constexpr (kPair) tmem_dealloc_pair(tmem, kTmemCols);
+    if constexpr (kPair) tmem_dealloc_pair(tmem, 256u);
     else tmem_dealloc(tmem, two_issuers ? 256u : kTmemCols);
   }
+  // a pair's two deallocations, like its allocations, one at a time
+  if constexpr (kPair) cluster_sync();
   if (two_issuers && warp == kMma2Warp) {
     tc_fence_after();
-    tmem_dealloc(tacc1, 256u);
+    if constexpr (kPair) tmem_dealloc_pair(tacc1, 256u);
+    else tmem_dealloc(tacc1, 256u);
   }
 }
 
-template <int kBlocks, bool kPair, bool kW4>
+template <int kBlocks, bool kPair, bool kW4, bool kTokM = false>
 cudaError_t launch(const FwdArgs& a, cudaStream_t s) {
   static bool attr_done[64] = {};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
-  auto kernel = fwd_kernel<kBlocks, kPair, kW4>;
+  auto kernel = fwd_kernel<kBlocks, kPair, kW4, kTokM>;
   if (dev < 64 && !attr_done[dev]) {
     err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (err != cudaSuccess) return err;
     attr_done[dev] = true;
   }
   // the SwiGLU epilogue pairs the two blocks of a single-SM tile
-  if (a.epi != kEpiPlain && (kBlocks != 2 || kPair)) return cudaErrorInvalidValue;
+  if (a.epi != kEpiPlain && (kBlocks != 2 || kPair || kTokM)) return cudaErrorInvalidValue;
   if (a.w4 != kW4) return cudaErrorInvalidValue;
   Params p;
   p.counts = a.counts;
@@ -1163,6 +1273,7 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s, int variant) {
     switch (variant) {
       case kFwdSingle: return fwd::launch<1, false, true>(a, s);
       case kFwdDual: return fwd::launch<2, false, true>(a, s);
+      case kFwdTokM: return fwd::launch<2, false, true, true>(a, s);
       default: return cudaErrorInvalidValue;
     }
   }
@@ -1171,6 +1282,7 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s, int variant) {
     case kFwdDual: return fwd::launch<2, false, false>(a, s);
     case kFwdPair: return fwd::launch<1, true, false>(a, s);
     case kFwdPairDual: return fwd::launch<2, true, false>(a, s);
+    case kFwdTokM: return fwd::launch<2, false, false, true>(a, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -96,6 +96,7 @@ enum FwdVariant : int {
   kFwdDual = 1,      // one CTA: 256 weight rows x q tokens (N % 256 == 0)
   kFwdPair = 2,      // CTA pair: 256 weight rows x q tokens, q/2 staged per SM (N % 256 == 0)
   kFwdPairDual = 3,  // CTA pair: 512 weight rows x q tokens, q/2 staged per SM (N % 512 == 0)
+  kFwdTokM = 4,      // one CTA, tokens on the MMA's M: 128 tokens x 256 weight rows (N % 256 == 0)
 };
 MG_HD int fwd_tile_rows(int variant) {
   return variant == kFwdSingle ? 128 : variant == kFwdPairDual ? 512 : 256;
@@ -107,6 +108,8 @@ MG_HD int fwd_tile_rows(int variant) {
 // one SM; ties go to the larger tile.
 MG_HD int pick_tile(bool fp8, const int64_t (&token_tiles)[kNumTileCand], int variant, int64_t N,
                     int64_t KB, int num_sms) {
+  // tokens on M: the MMA computes 128 token rows whatever the tile
+  if (variant == kFwdTokM) return 128;
   const bool pair = variant == kFwdPair || variant == kFwdPairDual;
   const int64_t NB = N / fwd_tile_rows(variant);
   const int workers = pair ? (num_sms >= 2 ? num_sms / 2 : 1) : num_sms;

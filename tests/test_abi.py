@@ -272,9 +272,9 @@ def test_wait_limit_setting(lib):
 def test_kernel_policy_setting(lib):
     assert lib.mg_get_kernel_policy() == 0
     try:
-        for v in (1, 2, 3, 4, 0):
+        for v in (1, 2, 3, 4, 5, 0):
             assert lib.mg_set_kernel_policy(v) == 0 and lib.mg_get_kernel_policy() == v
-        assert lib.mg_set_kernel_policy(5) == 1 and lib.mg_get_kernel_policy() == 0
+        assert lib.mg_set_kernel_policy(6) == 1 and lib.mg_get_kernel_policy() == 0
         assert lib.mg_set_kernel_policy(-1) == 1 and lib.mg_get_kernel_policy() == 0
     finally:
         lib.mg_set_kernel_policy(0)

@@ -11,11 +11,12 @@ from tests import gpu_util as gu
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(autouse=True, params=["auto", "single", "dual", "pair", "pair_dual"])
+@pytest.fixture(autouse=True, params=["auto", "single", "dual", "pair", "pair_dual", "tokm"])
 def kernel_policy(request, lib):
     """Run every case on every kernel family: one or two weight blocks per
-    tile, on one SM or on a CTA pair sharing each MMA.  A family whose tile
-    does not divide N falls back to a narrower one."""
+    tile, on one SM or on a CTA pair sharing each MMA, tokens on the MMA's
+    N or M axis.  A family whose tile does not divide N falls back to a
+    narrower one."""
     mb.set_kernel_policy(mb.POLICIES[request.param])
     yield request.param
     mb.set_kernel_policy(mb.POLICY_AUTO)

@@ -68,7 +68,7 @@ def test_contiguous_integer_exact(lib, cuda, tile_q):
     assert (Dbits[~written] == gu.SENTINEL_BITS).all()
 
 
-@pytest.mark.parametrize("policy", ["single", "dual", "pair", "pair_dual"])
+@pytest.mark.parametrize("policy", ["single", "dual", "pair", "pair_dual", "tokm"])
 def test_every_policy_runs_single_sm_families(lib, cuda, policy):
     """FP4 weights use the single-SM families; the pair policies fall back."""
     counts = [3, 250, 0, 64]
