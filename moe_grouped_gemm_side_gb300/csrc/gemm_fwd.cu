@@ -87,6 +87,10 @@ constexpr int kWsfArea = 2 * kWsfBytes + 2 * kWsfAtom;
 static_assert(kSfStage % 1024 == 0 && kWsfBytes % 1024 == 0 && kWsfAtom % 16 == 0,
               "TMA and tcgen05.cp sources stay aligned");
 constexpr int kGroupTiles = 8;                   // token tiles per raster group
+// CTA pairs, fp8: slots of the ring of scale groups (raw token scales and
+// scale words of four K-blocks each), loaded one group ahead of the stage
+// that consumes them
+constexpr int kGRing = 8;
 // Launches with one-block tiles and at most this many token tiles deal their
 // tiles by cost (see balanced_position)
 constexpr int kBalMax = 512;
@@ -95,7 +99,6 @@ constexpr int kBalMax = 512;
 // thread has read it.
 constexpr int kInfoRing = 32;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAccStride = 256;             // TMEM columns between accumulators
 constexpr int kSmemBytes = 227 * 1024;
 constexpr uint64_t kDrainNs = 200ull * 1000 * 1000;
 
@@ -118,8 +121,8 @@ struct Shared {
   uint64_t full[kMaxStages];      // operand bytes (of both CTAs of a pair) landed
   uint64_t empty[kMaxStages];     // the MMAs reading the stage are done
   uint64_t sf_full[kMaxStages];   // fp8: this CTA's raw scale bytes of the stage landed
-  uint64_t acc_full[2];
-  uint64_t acc_empty[2];
+  uint64_t acc_full[1];
+  uint64_t acc_empty[1];
   uint64_t drain;
   uint32_t tmem_base;
   uint32_t tmem_base2;  // two issuers: block 1's own TMEM allocation
@@ -134,9 +137,10 @@ struct Shared {
   // tokens, exchanged between the four epilogue warps of one half
   uint64_t amax_bar[2];
   float amax[4][256];
-  // pairs, fp8: a group of four K-blocks' scale words built in both CTAs
-  // (indexed by group & 3, phase = (group >> 2) & 1)
-  uint64_t sf_grp[4];
+  // pairs, fp8: group slot s of the scale ring: raw bytes landed (g_full),
+  // words built in both CTAs (sf_grp, on the first CTA)
+  uint64_t g_full[kGRing];
+  uint64_t sf_grp[kGRing];
 };
 
 struct Tile {
@@ -433,11 +437,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint64_t deadline = globaltimer_ns() + (uint64_t)p.wait_ns;
   const int32_t NB128 = p.N / kCtaRows;
   const int32_t KB = p.K / (p.fp8 ? 128 : 64);
-  // TMEM: accumulator(s) at columns 0 and 256; fp8 scale words after the
-  // last accumulator: weight words of each block (4 columns each), then the
-  // token words (8 columns).
-  const uint32_t sfa_col = 496u;
-  // (sfb_col: after the block-1 weight words when tiles have two blocks)
   // widest token tile: 256, but 240 for fp8 wherever an accumulator shares
   // its 256 TMEM columns with the scale words
   // (tokens on M: the MMA's M, 128 rows)
@@ -450,12 +449,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sh.full[i], (!kPair && p.fp8) ? 2 : 1);
       mbar_init(&sh.sf_full[i], 1);
     }
-    for (int i = 0; i < 2; ++i)
-      mbar_init(&sh.acc_empty[i], kEpiWarps * (kPair ? 2 : 1));  // one arrival per epilogue warp
+    mbar_init(&sh.acc_empty[0], kEpiWarps * (kPair ? 2 : 1));  // one arrival per epilogue warp
     // (empty, acc_full and drain count one commit per MMA-issuing thread:
     // initialised once the block count of the launch is known)
     for (int i = 0; i < 2; ++i) mbar_init(&sh.amax_bar[i], 4 * 32);
-    for (int i = 0; i < 4; ++i) mbar_init(&sh.sf_grp[i], 2);
+    for (int i = 0; i < kGRing; ++i) {
+      mbar_init(&sh.sf_grp[i], 2);
+      mbar_init(&sh.g_full[i], 1);
+    }
     sh.abort_flag = 0;
     fence_barrier_init();
   }
@@ -610,7 +611,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // accumulator and drains the CTA's tensor work
       const uint32_t issuers = kTokM ? 1u : 2u;
       for (int i = 0; i < kMaxStages; ++i) mbar_init(&sh.empty[i], issuers);
-      for (int i = 0; i < 2; ++i) mbar_init(&sh.acc_full[i], issuers);
+      mbar_init(&sh.acc_full[0], issuers);
       mbar_init(&sh.drain, issuers);
       fence_barrier_init();
     }
@@ -620,7 +621,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // two-block tiles, of the first and the last two K-steps of every stage
   // for one-block tiles), each into a 256-column TMEM allocation of its own:
   // its accumulator at columns 0-239 (bf16: 0-255) and the scale words its
-  // MMAs read at 240-251.  A CTA pair keeps one 512-column allocation.
+  // MMAs read at 240-251.  A CTA pair makes the same two allocations in
+  // each of its CTAs (cta_group::2), one at a time.
   // Tokens on M: one issuer; its accumulator fills 256 columns and the scale
   // words follow at 256-267.
   const bool two_issuers = !kTokM;
@@ -650,7 +652,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int32_t bal = sh.bal;
   const int32_t NB = p.N / (nblk * kBlockRows);  // tiles per token tile
   const int32_t tile_rows = nblk * kBlockRows;
-  const uint32_t sfb_col = nblk == 2 ? 504u : 500u;
   // Runs body with the launch's block count as a compile-time constant.
   auto with_blocks = [&](auto&& body) {
     if constexpr (kBlocks == 2) {
@@ -663,20 +664,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   // token rows this CTA stages per tile: all of them, or its half of a pair
   const int32_t stage_bytes =
       nblk * kWTileBytes + (kTokM ? 128 : (kPair ? sh.qn_max / 2 : sh.qn_max)) * kRowBytes;
-  const int32_t sf_bytes = p.fp8 ? kSfStage + (kW4 ? kWsfArea : 0) : 0;
+  // scale data: per stage on one SM; a ring of groups for a pair
+  const bool gring = kPair && p.fp8;
+  const int32_t sf_bytes = (p.fp8 && !kPair) ? kSfStage + (kW4 ? kWsfArea : 0) : 0;
+  const int32_t grp_area = gring ? kGRing * kSfStage : 0;
+  uint8_t* gbuf = sf_area;
   const int32_t avail = kSmemBytes - 1024 - (int32_t)(reinterpret_cast<uintptr_t>(sf_area) -
-                                                     reinterpret_cast<uintptr_t>(smem)) - 1024;
+                                                     reinterpret_cast<uintptr_t>(smem)) - 1024 - grp_area;
   int32_t S = avail / (stage_bytes + sf_bytes);
   S = min(S, kMaxStages);
   uint8_t* ring = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(sf_area) + (uintptr_t)S * sf_bytes + 1023) & ~uintptr_t(1023));
-  // accumulator sets: two (double buffered) with one block, unless fp8 scale
-  // words need the columns; one with two blocks
-  const uint32_t n_acc = (!two_issuers && nblk == 1 && (!p.fp8 || sh.qn_max <= 240)) ? 2u : 1u;
+      (reinterpret_cast<uintptr_t>(sf_area) + (uintptr_t)grp_area + (uintptr_t)S * sf_bytes + 1023) &
+      ~uintptr_t(1023));
+  const int32_t NG = (KB + kSfGroup - 1) / kSfGroup;   // scale groups per tile
+  // one accumulator per issuer: the tile's next MMAs wait for the epilogue
+  // to drain it
   const uint32_t tmem = sh.tmem_base;
-  // block b's accumulator for accumulator set 0 (set a adds a * kAccStride
-  // where a tile has one block)
-  const uint32_t tacc1 = two_issuers ? sh.tmem_base2 : tmem + kAccStride;
+  // the second issuer's allocation (block 1, or the last two K-steps)
+  const uint32_t tacc1 = sh.tmem_base2;
 
   if (warp == 0) {
     // ================================================= TMA producer
@@ -689,6 +694,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (kW4) tma_prefetch_desc(&tmSFW);
       uint32_t stage = 0, phase = 0;
       int64_t issued = 0;
+      int64_t gload = 0;  // pairs, fp8: scale groups loaded into the ring
+      auto load_group = [&](const Tile& gt, int32_t g) {
+        const uint32_t slot = (uint32_t)(gload % kGRing);
+        mbar_arrive_expect_tx(&sh.g_full[slot], (uint32_t)kSfRaw);
+        tma_load_3d(gbuf + (size_t)slot * kSfStage, &tmSF, &sh.g_full[slot], gt.sf_x, g * kSfGroup, gt.sf_z);
+        ++gload;
+      };
       bool ok = true;
       // The next tile is decoded right after the current tile's first stage
       // is issued, while the thread would wait for a free slot anyway.
@@ -719,7 +731,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // The raw scale bytes have a barrier of their own and are issued
           // first: the 1 KB lands well before the operands, so warp 6 builds
           // the scale words while the operands are still in flight.
-          if (p.fp8) {
+          if (p.fp8 && !gring) {
             uint8_t* sfs = sf_area + (size_t)stage * sf_bytes;
             // FP4 weights: every stage loads each block's scale box of its
             // group of four K-blocks (16 bytes per row: the TMA minimum)
@@ -755,6 +767,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (kb == 0 && t + n_units < total) nxt = decode_tile(t + n_units, tpre, cnt, rowbase, E, NB, q, p.masked, ttab, bal, total, n_units);
+          if (gring && (kb % kSfGroup) == 0) {
+            // a pair's scale groups run one group ahead of their first stage:
+            // the words then reach both CTAs' shared memory well before the
+            // copies that read them (loaded with the stage, the handshake
+            // between the pair's scale warps delayed every fourth stage by
+            // ~700 cycles)
+            const int32_t g = kb / kSfGroup;
+            if (gload == 0) load_group(tl, 0);
+            if (g + 1 < NG) load_group(tl, g + 1);
+            else if (t + n_units < total) load_group(nxt, 0);
+          }
           ++issued;
           if (++stage == (uint32_t)S) {
             stage = 0;
@@ -768,8 +791,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dl = globaltimer_ns() + kDrainNs;
       for (int64_t i = issued > S ? issued - S : 0; i < issued; ++i) {
         if (leader) wait_drain(&sh.full[i % S], (uint32_t)((i / S) & 1), dl);
-        if (p.fp8) wait_drain(&sh.sf_full[i % S], (uint32_t)((i / S) & 1), dl);
+        if (p.fp8 && !gring) wait_drain(&sh.sf_full[i % S], (uint32_t)((i / S) & 1), dl);
       }
+      for (int64_t i = gload > kGRing ? gload - kGRing : 0; i < gload; ++i)
+        wait_drain(&sh.g_full[i % kGRing], (uint32_t)((i / kGRing) & 1), dl);
       if (kPair && !ok) {
         // give the second CTA's operand copies still in flight time to land
         const uint64_t until = globaltimer_ns() + 100000ull;
@@ -859,21 +884,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
       // this thread's TMEM: its accumulator(s) and scale-word columns
       const uint32_t my_tmem = me == 0 ? tmem : tacc1;
-      const uint32_t my_sfa = two_issuers ? my_tmem + 240u : tmem + sfa_col;  // + 4 b: block b's words
-      const uint32_t my_sfb = two_issuers ? my_tmem + 244u : tmem + sfb_col;
+      const uint32_t my_sfa = my_tmem + 240u;  // weight words
+      const uint32_t my_sfb = my_tmem + 244u;  // token words
       uint32_t grp = 0;  // pairs: groups of scale words consumed
       with_blocks([&](auto bc) {
       constexpr int kB = decltype(bc)::value;
       // blocks this thread issues: all kB, or block `me` alone
-      const int b_lo = (two_issuers && kB == 2) ? me : 0, b_hi = (two_issuers && kB == 2) ? me + 1 : kB;
-      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      const int b_lo = kB == 2 ? me : 0, b_hi = kB == 2 ? me + 1 : kB;
+      uint32_t stage = 0, phase = 0, acc_phase = 0;
       bool ok = true;
       for (int32_t t = unit, ti = 0; ok && t < total; t += n_units, ++ti) {
-        if (!wait_bounded(&sh.acc_empty[acc], acc_phase ^ 1u, deadline, &sh.abort_flag, p.status)) break;
+        if (!wait_bounded(&sh.acc_empty[0], acc_phase ^ 1u, deadline, &sh.abort_flag, p.status)) break;
         tc_fence_after();
-        // block b accumulates at d0 + b * kAccStride (one allocation), or at
-        // the start of this thread's own allocation (two issuers)
-        const uint32_t d0 = tmem + acc * kAccStride;
         // The wait for stage kb+1 sits between the third and the fourth
         // K-step of stage kb, so the tensor pipe holds queued work while the
         // thread waits.  No tcgen05 fence follows the stage waits: the
@@ -905,9 +927,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (p.fp8 && sid == 0) {
-            const uint32_t sfs = smem_u32(sf_area + (size_t)stage * sf_bytes);
             if constexpr (kPair) {
-              if (!wait_bounded(&sh.sf_grp[grp & 3], (grp >> 2) & 1, deadline, &sh.abort_flag, p.status)) {
+              const uint32_t slot = grp % kGRing;
+              const uint32_t sfs = smem_u32(gbuf + (size_t)slot * kSfStage);
+              if (!wait_bounded(&sh.sf_grp[slot], (grp / kGRing) & 1, deadline, &sh.abort_flag, p.status)) {
                 ok = false;
                 break;
               }
@@ -917,6 +940,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               tmem_cp_32x128b_x4_pair_e(e0, my_sfb, desc_sf_32x16(sfs + kSfRaw + 512));
               if (qn > 128) tmem_cp_32x128b_x4_pair_e(e0, my_sfb + 4, desc_sf_32x16(sfs + kSfRaw + 1024));
             } else {
+              const uint32_t sfs = smem_u32(sf_area + (size_t)stage * sf_bytes);
               if (!kW4) {
                 // weight words of block b: at kSfRaw (block 0) or kSfW1 (block 1)
                 for (int b = b_lo; b < b_hi; ++b)
@@ -932,7 +956,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int b = 0; b < kB; ++b) {
               if (b < b_lo || b >= b_hi) continue;
               const uint64_t ad = desc_kmajor_sw128(a0 + b * kWTileBytes + ks * 32);
-              const uint32_t d = two_issuers ? my_tmem : d0 + b * kAccStride;
+              const uint32_t d = my_tmem;
               if constexpr (kPair) {
                 if (p.fp8) mma_mxf8_pair_e(e0, d, ad, bd, idesc, my_sfa + 4 * (b - b_lo), my_sfb, accum);
                 else mma_f16_pair_e(e0, d, ad, bd, idesc, accum);
@@ -966,12 +990,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
         }
         if (!ok) break;
-        if constexpr (kPair) mma_commit_pair_e(e0, &sh.acc_full[acc], 0x3);
-        else mma_commit_e(e0, &sh.acc_full[acc]);
-        if (++acc == n_acc) {
-          acc = 0;
-          acc_phase ^= 1u;
-        }
+        if constexpr (kPair) mma_commit_pair_e(e0, &sh.acc_full[0], 0x3);
+        else mma_commit_e(e0, &sh.acc_full[0]);
+        acc_phase ^= 1u;
       }
       });
       // all tcgen05 work of the CTA (pair) completes before TMEM is released
@@ -983,13 +1004,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == kSfWarp) {
     // ================================================= fp8 scale words
-    // For every stage, in the order the MMA thread consumes them: wait until
-    // its raw scale bytes have landed; on the first K-block of each group of
-    // four, write the
-    // TMEM scale words (weights of each of this CTA's blocks, tokens) next to
-    // the raw bytes; then mark the stage ready on the first CTA of the pair.
-    // A stage's words are rewritten only after it has been refilled, i.e.
-    // after the MMAs and copies that read them.
+    // One SM: for every stage, in the order the MMA threads consume them,
+    // wait until its raw scale bytes have landed; on the first K-block of
+    // each group of four, write the TMEM scale words (weights of each block,
+    // tokens) next to the raw bytes (FP4 weights: rearrange the stage's
+    // weight-scale atom), then arrive on the stage's operand barrier.  A
+    // stage's words are rewritten only after it has been refilled, i.e. after
+    // the MMAs and copies that read them.  A pair: the same words once per
+    // group, in the group ring, published on the first CTA's sf_grp.
     if (p.fp8 && S > 0) {
       uint32_t stage = 0, phase = 0;
       bool ok = true;
@@ -1022,19 +1044,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t gword[kB];
 #pragma unroll
         for (int b = 0; b < kB; ++b) gword[b] = kW4 ? 0u : group_weight_word(wsf[b], lane, KB);
-        for (int32_t kb = 0; kb < KB; ++kb) {
-          // A pair's scale words change only on the first K-block of a
-          // group, and the MMA thread waits for them only there, so the
-          // other stages are skipped: no wait, no arrival.  (Waiting on
-          // them would let this warp fall a whole ring cycle behind, since
-          // nothing holds the ring back for it on those stages.)
-          if (kPair && (kb % kSfGroup) != 0) {
-            if (++stage == (uint32_t)S) {
-              stage = 0;
-              phase ^= 1u;
+        if constexpr (kPair) {
+          // a pair: the tile's scale groups in order, as they land in the ring
+          for (int32_t g = 0; g < NG; ++g) {
+            const uint32_t slot = wgrp % kGRing;
+            if (!warp_wait(&sh.g_full[slot], (wgrp / kGRing) & 1, deadline, &sh.abort_flag, p.status)) {
+              ok = false;
+              break;
             }
-            continue;
+            uint8_t* gb = gbuf + (size_t)slot * kSfStage;
+            sf_build_words(gb, __shfl_sync(0xffffffffu, gword[0], g), lane);
+            if (kB == 2) {
+              const uint32_t w1 = __shfl_sync(0xffffffffu, gword[kB - 1], g);
+              *reinterpret_cast<uint4*>(gb + kSfW1 + lane * 16) = make_uint4(w1, w1, w1, w1);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(grp0 + slot * (uint32_t)sizeof(uint64_t));
+            ++wgrp;
+            if (g == 0 && t + n_units < total) fetch_wsf(t + n_units, wsf_nxt);
           }
+        } else {
+        for (int32_t kb = 0; kb < KB; ++kb) {
           if (!warp_wait(&sh.sf_full[stage], phase, deadline, &sh.abort_flag, p.status)) {
             ok = false;
             break;
@@ -1064,27 +1095,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if ((kb % kSfGroup) == 0 || kW4) fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) {
-            if constexpr (kPair) {
-              if ((kb % kSfGroup) == 0) {
-                mbar_arrive_cluster(grp0 + (wgrp & 3) * (uint32_t)sizeof(uint64_t));
-                ++wgrp;
-              }
-            } else {
-              mbar_arrive(&sh.full[stage]);
-            }
-          }
+          if (lane == 0) mbar_arrive(&sh.full[stage]);
           if (kb == 0 && t + n_units < total && !kW4) fetch_wsf(t + n_units, wsf_nxt);
           if (++stage == (uint32_t)S) {
             stage = 0;
             phase ^= 1u;
           }
         }
+        }
       }
       });
     }
   } else if (warp == kMma2Warp) {
-    // second MMA issuer: idle in a CTA pair
+    // second MMA issuer: idle with tokens on M (one issuer)
   } else {
     // ================================================= epilogue
     const uint32_t quad = warp & 3u;  // TMEM lanes this warp may access
@@ -1093,16 +1116,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool odd = (lane & 1u) != 0;
     with_blocks([&](auto bc) {
     constexpr int kB = decltype(bc)::value;
-    uint32_t acc = 0, acc_phase = 0;
-    uint32_t tile_par = 0;  // SwiGLU to E4M3: parity of tiles done, the exchange barrier's phase
+    uint32_t acc_phase = 0;
+    [[maybe_unused]] uint32_t tile_par = 0;  // SwiGLU to E4M3: parity of tiles done, the exchange barrier's phase
     for (int32_t t = unit; S > 0 && t < total; t += n_units) {
       const Tile tl = decode_tile(t, tpre, cnt, rowbase, E, NB, q, p.masked, ttab, bal, total, n_units);
-      if (!warp_wait(&sh.acc_full[acc], acc_phase, deadline, &sh.abort_flag, p.status)) break;
+      if (!warp_wait(&sh.acc_full[0], acc_phase, deadline, &sh.abort_flag, p.status)) break;
       tc_fence_after();
-      const uint32_t taddr = tmem + ((quad * 32u) << 16) + acc * kAccStride;
+      const uint32_t taddr = tmem + ((quad * 32u) << 16);
       // block 1's accumulator (the up half of a SwiGLU tile)
-      const uint32_t taddr1 = two_issuers ? tacc1 + ((quad * 32u) << 16) : taddr + kAccStride;
-      bool released = false;  // this warp's arrival on acc_empty is made
+      [[maybe_unused]] const uint32_t taddr1 = tacc1 + ((quad * 32u) << 16);
       bool swiglu = false;
       if constexpr (kB == 2 && !kPair && !kTokM) swiglu = p.epi != kEpiPlain;
       if constexpr (kTokM) {
@@ -1183,18 +1205,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (!released) {
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          if constexpr (kPair) mbar_arrive_cluster(acc_empty0 + acc * (uint32_t)sizeof(uint64_t));
-          else mbar_arrive(&sh.acc_empty[acc]);
-        }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if constexpr (kPair) mbar_arrive_cluster(acc_empty0);
+        else mbar_arrive(&sh.acc_empty[0]);
       }
-      if (++acc == n_acc) {
-        acc = 0;
-        acc_phase ^= 1u;
-      }
+      acc_phase ^= 1u;
     }
     });
   }
