@@ -26,15 +26,16 @@
 // moves ~94 KB through an SM's shared memory for 3.9 M fp8 multiply-adds and
 // the tensor pipe waits.  Two blocks against the same token tile, and the
 // pair's split of the token operand, cut the bytes per multiply-add.  Two
-// 240/256-column fp32 accumulators fill TMEM, so a tile's epilogue is not
-// overlapped with the next tile's main loop.
+// 240/256-column fp32 accumulators fill TMEM, so the next tile's MMAs wait
+// until the epilogue has read the accumulators; the epilogue then parks most
+// of the tile in registers (as bf16) and stores it while they run.
 //
-// CTA = 12 warps: warp 0 issues TMA; warps 1 and 11 issue the tcgen05.mma
-// and tcgen05.cp on one SM (below), warp 1 alone for a CTA pair (the pair's
-// first CTA); warps 2-5 and 7-10 drain the fp32 accumulators from TMEM (two
-// warps per 32-lane quadrant, alternate 16-token chunks) and store bf16 rows;
-// warp 6 (fp8 only) turns each stage's raw UE8M0 bytes into the TMEM
-// scale-word layout, four K-blocks per word.
+// CTA = 16 warps: warp 0 issues TMA; warps 1 and 11 issue the tcgen05.mma
+// and tcgen05.cp (below; on a CTA pair those of the first CTA); warps 2-5,
+// 7-10 and 12-15 drain the fp32 accumulators from TMEM (three warps per
+// 32-lane quadrant, every third 16-token chunk) and store bf16 rows; warp 6
+// (fp8 only) turns the raw UE8M0 bytes into the TMEM scale-word layout, four
+// K-blocks per word.
 //
 // MMA issue.  The tensor pipe queues only about two MMAs, so whatever the
 // issuing thread does between MMAs (a barrier test ~90 cycles, a commit ~60,
@@ -62,11 +63,15 @@
 namespace mg {
 namespace fwd {
 
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
 constexpr int kSfWarp = 6;
 // Second MMA-issuing warp of single-SM two-block tiles (block 1's MMAs).
 constexpr int kMma2Warp = 11;
-constexpr int kEpiWarps = 8;                     // warps 2-5 and 7-10: two per TMEM lane quadrant
+// warps 2-5, 7-10 and 12-15: three per TMEM lane quadrant
+constexpr int kEpiWarps = 12;
+// plain epilogue: chunks of 16 tokens a warp parks in registers (as bf16)
+// before it releases the accumulator
+constexpr int kParked = 4;
 constexpr int kMaxStages = 16;
 constexpr int kCtaRows = 128;                    // weight rows of one block on one SM
 constexpr int kRowBytes = 128;                   // K bytes per stage and row
@@ -1111,7 +1116,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ================================================= epilogue
     const uint32_t quad = warp & 3u;  // TMEM lanes this warp may access
-    const int32_t half = warp >= kSfWarp ? 1 : 0;
+    // which of the quadrant's three warps (the SwiGLU and tokens-on-M
+    // epilogues use the first two, as halves)
+    const int32_t third = warp < kSfWarp ? 0 : (warp < kMma2Warp ? 1 : 2);
+    const int32_t half = third;
     const uint32_t acc_empty0 = mapa_shared(smem_u32(&sh.acc_empty[0]), 0);
     const bool odd = (lane & 1u) != 0;
     with_blocks([&](auto bc) {
@@ -1125,9 +1133,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t taddr = tmem + ((quad * 32u) << 16);
       // block 1's accumulator (the up half of a SwiGLU tile)
       [[maybe_unused]] const uint32_t taddr1 = tacc1 + ((quad * 32u) << 16);
+      bool released = false;  // this warp's arrival on acc_empty is made
       bool swiglu = false;
       if constexpr (kB == 2 && !kPair && !kTokM) swiglu = p.epi != kEpiPlain;
-      if constexpr (kTokM) {
+      if (kTokM && third == 2) {
+        // (not needed by this epilogue)
+      } else if constexpr (kTokM) {
         // Tokens on M: TMEM lane = the tile's token, column = weight row, so
         // each thread holds one output row; the two warps of a lane quadrant
         // take 128 of the 256 columns each and store 16 bytes at a time.
@@ -1158,7 +1169,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else if (swiglu) {
-        if (p.epi == kEpiSwigluBf16) {
+        if (third == 2) {
+          // (not needed by this epilogue)
+        } else if (p.epi == kEpiSwigluBf16) {
           swiglu_bf16_tile(p, tl, taddr, taddr1, quad, half, lane);
         } else if (!swiglu_fp8_tile(p, sh, tl, taddr, taddr1, quad, half, lane, tile_par, deadline)) {
           break;
@@ -1168,9 +1181,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // this thread's output column of block 0; block b is b * kBlockRows further
         const int32_t n = tl.nb * tile_rows + (int32_t)(rank * kCtaRows + quad * 32 + lane);
         __nv_bfloat16* dpair = static_cast<__nv_bfloat16*>(p.D) + (int64_t)tl.row0 * p.N + (n & ~1);
-        // the two warps of a lane quadrant take alternate 16-token chunks
-        for (int32_t c0 = 16 * half; c0 < tl.qn; c0 += 32) {
-          uint32_t r[kB][16];
+        // The quadrant's three warps take every third 16-token chunk.  A
+        // warp reads its first kParked chunks into registers (rounded to
+        // bf16, two tokens per register) and releases the accumulator before
+        // storing them, so the next tile's MMAs run during the stores.
+        // Chunks past those (only the widest tiles have them) are stored
+        // before the release.
+        auto load_chunk = [&](int32_t c0, uint32_t (&r)[kB][16]) {
 #pragma unroll
           for (int b = 0; b < kB; ++b) tmem_ld16((b == 0 ? taddr : taddr1) + (uint32_t)c0, r[b]);
           if constexpr (kB == 1) {
@@ -1188,28 +1205,70 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
 #pragma unroll
           for (int b = 0; b < kB; ++b) tmem_regs_ready(r[b]);
-          // Lanes 2j and 2j+1 hold adjacent output columns.  One exchange per
-          // pair of tokens gives the even lane both columns of token i and the
-          // odd lane both columns of token i+1, so each store writes 4 bytes.
+        };
+        // Lanes 2j and 2j+1 hold adjacent output columns, a register two
+        // tokens of one column.  One exchange per register gives the even
+        // lane both columns of the first token and the odd lane both
+        // columns of the second, so each store writes 4 bytes.
+        auto store_chunk = [&](int32_t c0, const uint32_t (&v)[kB][8]) {
 #pragma unroll
-          for (int i = 0; i < 16; i += 2) {
-            const int32_t row = c0 + i + (odd ? 1 : 0);
+          for (int i = 0; i < 8; ++i) {
+            const int32_t row = c0 + 2 * i + (odd ? 1 : 0);
 #pragma unroll
             for (int b = 0; b < kB; ++b) {
-              const float mine = __uint_as_float(odd ? r[b][i + 1] : r[b][i]);
-              const float recv = __shfl_xor_sync(0xffffffffu, __uint_as_float(odd ? r[b][i] : r[b][i + 1]), 1);
-              const __nv_bfloat162 v = odd ? __floats2bfloat162_rn(recv, mine) : __floats2bfloat162_rn(mine, recv);
+              const uint32_t mine = v[b][i];
+              const uint32_t recv = __shfl_xor_sync(0xffffffffu, mine, 1);
+              const uint32_t out = odd ? __byte_perm(recv, mine, 0x7632) : __byte_perm(mine, recv, 0x5410);
               if (row < tl.rows)
-                *reinterpret_cast<__nv_bfloat162*>(dpair + (int64_t)row * p.N + b * kBlockRows) = v;
+                *reinterpret_cast<uint32_t*>(dpair + (int64_t)row * p.N + b * kBlockRows) = out;
             }
           }
+        };
+        auto pack_chunk = [&](const uint32_t (&r)[kB][16], uint32_t (&v)[kB][8]) {
+#pragma unroll
+          for (int b = 0; b < kB; ++b)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[b][2 * i]), __uint_as_float(r[b][2 * i + 1]));
+              v[b][i] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+        };
+        for (int32_t c0 = 16 * third + 48 * kParked; c0 < tl.qn; c0 += 48) {
+          uint32_t r[kB][16], v[kB][8];
+          load_chunk(c0, r);
+          pack_chunk(r, v);
+          store_chunk(c0, v);
         }
+        uint32_t park[kParked][kB][8];
+#pragma unroll
+        for (int j = 0; j < kParked; ++j) {
+          const int32_t c0 = 16 * third + 48 * j;
+          if (c0 < tl.qn) {
+            uint32_t r[kB][16];
+            load_chunk(c0, r);
+            pack_chunk(r, park[j]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (kPair) mbar_arrive_cluster(acc_empty0);
+          else mbar_arrive(&sh.acc_empty[0]);
+        }
+#pragma unroll
+        for (int j = 0; j < kParked; ++j) {
+          const int32_t c0 = 16 * third + 48 * j;
+          if (c0 < tl.qn) store_chunk(c0, park[j]);
+        }
+        released = true;
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if constexpr (kPair) mbar_arrive_cluster(acc_empty0);
-        else mbar_arrive(&sh.acc_empty[0]);
+      if (!released) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (kPair) mbar_arrive_cluster(acc_empty0);
+          else mbar_arrive(&sh.acc_empty[0]);
+        }
       }
       acc_phase ^= 1u;
     }

@@ -15,10 +15,21 @@
 // zeroes those rows of the staged operands in shared memory, and the MMA
 // thread issues only the 16-token steps that still hold valid tokens.
 //
-// Tiles of all experts are ordered by descending token count and dealt to
-// the persistent CTAs in a snake order, so every CTA receives a similar mix
-// of long and short tiles.  Experts with no tokens produce zero tiles that
-// the epilogue writes without any load or MMA.
+// Schedule.  An expert's tiles all stream the same token range of dY and X,
+// so they read it from DRAM once only if they run at the same time.  When
+// one expert's NT tiles fit the grid, the first floor(P / NT) * NT CTAs form
+// groups of NT, and a group runs its experts one after another, all NT tiles
+// of an expert side by side (tile l on the group's CTA l); the remaining
+// P mod NT CTAs take the smallest experts, whose token ranges stay in L2
+// while those CTAs go over them in several rounds.  Experts are split
+// between the two by their cost (64-token stages plus a fixed epilogue
+// share per tile), smallest first into the leftover CTAs while they stay
+// within the grid's average load; the groups take the rest, largest first,
+// each to the least loaded group.  Otherwise (an expert has more tiles than
+// the grid, or the leftover CTAs would get nothing) the tiles of all experts,
+// by descending token count, are dealt in a snake order.  Experts with no
+// tokens produce zero tiles that the epilogue writes without any load or
+// MMA.
 //
 // CTA = 11 warps: warp 0 issues TMA; warp 1 owns TMEM and one of its threads
 // issues every tcgen05.mma (nothing else runs between MMAs, so the tensor
@@ -44,6 +55,9 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccStride = 256;
 constexpr int kSmemBytes = 227 * 1024;
 constexpr uint64_t kDrainNs = 200ull * 1000 * 1000;
+constexpr int kMaxGroups = 256;           // expert groups of the schedule
+constexpr int kTileOverhead = 8;          // a tile's epilogue, in 64-token stages
+static_assert((2 * kMaxExperts + kMaxGroups) * 4 <= kEpiWarps * kOutBox, "schedule scratch fits the staging area");
 
 struct Params {
   const int32_t* counts;
@@ -63,6 +77,9 @@ struct Shared {
   uint32_t tmem_base;
   int32_t abort_flag;
   int32_t n_valid;
+  // schedule: mode 1 = expert groups, 0 = snake over all tiles
+  int32_t mode, n_grp, n_left, nA;
+  int32_t goff[kMaxGroups + 1];  // group g's experts: order[goff[g] .. goff[g+1])
 };
 
 struct Tile {
@@ -191,15 +208,82 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     order[rank] = e;
   }
+  __syncthreads();
   if (threadIdx.x == 0) {
     int32_t nv = 0;
     for (int32_t e = 0; e < E; ++e) nv += cnt[e] >= 0;
     sh.n_valid = nv;
+    // ---- schedule (see the header comment)
+    const int32_t P = (int32_t)gridDim.x;
+    int32_t ng = NT <= P ? P / NT : 0;
+    if (ng > kMaxGroups) ng = 0;
+    const int32_t nl = P - ng * NT;
+    auto cost = [&](int32_t e) { return (int64_t)((cnt[e] + kBlockT - 1) / kBlockT) + kTileOverhead; };
+    int64_t tot = 0;
+    for (int32_t r = 0; r < nv; ++r) tot += cost(order[r]);
+    int32_t nA = nv;
+    if (ng > 0 && nl > 0) {
+      // leftover CTAs: NT * load / nl per CTA against the average NT * tot / P
+      int64_t sl = 0;
+      while (nA > 0 && (sl + cost(order[nA - 1])) * P <= tot * nl) sl += cost(order[--nA]);
+    }
+    const int32_t mode = (ng > 0 && nv > 0 && (nl == 0 || nA < nv)) ? 1 : 0;
+    sh.mode = mode;
+    sh.n_grp = ng;
+    sh.n_left = nl;
+    sh.nA = nA;
+    if (mode == 1) {
+      // group of each of order[0 .. nA): least loaded group (ties: lowest),
+      // in a snake over the groups when there are many; then order[0 .. nA)
+      // regrouped by group (counting sort, stable), in the epilogue staging
+      // area, which is unused until the main loops (2 * E + ng ints: at
+      // most 2 * 1024 + 256, a quarter of it)
+      int32_t* grp = reinterpret_cast<int32_t*>(stage_out);
+      int32_t* tmp = grp + E;
+      int64_t load[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      for (int32_t g = 0; g <= ng; ++g) sh.goff[g] = 0;
+      for (int32_t r = 0; r < nA; ++r) {
+        int32_t g;
+        if (ng <= 8) {
+          g = 0;
+          for (int32_t h = 1; h < ng; ++h) if (load[h] < load[g]) g = h;
+          load[g] += cost(order[r]);
+        } else {
+          const int32_t k = r % ng;
+          g = ((r / ng) & 1) ? ng - 1 - k : k;
+        }
+        grp[r] = g;
+        ++sh.goff[g + 1];
+      }
+      for (int32_t g = 0; g < ng; ++g) sh.goff[g + 1] += sh.goff[g];
+      int32_t* put = tmp + E;
+      for (int32_t g = 0; g < ng; ++g) put[g] = sh.goff[g];
+      for (int32_t r = 0; r < nA; ++r) tmp[put[grp[r]]++] = order[r];
+      for (int32_t r = 0; r < nA; ++r) order[r] = tmp[r];
+    }
   }
   __syncthreads();
   tc_fence_after();
 
   const int32_t total = sh.n_valid * NT;
+  // position (order index * NT + tile) of this CTA's r-th tile; -1: no more,
+  // -2: none in this round
+  const int32_t mode = sh.mode, ng = sh.n_grp, nl = sh.n_left, nA = sh.nA;
+  auto tile_pos = [&](int32_t r) -> int32_t {
+    if (mode == 0) return snake_pos(r, total);
+    const int32_t c = (int32_t)blockIdx.x;
+    if (c < ng * NT) {
+      const int32_t g = c / NT, l = c - g * NT;
+      const int32_t k = sh.goff[g] + r;
+      return k < sh.goff[g + 1] ? k * NT + l : -1;
+    }
+    const int32_t b = c - ng * NT;
+    const int32_t nlt = (sh.n_valid - nA) * NT;  // the leftover CTAs' tiles
+    const int64_t base = (int64_t)r * nl;
+    if (base >= nlt) return -1;
+    const int64_t i = base + ((r & 1) ? nl - 1 - b : b);
+    return i < nlt ? nA * NT + (int32_t)i : -2;
+  };
   const int32_t avail = kSmemBytes - 1024 - (int32_t)(reinterpret_cast<uintptr_t>(ring) -
                                                      reinterpret_cast<uintptr_t>(smem));
   if (threadIdx.x == 0 && avail < kStageBytes) set_status(p.status, MG_ERR_UNSUPPORTED);
@@ -222,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int64_t issued = 0;
       bool ok = true;
       for (int32_t r = 0; ok; ++r) {
-        const int32_t pos = snake_pos(r, total);
+        const int32_t pos = tile_pos(r);
         if (pos == -1) break;
         if (pos < 0) continue;
         const Tile tl = decode_tile(pos, order, cnt, tokoff, NBk, NT, p.K);
@@ -270,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       for (int32_t r = 0; ok; ++r) {
-        const int32_t pos = snake_pos(r, total);
+        const int32_t pos = tile_pos(r);
         if (pos == -1) break;
         if (pos < 0) continue;
         const Tile tl = decode_tile(pos, order, cnt, tokoff, NBk, NT, p.K);
@@ -332,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       for (int32_t r = 0; ok; ++r) {
-        const int32_t pos = snake_pos(r, total);
+        const int32_t pos = tile_pos(r);
         if (pos == -1) break;
         if (pos < 0) continue;
         const Tile tl = decode_tile(pos, order, cnt, tokoff, NBk, NT, p.K);
@@ -374,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool out_pending = false;
     uint32_t acc = 0, acc_phase = 0;
     for (int32_t r = 0; S > 0; ++r) {
-      const int32_t pos = snake_pos(r, total);
+      const int32_t pos = tile_pos(r);
       if (pos == -1) break;
       if (pos < 0) continue;
       const Tile tl = decode_tile(pos, order, cnt, tokoff, NBk, NT, p.K);

@@ -69,6 +69,25 @@ def test_prefill_fp8_sampled_experts(lib, cuda, gemm_index):
         gu.check_frobenius(Dbits[o:o + t], og.expert_product(a, b))
 
 
+def test_prefill_fp8_gemm2_every_expert_all_rows(lib, cuda):
+    """Skewed FP8 prefill, GEMM2 (N=7168, K=2048): every expert, all of its
+    rows and columns, per-expert Frobenius rule (the oracle's ~1 TFLOP of
+    fp64 work takes seconds here)."""
+    counts, p, ops, Dbits = _contiguous_full("prefill_fp8_e64_t32768_n4096_k7168", cuda, 1)
+    A = ops.A.cpu().numpy()
+    SFA = ops.SFA.cpu().numpy()
+    checked = 0
+    for e, t in enumerate(counts):
+        if t == 0:
+            continue
+        o = p.offsets[e]
+        a = on.dequant_rows(A[o:o + t], SFA[:, o:o + t])
+        b = on.dequant_weight(ops.B[e].cpu().numpy(), ops.SFB[e].cpu().numpy())
+        gu.check_frobenius(Dbits[o:o + t], og.expert_product(a, b))
+        checked += t
+    assert checked == sum(counts)
+
+
 def _row_sample(t, q, rng, extra=8):
     """Rows of an expert to check: its first rows, the rows of its last
     token tile (trimmed to a multiple of 16 by the kernel, capped at 48),
