@@ -57,7 +57,8 @@ CONFIGS = [
 ]
 FP8_OVER_BF16 = 2.0   # nominal dense fp8 : bf16 tensor throughput ratio
 METRIC = "effective TFLOPS (valid rows only)"
-L2_NOTE = "L2 flushed between timed reps: 2 x l2CacheSize bytes written outside the CUDA events"
+L2_NOTE = ("L2 flushed between timed reps: 2 x l2CacheSize bytes written, then a ~0.2 ms GPU spin, "
+           "both outside the CUDA events")
 
 
 def _binding():
@@ -631,7 +632,11 @@ def cpu_baseline(w, budget_s):
 
 class L2Flush:
     """Writes 2 x l2CacheSize bytes between timed repetitions, so every rep
-    reads its operands from HBM."""
+    reads its operands from HBM; then the GPU spins ~0.2 ms, so the host has
+    queued the next start event and launch before the GPU reaches them (a
+    short GEMM's host-side preparation otherwise lands inside its events)."""
+
+    SETTLE_CYCLES = 400_000
 
     def __init__(self, dev):
         l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -640,6 +645,7 @@ class L2Flush:
 
     def __call__(self):
         self.buf.fill_(1)
+        torch.cuda._sleep(self.SETTLE_CYCLES)
 
 
 def timed_reps(w, lib, stream, flush, reps):
@@ -653,6 +659,69 @@ def timed_reps(w, lib, stream, flush, reps):
         w.step(lib, stream, evs[i])
     torch.cuda.synchronize()
     return [[evs[i][g][0].elapsed_time(evs[i][g][1]) for g in range(n_g)] for i in range(reps)]
+
+
+def exemplar_table_path(w):
+    """The tuned exemplar table of a masked workload's shape, if there is one."""
+    sp = w.spec
+    if sp.get("form") != "masked":
+        return None
+    name = f"{sp['dtype']}_masked_e{w.E}_m{sp['M_max']}_n{sp['N']}_k{sp['K']}.json"
+    path = os.path.join(ROOT, "moe_grouped_gemm_side_gb300", "exemplars", name)
+    return path if os.path.exists(path) else None
+
+
+def selector_record(w, stream, flush, reps):
+    """Masked decode: the exemplar selector's choice (select kernel + tactic
+    GEMM, both timed) next to every fixed tactic; the built-in cost model's
+    time is the record's own ms_per_step."""
+    path = exemplar_table_path(w)
+    if path is None:
+        return None
+    mb = w.mb
+    with open(path) as f:
+        meta = json.load(f)
+    table = mb.exemplar_table(meta["exemplars"])
+    dev = w.d_counts.device
+    d_table = mb.exemplar_table_device(table, device=dev)
+    g = w.gemms[0]
+    tactic = torch.zeros(3, dtype=torch.int32, device=dev)
+
+    def run_tactic():
+        mb.mgemm_masked_tactic(g["A"], g["B"], g["D"], w.d_counts, tactic, SFA=g["SFA"], SFB=g["SFB"],
+                               status=w.status, stream=stream)
+
+    def run_selected():
+        mb.select_exemplar(w.d_counts, d_table, len(table), tactic, status=w.status, stream=stream)
+        run_tactic()
+
+    def median_ms(fn):
+        for _ in range(3):
+            flush()
+            fn()
+        ts = []
+        for _ in range(reps):
+            flush()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return sorted(ts)[len(ts) // 2]
+
+    ex_ms = median_ms(run_selected)
+    chosen = tactic.cpu().tolist()
+    fixed = {}
+    for cand in meta["candidates"]:
+        tq, blocks = (int(x) for x in cand.split("x"))
+        tactic.copy_(torch.tensor([tq, blocks, 0], dtype=torch.int32))
+        fixed[cand] = median_ms(run_tactic)
+    w.check_status()
+    best = min(fixed, key=fixed.get)
+    return {"table": os.path.relpath(path, ROOT), "table_default": meta.get("default"),
+            "exemplar": {"tactic": f"{chosen[0]}x{chosen[1]}", "index": chosen[2], "ms": ex_ms},
+            "fixed_ms": fixed, "best_fixed": best, "exemplar_vs_best_fixed": ex_ms / fixed[best]}
 
 
 def config_record(w, lib, stream, flush, peaks, args, cpu=None):
@@ -682,6 +751,10 @@ def config_record(w, lib, stream, flush, peaks, args, cpu=None):
         rec["P_at_tile"] = [t["P_at_tile"] for t in tac]
         rec["pad_frac_at_tile"] = [t["pad_frac_at_tile"] for t in tac]
         rec["effective_experts"] = tac[0]["effective_experts"]
+    sel = selector_record(w, stream, flush, args.reps)
+    if sel is not None:
+        sel["cost_model_ms"] = ms
+        rec["selector"] = sel
     if cpu is None and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, args.config_cpu_budget)
     rec["cpu_baseline"] = cpu

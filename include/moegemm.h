@@ -336,9 +336,11 @@ mg_status mgemm_masked_swiglu(mg_dtype dt, mg_swiglu_out out, const void* A, con
  * and both launches can be captured in one CUDA graph.  Arguments, results
  * and errors are those of mgemm_contiguous / mgemm_masked (with tile_q taken
  * from the tactic; tiles wider than the kernel allows are narrowed, which
- * does not change the result).  These calls run the single-SM kernel of two
- * 128-row blocks (N % 256 == 0) or of one block; a tactic that is not valid
- * is reported as MG_ERR_DEVICE_ARG and the kernel's own choice is used.
+ * does not change the result).  These calls run the kernel family that
+ * mg_set_kernel_policy selects for mgemm_contiguous / mgemm_masked, with
+ * tiles of one or two of that family's weight blocks (`blocks`: 128 rows on
+ * one SM, 256 on an SM pair); a tactic that is not valid is reported as
+ * MG_ERR_DEVICE_ARG and the kernel's own choice is used.
  * ------------------------------------------------------------------------ */
 mg_status mgemm_contiguous_tactic(mg_dtype dt, const void* A, const uint8_t* SFA, const void* B,
                                   const uint8_t* SFB, void* D, const int32_t* d_counts, int32_t E,

@@ -445,7 +445,7 @@ mg_status mgemm_contiguous_tactic(mg_dtype dt, const void* A, const uint8_t* SFA
                                        d_status);
   if (st != MG_OK) return st;
   a.tactic = d_tactic;
-  return from_cuda(launch_fwd(a, static_cast<cudaStream_t>(stream), N % 256 == 0 ? kFwdDual : kFwdSingle));
+  return from_cuda(launch_fwd_any(a, static_cast<cudaStream_t>(stream)));
 }
 
 mg_status mgemm_masked_tactic(mg_dtype dt, const void* A, const uint8_t* SFA, const void* B,
@@ -457,7 +457,7 @@ mg_status mgemm_masked_tactic(mg_dtype dt, const void* A, const uint8_t* SFA, co
   const mg_status st = prep_masked(a, dt, A, SFA, B, SFB, D, d_valid_m, E, M_max, N, K, d_status);
   if (st != MG_OK) return st;
   a.tactic = d_tactic;
-  return from_cuda(launch_fwd(a, static_cast<cudaStream_t>(stream), N % 256 == 0 ? kFwdDual : kFwdSingle));
+  return from_cuda(launch_fwd_any(a, static_cast<cudaStream_t>(stream)));
 }
 
 mg_status kgemm_grouped(const void* dY, const void* X, float* dW, const int32_t* d_counts,

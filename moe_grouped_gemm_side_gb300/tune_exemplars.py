@@ -6,15 +6,17 @@ can differ by more than 10 %, so the table is measured, not derived from the
 padding formula; the benchmark covers low-token decode buckets and broad and
 concentrated histograms at the same token count U.
 
-Tuning: for each histogram of a seeded set (U from 32 to 32768 assignments,
-Dirichlet shares from concentrated to broad, Zipf ranks), every candidate
-(token tile x weight blocks per tile) runs the contiguous grouped GEMM
-through ``mgemm_contiguous_tactic``.  The histogram becomes one exemplar (its
-features from ``moe_exemplar_features_host``) whose tactic is the default
-(the widest tile, two blocks) unless the fastest candidate beats it by more
-than ``--min-gain``: many candidates finish within the run-to-run spread of
-each other, and a table of near-ties would carry that noise to neighbouring
-histograms.
+Tuning: for each histogram of a seeded set (contiguous form: U from 32 to
+32768 assignments; masked decode form: U from 16 to 2048 valid rows, no
+expert above M_max; Dirichlet shares from concentrated to broad, Zipf ranks),
+every candidate (token tile x weight blocks per tile) runs the grouped GEMM
+through ``mgemm_contiguous_tactic`` / ``mgemm_masked_tactic``.  The default
+tactic is the candidate with the best geometric-mean time over the whole
+tuning set; each histogram becomes one exemplar (its features from
+``moe_exemplar_features_host``) that keeps the default unless its fastest
+candidate beats the default by more than ``--min-gain``: many candidates
+finish within the run-to-run spread of each other, and a table of near-ties
+would carry that noise to neighbouring histograms.
 
 Evaluation, on histograms drawn with other seeds: the latency of the
 exemplar choice, of the built-in cost-model choice (tile_q = 0), and of
@@ -25,6 +27,8 @@ with and without the hysteresis margin.
 Usage (writes the table and a summary):
     python -m moe_grouped_gemm_side_gb300.tune_exemplars --dtype fp8 --N 4096 --K 7168 \\
         --out moe_grouped_gemm_side_gb300/exemplars/fp8_e64_n4096_k7168.json
+    python -m moe_grouped_gemm_side_gb300.tune_exemplars --form masked --E 16 --M-max 256 \\
+        --out moe_grouped_gemm_side_gb300/exemplars/fp8_masked_e16_m256_n4096_k7168.json
     python -m moe_grouped_gemm_side_gb300.tune_exemplars --evaluate TABLE.json
 """
 import argparse
@@ -41,26 +45,48 @@ from . import workloads as wl
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 TILES = {"fp8": (16, 32, 64, 128, 240), "bf16": (16, 32, 64, 128, 256)}
-U_TUNE = (32, 64, 128, 256, 512, 1024, 2048, 4096, 8192, 16384, 32768)
-U_EVAL = (32, 48, 64, 96, 200, 1024, 1500, 3000, 6000, 12000, 24000, 32768)
+U_TUNE = {"contiguous": (32, 64, 128, 256, 512, 1024, 2048, 4096, 8192, 16384, 32768),
+          "masked": (16, 32, 64, 128, 256, 512, 1024, 2048)}
+U_EVAL = {"contiguous": (32, 48, 64, 96, 200, 1024, 1500, 3000, 6000, 12000, 24000, 32768),
+          "masked": (24, 32, 48, 64, 96, 200, 454, 768, 1024, 1500)}
 SHAPES = (("dirichlet", 0.2), ("dirichlet", 1.0), ("dirichlet", 8.0), ("zipf", 1.2), ("zipf", 0.6))
 
 
-def histogram(shape, param, E, U, seed):
+def histogram(shape, param, E, U, seed, cap=None):
+    """A seeded histogram of U rows over E experts; with a cap (the masked
+    form's M_max) rows above it move, one at a time, to the largest experts
+    still below it."""
     if shape == "dirichlet":
-        return wl.counts_dirichlet(seed=seed, E=E, total=U, alpha=param)
-    return wl.counts_zipf_prefill(seed=seed, E=E, total=U, s=param)
+        c = wl.counts_dirichlet(seed=seed, E=E, total=U, alpha=param)
+    else:
+        c = wl.counts_zipf_prefill(seed=seed, E=E, total=U, s=param)
+    if cap is not None:
+        assert U <= cap * E
+        excess = sum(max(0, x - cap) for x in c)
+        c = [min(x, cap) for x in c]
+        order = sorted(range(E), key=lambda e: (-c[e], e))
+        while excess > 0:
+            for e in order:
+                if excess > 0 and c[e] < cap:
+                    c[e] += 1
+                    excess -= 1
+    return c
 
 
 class Bench:
     """Operands sized for the largest histogram; each call times one tactic."""
 
-    def __init__(self, dtype, E, N, K, max_rows, dev="cuda", align=16):
+    def __init__(self, dtype, E, N, K, max_rows, dev="cuda", align=16, form="contiguous", M_max=0):
         self.dtype, self.E, self.N, self.K, self.align, self.dev = dtype, E, N, K, align, dev
-        self.rows_cap = (max_rows + E * align + 15) // 16 * 16
-        ops = wl.make_contiguous(E, self.rows_cap, N, K, dtype, 77, dev)
+        self.form = form
+        if form == "masked":
+            ops = wl.make_masked(E, M_max, N, K, dtype, 77, dev)
+            self.D = torch.empty((E, M_max, N), dtype=torch.bfloat16, device=dev)
+        else:
+            self.rows_cap = (max_rows + E * align + 15) // 16 * 16
+            ops = wl.make_contiguous(E, self.rows_cap, N, K, dtype, 77, dev)
+            self.D = torch.empty((self.rows_cap, N), dtype=torch.bfloat16, device=dev)
         self.A, self.B, self.SFA, self.SFB = ops.A, ops.B, ops.SFA, ops.SFB
-        self.D = torch.empty((self.rows_cap, N), dtype=torch.bfloat16, device=dev)
         self.tactic = torch.zeros(3, dtype=torch.int32, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # larger than L2
@@ -71,6 +97,9 @@ class Bench:
         ts = []
         for _ in range(reps):
             self.flush.zero_()
+            # the GPU spins ~0.2 ms so the launch below is queued before the
+            # start event is reached (its host-side checks stay outside)
+            torch.cuda._sleep(400_000)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
             fn()
@@ -79,13 +108,22 @@ class Bench:
             ts.append(a.elapsed_time(b) * 1e3)
         return float(np.median(ts))
 
+    def run_tactic(self, d_counts):
+        if self.form == "masked":
+            mb.mgemm_masked_tactic(self.A, self.B, self.D, d_counts, self.tactic, SFA=self.SFA, SFB=self.SFB,
+                                   status=self.status)
+        else:
+            mb.mgemm_contiguous_tactic(self.A, self.B, self.D, d_counts, self.align, self.tactic, SFA=self.SFA,
+                                       SFB=self.SFB, status=self.status)
+
     def time_tactic(self, d_counts, tq, blocks, reps=9):
         self.tactic.copy_(torch.tensor([tq, blocks, 0], dtype=torch.int32))
-        return self._time(lambda: mb.mgemm_contiguous_tactic(
-            self.A, self.B, self.D, d_counts, self.align, self.tactic, SFA=self.SFA, SFB=self.SFB,
-            status=self.status), reps)
+        return self._time(lambda: self.run_tactic(d_counts), reps)
 
     def time_builtin(self, d_counts, reps=9):
+        if self.form == "masked":
+            return self._time(lambda: mb.mgemm_masked(
+                self.A, self.B, self.D, d_counts, SFA=self.SFA, SFB=self.SFB, status=self.status), reps)
         return self._time(lambda: mb.mgemm_contiguous(
             self.A, self.B, self.D, d_counts, self.align, SFA=self.SFA, SFB=self.SFB, status=self.status), reps)
 
@@ -99,32 +137,50 @@ class Bench:
         return times, d_counts
 
 
-def pick_tactic(times, dtype, min_gain):
-    """The tactic an exemplar keeps: the default (widest tile, two blocks)
-    unless the fastest candidate beats it by more than min_gain."""
+def pick_tactic(times, default, min_gain):
+    """The tactic an exemplar keeps: the default unless the fastest
+    candidate beats it by more than min_gain."""
     best = min(times, key=times.get)
-    default = f"{TILES[dtype][-1]}x2"
     return best if times[best] < times[default] * (1.0 - min_gain) else default
 
 
+def default_tactic(all_times):
+    """The candidate with the best geometric-mean time over a set of sweeps."""
+    keys = list(all_times[0])
+    return min(keys, key=lambda k: float(np.mean([math.log(t[k]) for t in all_times])))
+
+
+def make_bench(args, form, U_set):
+    if form == "masked":
+        return Bench(args.dtype, args.E, args.N, args.K, 0, form="masked", M_max=args.M_max)
+    return Bench(args.dtype, args.E, args.N, args.K, max(U_set))
+
+
 def tune(args):
-    bench = Bench(args.dtype, args.E, args.N, args.K, max(U_TUNE))
-    exemplars = []
-    for U in U_TUNE:
+    cap = args.M_max if args.form == "masked" else None
+    U_set = [U for U in U_TUNE[args.form] if cap is None or U <= cap * args.E]
+    bench = make_bench(args, args.form, U_set)
+    sweeps = []
+    for U in U_set:
         for i, (shape, param) in enumerate(SHAPES):
-            counts = histogram(shape, param, args.E, U, seed=2000 + 37 * i + U)
+            counts = histogram(shape, param, args.E, U, seed=2000 + 37 * i + U, cap=cap)
             times, _ = bench.sweep(counts)
+            sweeps.append((U, shape, param, counts, times))
             best = min(times, key=times.get)
-            default = f"{TILES[args.dtype][-1]}x2"
-            pick = pick_tactic(times, args.dtype, args.min_gain)
-            tq, blocks = (int(x) for x in pick.split("x"))
-            lu, shares = mb.exemplar_features_host(counts)
-            exemplars.append({"lu": lu, "shares": shares, "tile_q": tq, "blocks": blocks, "U": U,
-                              "shape": f"{shape}({param})", "counts": counts, "times_us": times})
-            print(f"U={U:6d} {shape}({param}): best {best} {times[best]:.1f} us, default {times[default]:.1f} us"
-                  f" -> {pick}", flush=True)
-    out = {"dtype": args.dtype, "E": args.E, "N": args.N, "K": args.K, "align_q": bench.align,
-           "min_gain": args.min_gain,
+            print(f"U={U:6d} {shape}({param}): best {best} {times[best]:.1f} us", flush=True)
+    default = default_tactic([sw[4] for sw in sweeps])
+    exemplars = []
+    for U, shape, param, counts, times in sweeps:
+        pick = pick_tactic(times, default, args.min_gain)
+        tq, blocks = (int(x) for x in pick.split("x"))
+        lu, shares = mb.exemplar_features_host(counts)
+        exemplars.append({"lu": lu, "shares": shares, "tile_q": tq, "blocks": blocks, "U": U,
+                          "shape": f"{shape}({param})", "counts": counts, "times_us": times})
+    differ = sum(1 for x in exemplars if f"{x['tile_q']}x{x['blocks']}" != default)
+    print(f"default tactic {default}; {differ} of {len(exemplars)} exemplars keep another", flush=True)
+    out = {"dtype": args.dtype, "form": args.form, "E": args.E, "N": args.N, "K": args.K,
+           "M_max": args.M_max if args.form == "masked" else None, "align_q": bench.align,
+           "default": default, "min_gain": args.min_gain,
            "candidates": [f"{t}x{b}" for t in TILES[args.dtype] for b in (1, 2)],
            "exemplars": exemplars}
     os.makedirs(os.path.dirname(os.path.abspath(args.out)), exist_ok=True)
@@ -141,13 +197,19 @@ def load_table(path):
 
 def evaluate(args):
     meta, table = load_table(args.evaluate)
-    entries = meta["exemplars"]
-    bench = Bench(meta["dtype"], meta["E"], meta["N"], meta["K"], max(U_EVAL))
+    form = meta.get("form", "contiguous")
+    cap = meta.get("M_max") if form == "masked" else None
+    args.M_max = cap
+    U_set = [U for U in U_EVAL[form] if cap is None or U <= cap * meta["E"]]
+    ev = argparse.Namespace(dtype=meta["dtype"], E=meta["E"], N=meta["N"], K=meta["K"], M_max=cap)
+    bench = make_bench(ev, form, U_set)
     d_table = mb.exemplar_table_device(table)
+    fixed = [meta.get("default", "240x2" if meta["dtype"] == "fp8" else "256x2"), "32x1", "128x1"]
+    fixed = list(dict.fromkeys(fixed))
     rows = []
-    for U in U_EVAL:
+    for U in U_set:
         for i, (shape, param) in enumerate(SHAPES):
-            counts = histogram(shape, param, meta["E"], U, seed=9000 + 53 * i + U)   # held out
+            counts = histogram(shape, param, meta["E"], U, seed=9000 + 53 * i + U, cap=cap)   # held out
             times, d_counts = bench.sweep(counts)
             best = min(times.values())
             mb.select_exemplar(d_counts, d_table, len(table), bench.tactic, status=bench.status)
@@ -158,7 +220,7 @@ def evaluate(args):
             lu, shares = mb.exemplar_features_host(counts)
             rows.append({"U": U, "shape": f"{shape}({param})", "best_us": best, "best": min(times, key=times.get),
                          "exemplar": f"{tq}x{blocks}", "exemplar_us": t_ex, "costmodel_us": t_cm,
-                         "fixed_us": {k: times[k] for k in ("240x2" if meta["dtype"] == "fp8" else "256x2", "32x1")},
+                         "fixed_us": {k: times[k] for k in fixed},
                          "eff_experts": (sum(counts) ** 2 / max(1, sum(c * c for c in counts)))})
             r = rows[-1]
             print(f"U={U:6d} {r['shape']:15s} best {r['best']:6s} {best:8.1f}  exemplar {r['exemplar']:6s} "
@@ -178,10 +240,12 @@ def evaluate(args):
     for margin in (0, 30000):
         switches, prev = 0, -1
         state.fill_(-1)
-        for base_U in (1024, 8192):
-            base = np.array(histogram("dirichlet", 1.0, meta["E"], base_U, seed=31))
+        for base_U in ((256, 1024) if form == "masked" else (1024, 8192)):
+            base = np.array(histogram("dirichlet", 1.0, meta["E"], base_U, seed=31, cap=cap))
             for _ in range(40):
                 c = np.maximum(0, base + rng.integers(-base.max() // 20 - 1, base.max() // 20 + 2, size=base.size))
+                if cap is not None:
+                    c = np.minimum(c, cap)
                 mb.select_exemplar(torch.tensor(c.tolist(), dtype=torch.int32, device="cuda"), d_table, len(table),
                                    bench.tactic, margin=margin, d_state=state)
                 torch.cuda.synchronize()
@@ -199,6 +263,8 @@ def evaluate(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--dtype", default="fp8", choices=["fp8", "bf16"])
+    ap.add_argument("--form", default="contiguous", choices=["contiguous", "masked"])
+    ap.add_argument("--M-max", dest="M_max", type=int, default=256, help="masked form: rows per expert")
     ap.add_argument("--E", type=int, default=64)
     ap.add_argument("--N", type=int, default=4096)
     ap.add_argument("--K", type=int, default=7168)

@@ -94,16 +94,36 @@ def test_host_operands_follow_the_workload_recipe(name):
 
 def test_exemplar_tuner_guardrail():
     """The tuner keeps the default tactic unless another beats it by more
-    than the margin; its histograms have the stated totals."""
+    than the margin; the default is the best geometric mean over the tuning
+    sweeps; its histograms have the stated totals and respect M_max."""
     from moe_grouped_gemm_side_gb300 import tune_exemplars as te
     t = {"240x2": 100.0, "16x1": 98.0, "32x2": 101.0}
-    assert te.pick_tactic(t, "fp8", 0.03) == "240x2"           # 2 % better: not enough
-    assert te.pick_tactic(dict(t, **{"16x1": 96.0}), "fp8", 0.03) == "16x1"
-    assert te.pick_tactic({"256x2": 10.0, "64x2": 9.0}, "bf16", 0.03) == "64x2"
+    assert te.pick_tactic(t, "240x2", 0.03) == "240x2"           # 2 % better: not enough
+    assert te.pick_tactic(dict(t, **{"16x1": 96.0}), "240x2", 0.03) == "16x1"
+    assert te.pick_tactic({"256x2": 10.0, "64x2": 9.0}, "256x2", 0.03) == "64x2"
+    sweeps = [{"a": 1.0, "b": 2.0}, {"a": 4.0, "b": 1.0}, {"a": 1.0, "b": 1.5}]
+    assert te.default_tactic(sweeps) == "b"                       # geomeans 1.59 vs 1.44
+    sweeps[1]["a"] = 2.0
+    assert te.default_tactic(sweeps) == "a"                       # 1.26 vs 1.44
+    assert te.default_tactic([{"a": 2.0, "b": 1.0}]) == "b"
     for U in (32, 1024, 32768):
         for i, (shape, param) in enumerate(te.SHAPES):
             c = te.histogram(shape, param, 64, U, seed=2000 + 37 * i + U)
             assert len(c) == 64 and sum(c) == U and min(c) >= 0
+    for U in te.U_TUNE["masked"] + te.U_EVAL["masked"]:
+        for i, (shape, param) in enumerate(te.SHAPES):
+            c = te.histogram(shape, param, 16, U, seed=9000 + 53 * i + U, cap=256)
+            assert len(c) == 16 and sum(c) == U and 0 <= min(c) and max(c) <= 256
+
+
+def test_exemplar_table_only_for_masked_shapes():
+    """The bench's selector record looks for a tuned table of the masked
+    decode shape only; the committed one is there."""
+    assert bench.exemplar_table_path(bench.Workload("prefill_fp8_e64_t32768_n4096_k7168")) is None
+    assert bench.exemplar_table_path(bench.Workload("kgrouped_bf16_e32_t65536_n4096_k2048")) is None
+    p = bench.exemplar_table_path(bench.Workload("masked_fp8_e16_m256_n4096_k7168"))
+    assert p is not None and p.endswith("fp8_masked_e16_m256_n4096_k7168.json")
+    assert bench.exemplar_table_path(bench.Workload("masked_fp8xfp4_e16_m256_n4096_k7168")) is None
 
 
 PEAKS = {"hbm_gbs": 6789.6, "bf16_tflops": 1869.1, "source": "measured"}
