@@ -154,8 +154,10 @@ def test_roofline_traffic_is_per_launch(case):
         assert rec["launches"] == launches
         assert r["traffic_per_step"] == rec["bytes_per_step"]
         assert r["traffic"] == pytest.approx(rec["bytes_per_step"] / launches)
-        # operands come from DRAM about once: traffic within 20 % of the algorithmic bytes
-        assert 0.99 <= r["traffic"] / r["algorithmic_bytes_per_launch"] < 1.2
+        # operands come from DRAM about once: traffic within 20 % of the
+        # algorithmic bytes (a little below them where part of the output is
+        # still in the write-back L2 when the kernel ends)
+        assert 0.9 <= r["traffic"] / r["algorithmic_bytes_per_launch"] < 1.2
     else:
         assert r["traffic"] is None and r["traffic_per_step"] is None
 
