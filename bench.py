@@ -695,6 +695,12 @@ def selector_record(w, stream, flush, reps):
         mb.select_exemplar(w.d_counts, d_table, len(table), tactic, status=w.status, stream=stream)
         run_tactic()
 
+    fused_tactic = torch.zeros(3, dtype=torch.int32, device=dev)
+
+    def run_fused():
+        mb.mgemm_masked_exemplar(g["A"], g["B"], g["D"], w.d_counts, d_table, len(table), SFA=g["SFA"],
+                                 SFB=g["SFB"], tactic_out=fused_tactic, status=w.status, stream=stream)
+
     def median_ms(fn):
         for _ in range(3):
             flush()
@@ -712,6 +718,8 @@ def selector_record(w, stream, flush, reps):
 
     ex_ms = median_ms(run_selected)
     chosen = tactic.cpu().tolist()
+    fused_ms = median_ms(run_fused) if w.E <= 32 else None
+    fused = fused_tactic.cpu().tolist()
     fixed = {}
     for cand in meta["candidates"]:
         tq, blocks = (int(x) for x in cand.split("x"))
@@ -720,8 +728,13 @@ def selector_record(w, stream, flush, reps):
     w.check_status()
     best = min(fixed, key=fixed.get)
     return {"table": os.path.relpath(path, ROOT), "table_default": meta.get("default"),
-            "exemplar": {"tactic": f"{chosen[0]}x{chosen[1]}", "index": chosen[2], "ms": ex_ms},
-            "fixed_ms": fixed, "best_fixed": best, "exemplar_vs_best_fixed": ex_ms / fixed[best]}
+            "exemplar": {"tactic": f"{chosen[0]}x{chosen[1]}", "index": chosen[2], "ms": ex_ms,
+                         "path": "select kernel + tactic GEMM"},
+            "exemplar_in_gemm": None if fused_ms is None else {
+                "tactic": f"{fused[0]}x{fused[1]}", "index": fused[2], "ms": fused_ms,
+                "path": "mgemm_masked_exemplar (choice in the GEMM prologue)"},
+            "fixed_ms": fixed, "best_fixed": best,
+            "exemplar_vs_best_fixed": (fused_ms if fused_ms is not None else ex_ms) / fixed[best]}
 
 
 def config_record(w, lib, stream, flush, peaks, args, cpu=None):

@@ -351,6 +351,23 @@ mg_status mgemm_masked_tactic(mg_dtype dt, const void* A, const uint8_t* SFA, co
                               int32_t M_max, int32_t N, int32_t K, const int32_t* d_tactic,
                               int32_t* d_status, void* stream);
 
+/* The masked form with the exemplar matched inside the GEMM ("MoE GroupGEMM
+ * padding under expert skew", "Adapt kernels without adding a CPU stall":
+ * the choice stays on the GPU, here without a kernel of its own, which on
+ * decode batches cost more than the tile choice saves).  Every CTA computes
+ * the features of d_valid_m and picks the nearest exemplar exactly as
+ * moe_select_exemplar does with margin 0 and no history (no state is
+ * shared between CTAs), then runs with its tile_q and blocks.  E <= 32
+ * (decode batches; MG_ERR_UNSUPPORTED above), 1 <= n <= 1024, d_table and
+ * d_tactic_out 16-byte aligned.  d_tactic_out: int32 [3] or NULL; if given,
+ * the first CTA writes {tile_q, blocks, index} of the choice.  A table entry
+ * with an invalid tactic is reported as MG_ERR_DEVICE_ARG and the kernel's
+ * own choice is used.  Other arguments, results and errors as mgemm_masked. */
+mg_status mgemm_masked_exemplar(mg_dtype dt, const void* A, const uint8_t* SFA, const void* B,
+                                const uint8_t* SFB, void* D, const int32_t* d_valid_m, int32_t E,
+                                int32_t M_max, int32_t N, int32_t K, const mg_exemplar* d_table,
+                                int32_t n, int32_t* d_tactic_out, int32_t* d_status, void* stream);
+
 /* ------------------------------------------------------------------------
  * K-grouped weight-gradient GEMM ("flops/deepgemm-grouped-masked-moe-gemm",
  * "Workarounds": K-grouped GEMM for MoE weight backward, M and N fixed and

@@ -55,6 +55,8 @@ SIGNATURES = {
     "mgemm_contiguous_tactic": (_i32, [_i32, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32, _vp,
                                        _vp, _vp]),
     "mgemm_masked_tactic": (_i32, [_i32, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp]),
+    "mgemm_masked_exemplar": (_i32, [_i32, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _i32, _vp,
+                                     _vp, _vp]),
     "kgemm_grouped": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _vp, _vp]),
     "mg_set_wait_limit_ns": (_i32, [_i64]),
     "mg_get_wait_limit_ns": (_i64, []),
@@ -401,6 +403,21 @@ def mgemm_masked_tactic(A, B, D, d_valid_m, d_tactic, SFA=None, SFB=None, status
     _check("mgemm_masked_tactic", lib.mgemm_masked_tactic(
         dt, _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(D), _ptr(d_valid_m), E,
         M_max, N, K, _ptr(d_tactic), _ptr(status), _stream(stream)))
+
+
+def mgemm_masked_exemplar(A, B, D, d_valid_m, d_table, n: int, SFA=None, SFB=None, tactic_out=None,
+                          status=None, stream=None):
+    """mgemm_masked with the exemplar matched inside the GEMM (E <= 32)."""
+    lib = load()
+    E, M_max, K = A.shape
+    N = B.shape[1]
+    dt = _fwd_dtype(A, B, K)
+    _check_fwd(dt, A, B, D, d_valid_m, SFA, SFB, status, E * M_max, M_max, E, N, K, E)
+    _need(d_table, "table", n * EXEMPLAR_DTYPE.itemsize)
+    _opt(tactic_out, "tactic_out", 12, _int32())
+    _check("mgemm_masked_exemplar", lib.mgemm_masked_exemplar(
+        dt, _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(D), _ptr(d_valid_m), E,
+        M_max, N, K, _ptr(d_table), n, _ptr(tactic_out), _ptr(status), _stream(stream)))
 
 
 def kgemm_grouped(dY, X, dW, d_counts, status=None, stream=None):

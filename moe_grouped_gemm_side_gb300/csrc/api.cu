@@ -460,6 +460,22 @@ mg_status mgemm_masked_tactic(mg_dtype dt, const void* A, const uint8_t* SFA, co
   return from_cuda(launch_fwd_any(a, static_cast<cudaStream_t>(stream)));
 }
 
+mg_status mgemm_masked_exemplar(mg_dtype dt, const void* A, const uint8_t* SFA, const void* B,
+                                const uint8_t* SFB, void* D, const int32_t* d_valid_m, int32_t E,
+                                int32_t M_max, int32_t N, int32_t K, const mg_exemplar* d_table,
+                                int32_t n, int32_t* d_tactic_out, int32_t* d_status, void* stream) {
+  if (d_table == nullptr || n <= 0) return MG_ERR_INVALID_ARG;
+  if (!aligned16(d_table) || (d_tactic_out != nullptr && !aligned16(d_tactic_out))) return MG_ERR_INVALID_ARG;
+  if (E > kFusedExemplarMaxExperts || n > kSelMaxExemplars) return MG_ERR_UNSUPPORTED;
+  FwdArgs a;
+  const mg_status st = prep_masked(a, dt, A, SFA, B, SFB, D, d_valid_m, E, M_max, N, K, d_status);
+  if (st != MG_OK) return st;
+  a.table = d_table;
+  a.n_table = n;
+  a.tactic_out = d_tactic_out;
+  return from_cuda(launch_fwd_any(a, static_cast<cudaStream_t>(stream)));
+}
+
 mg_status kgemm_grouped(const void* dY, const void* X, float* dW, const int32_t* d_counts,
                         int32_t E, int64_t T_cap, int32_t N, int32_t K, int32_t* d_status,
                         void* stream) {

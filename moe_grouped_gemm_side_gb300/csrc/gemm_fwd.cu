@@ -120,6 +120,9 @@ struct Params {
   int32_t epi;       // kEpiPlain, kEpiSwigluBf16 or kEpiSwigluFp8
   int32_t sfy_ld;
   const int32_t* tactic;  // device {tile_q, blocks} chosen elsewhere on the GPU, or null
+  const mg_exemplar* table;  // exemplar table to match in the prologue (E <= 32), or null
+  int32_t n_table;
+  int32_t* tactic_out;    // with a table: the first CTA writes {tile_q, blocks, index}
 };
 
 struct Shared {
@@ -508,7 +511,80 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     int32_t q = p.tile_q;
     int32_t want_blocks = 0;  // 0: decided below from the tile count
-    if (p.tactic != nullptr) {
+    if (p.table != nullptr) {
+      // The exemplar choice of the separate select kernel (no history),
+      // made by every CTA's warp 0 for E <= 32: lane e holds expert e's
+      // count; the warp sorts them (descending, bitonic), forms the prefix
+      // sums, the 16 shares and the log feature, and takes the nearest
+      // exemplar (L1, ties to the lower index).  Integer arithmetic only,
+      // so every CTA makes the same choice.
+      int64_t c = (int32_t)lane < E ? (int64_t)cnt[lane] : 0;
+#pragma unroll
+      for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+          const int64_t o = __shfl_xor_sync(0xffffffffu, c, j);
+          const bool desc = (lane & (uint32_t)k) == 0, lower = (lane & (uint32_t)j) == 0;
+          c = (desc == lower) ? max(c, o) : min(c, o);
+        }
+      }
+      int64_t v = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int64_t nv = __shfl_up_sync(0xffffffffu, v, o);
+        if ((int)lane >= o) v += nv;
+      }
+      const int64_t U = __shfl_sync(0xffffffffu, v, E - 1);
+      int32_t share[kExemplarShares];
+#pragma unroll
+      for (int k = 0; k < kExemplarShares; ++k) {
+        const int32_t m = ((k + 1) * E + kExemplarShares - 1) / kExemplarShares;
+        const int64_t vm = __shfl_sync(0xffffffffu, v, m - 1);
+        share[k] = U > 0 ? (int32_t)((int64_t)kShareOne * vm / U) : 0;
+      }
+      int32_t lu = 0;
+      if (U > 0) {
+        const int e = 63 - __clzll(U);
+        lu = 16 * e + (int32_t)((16 * (U - (int64_t(1) << e))) >> e);
+      }
+      int64_t bd = INT64_MAX;
+      int32_t bi = 0x7fffffff;
+      for (int32_t i = (int32_t)lane; i < p.n_table; i += 32) {
+        int64_t d = (int64_t)kLuWeight * llabs((int64_t)lu - p.table[i].lu);
+#pragma unroll
+        for (int k = 0; k < kExemplarShares; ++k) d += llabs((int64_t)share[k] - p.table[i].share[k]);
+        if (d < bd) {
+          bd = d;
+          bi = i;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const int64_t od = __shfl_xor_sync(0xffffffffu, bd, o);
+        const int32_t oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (od < bd || (od == bd && oi < bi)) {
+          bd = od;
+          bi = oi;
+        }
+      }
+      const int32_t tq = p.table[bi].tile_q, tb = p.table[bi].blocks;
+      const bool ok = tq >= 16 && tq <= 256 && tq % 16 == 0 && (tb == 1 || tb == 2);
+      if (ok) {
+        q = tq;
+        want_blocks = min(tb, kBlocks);
+      } else if (lane == 0) {
+        set_status(p.status, MG_ERR_DEVICE_ARG);
+      }
+      if (blockIdx.x == 0 && lane == 0 && p.tactic_out != nullptr) {
+        p.tactic_out[0] = ok ? tq : 0;
+        p.tactic_out[1] = ok ? tb : 0;
+        p.tactic_out[2] = bi;
+      }
+    } else if (p.tactic != nullptr) {
+      // A tactic call may start while the kernel that writes the tactic is
+      // still running (programmatic dependent launch): the wait returns once
+      // that grid has completed and its writes are visible.
+      griddep_wait();
       const int32_t tq = p.tactic[0], tb = p.tactic[1];
       if (tq >= 16 && tq <= 256 && tq % 16 == 0 && (tb == 1 || tb == 2)) {
         q = tq;
@@ -1315,6 +1391,9 @@ cudaError_t launch(const FwdArgs& a, cudaStream_t s) {
   p.epi = a.epi;
   p.sfy_ld = a.sfy_ld;
   p.tactic = a.tactic;
+  p.table = a.table;
+  p.n_table = a.n_table;
+  p.tactic_out = a.tactic_out;
   p.status = a.status;
   p.wait_ns = a.wait_ns;
   p.E = a.E;
@@ -1332,13 +1411,24 @@ cudaError_t launch(const FwdArgs& a, cudaStream_t s) {
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kPair ? 2 : 1;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];
+  unsigned n_attr = 0;
+  if (kPair) {
+    attr[n_attr].id = cudaLaunchAttributeClusterDimension;
+    attr[n_attr].val.clusterDim.x = 2;
+    attr[n_attr].val.clusterDim.y = 1;
+    attr[n_attr].val.clusterDim.z = 1;
+    ++n_attr;
+  }
+  if (a.tactic != nullptr) {
+    // the prologue (TMEM, barriers, counts) overlaps the kernel that writes
+    // the tactic; the tactic itself is read after griddepcontrol.wait
+    attr[n_attr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n_attr].val.programmaticStreamSerializationAllowed = 1;
+    ++n_attr;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = kPair ? 1 : 0;
+  cfg.numAttrs = n_attr;
   return cudaLaunchKernelEx(&cfg, kernel, a.tmW, a.tmA64, a.tmA16, a.tmA8, a.tmSF, a.tmSFW, p);
 }
 

@@ -33,6 +33,9 @@ struct FwdArgs {
   int32_t sfy_ld = 0;
   int32_t* status = nullptr;
   const int32_t* tactic = nullptr;  // device {tile_q, blocks} or null
+  const mg_exemplar* table = nullptr;  // exemplar table matched in the prologue, or null
+  int32_t n_table = 0;
+  int32_t* tactic_out = nullptr;    // with a table: {tile_q, blocks, index} of the choice, or null
   int64_t wait_ns = 0;
   CUtensorMap tmW{}, tmA64{}, tmA16{}, tmA8{}, tmSF{};
   CUtensorMap tmSFW{};              // w4: weight scales [E*N, K/32]
@@ -64,6 +67,7 @@ constexpr int32_t kShareOne = 65536;
 constexpr int32_t kLuWeight = 2048;
 constexpr int kSelMaxExperts = 4096;
 constexpr int kSelMaxExemplars = 1024;
+constexpr int kFusedExemplarMaxExperts = 32;  // mgemm_masked_exemplar: one warp per CTA
 cudaError_t launch_exemplar(const int32_t* counts, int32_t E, const mg_exemplar* table, int32_t n,
                             int32_t margin, int32_t* state, int32_t* tactic, int32_t* status,
                             cudaStream_t s);

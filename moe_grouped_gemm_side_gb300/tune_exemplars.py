@@ -50,6 +50,20 @@ U_TUNE = {"contiguous": (32, 64, 128, 256, 512, 1024, 2048, 4096, 8192, 16384, 3
 U_EVAL = {"contiguous": (32, 48, 64, 96, 200, 1024, 1500, 3000, 6000, 12000, 24000, 32768),
           "masked": (24, 32, 48, 64, 96, 200, 454, 768, 1024, 1500)}
 SHAPES = (("dirichlet", 0.2), ("dirichlet", 1.0), ("dirichlet", 8.0), ("zipf", 1.2), ("zipf", 0.6))
+# masked form only: decode batches drawn like the decode workload (valid_m
+# per expert from a Zipf law on 0..M_max, at least 3 idle experts), so U is
+# whatever the draw gives; (exponent, seeds for tuning, held-out seeds)
+DECODE_SHAPES = ((0.8, range(3000, 3020), range(9500, 9506)), (1.1, range(3100, 3120), range(9600, 9606)),
+                 (1.4, range(3200, 3220), range(9700, 9706)), (1.7, range(3300, 3320), range(9800, 9806)))
+
+
+def decode_histograms(E, M_max, held_out):
+    """(label, counts) of the decode-shaped histograms."""
+    out = []
+    for s_exp, tune_seeds, eval_seeds in DECODE_SHAPES:
+        for seed in (eval_seeds if held_out else tune_seeds):
+            out.append((f"zipf_decode({s_exp})", wl.counts_zipf_decode(seed=seed, E=E, M_max=M_max, s=s_exp)))
+    return out
 
 
 def histogram(shape, param, E, U, seed, cap=None):
@@ -161,21 +175,23 @@ def tune(args):
     U_set = [U for U in U_TUNE[args.form] if cap is None or U <= cap * args.E]
     bench = make_bench(args, args.form, U_set)
     sweeps = []
-    for U in U_set:
-        for i, (shape, param) in enumerate(SHAPES):
-            counts = histogram(shape, param, args.E, U, seed=2000 + 37 * i + U, cap=cap)
-            times, _ = bench.sweep(counts)
-            sweeps.append((U, shape, param, counts, times))
-            best = min(times, key=times.get)
-            print(f"U={U:6d} {shape}({param}): best {best} {times[best]:.1f} us", flush=True)
-    default = default_tactic([sw[4] for sw in sweeps])
+    hists = [(U, f"{shape}({param})", histogram(shape, param, args.E, U, seed=2000 + 37 * i + U, cap=cap))
+             for U in U_set for i, (shape, param) in enumerate(SHAPES)]
+    if args.form == "masked":
+        hists += [(sum(c), label, c) for label, c in decode_histograms(args.E, args.M_max, held_out=False)]
+    for U, label, counts in hists:
+        times, _ = bench.sweep(counts)
+        sweeps.append((U, label, counts, times))
+        best = min(times, key=times.get)
+        print(f"U={U:6d} {label}: best {best} {times[best]:.1f} us", flush=True)
+    default = default_tactic([sw[3] for sw in sweeps])
     exemplars = []
-    for U, shape, param, counts, times in sweeps:
+    for U, label, counts, times in sweeps:
         pick = pick_tactic(times, default, args.min_gain)
         tq, blocks = (int(x) for x in pick.split("x"))
         lu, shares = mb.exemplar_features_host(counts)
         exemplars.append({"lu": lu, "shares": shares, "tile_q": tq, "blocks": blocks, "U": U,
-                          "shape": f"{shape}({param})", "counts": counts, "times_us": times})
+                          "shape": label, "counts": counts, "times_us": times})
     differ = sum(1 for x in exemplars if f"{x['tile_q']}x{x['blocks']}" != default)
     print(f"default tactic {default}; {differ} of {len(exemplars)} exemplars keep another", flush=True)
     out = {"dtype": args.dtype, "form": args.form, "E": args.E, "N": args.N, "K": args.K,
@@ -207,30 +223,45 @@ def evaluate(args):
     fixed = [meta.get("default", "240x2" if meta["dtype"] == "fp8" else "256x2"), "32x1", "128x1"]
     fixed = list(dict.fromkeys(fixed))
     rows = []
-    for U in U_set:
-        for i, (shape, param) in enumerate(SHAPES):
-            counts = histogram(shape, param, meta["E"], U, seed=9000 + 53 * i + U, cap=cap)   # held out
-            times, d_counts = bench.sweep(counts)
-            best = min(times.values())
-            mb.select_exemplar(d_counts, d_table, len(table), bench.tactic, status=bench.status)
-            torch.cuda.synchronize()
-            tq, blocks, idx = bench.tactic.cpu().tolist()
-            t_ex = times[f"{tq}x{blocks}"]
-            t_cm = bench.time_builtin(d_counts)
-            lu, shares = mb.exemplar_features_host(counts)
-            rows.append({"U": U, "shape": f"{shape}({param})", "best_us": best, "best": min(times, key=times.get),
-                         "exemplar": f"{tq}x{blocks}", "exemplar_us": t_ex, "costmodel_us": t_cm,
-                         "fixed_us": {k: times[k] for k in fixed},
-                         "eff_experts": (sum(counts) ** 2 / max(1, sum(c * c for c in counts)))})
-            r = rows[-1]
-            print(f"U={U:6d} {r['shape']:15s} best {r['best']:6s} {best:8.1f}  exemplar {r['exemplar']:6s} "
-                  f"{t_ex:8.1f}  cost model {t_cm:8.1f}", flush=True)
+    hists = [(U, f"{shape}({param})", histogram(shape, param, meta["E"], U, seed=9000 + 53 * i + U, cap=cap))
+             for U in U_set for i, (shape, param) in enumerate(SHAPES)]   # held out
+    if form == "masked":
+        hists += [(sum(c), label, c) for label, c in decode_histograms(meta["E"], cap, held_out=True)]
+    for U, label, counts in hists:
+        times, d_counts = bench.sweep(counts)
+        best = min(times.values())
+        mb.select_exemplar(d_counts, d_table, len(table), bench.tactic, status=bench.status)
+        torch.cuda.synchronize()
+        tq, blocks, idx = bench.tactic.cpu().tolist()
+        t_ex = times[f"{tq}x{blocks}"]
+        t_cm = bench.time_builtin(d_counts)
+        lu, shares = mb.exemplar_features_host(counts)
+        # the real path: the select kernel, then the GEMM reading its tactic
+        t_path = bench._time(lambda: (mb.select_exemplar(d_counts, d_table, len(table), bench.tactic,
+                                                         status=bench.status), bench.run_tactic(d_counts)), 9)
+        # masked, E <= 32: the choice made inside the GEMM (no select kernel)
+        t_fused = None
+        if bench.form == "masked" and meta["E"] <= 32:
+            t_fused = bench._time(lambda: mb.mgemm_masked_exemplar(
+                bench.A, bench.B, bench.D, d_counts, d_table, len(table), SFA=bench.SFA, SFB=bench.SFB,
+                status=bench.status), 9)
+        rows.append({"U": U, "shape": label, "best_us": best, "best": min(times, key=times.get),
+                     "exemplar": f"{tq}x{blocks}", "exemplar_us": t_ex, "exemplar_path_us": t_path,
+                     "exemplar_in_gemm_us": t_fused,
+                     "costmodel_us": t_cm,
+                     "fixed_us": {k: times[k] for k in fixed},
+                     "eff_experts": (sum(counts) ** 2 / max(1, sum(c * c for c in counts)))})
+        r = rows[-1]
+        print(f"U={U:6d} {r['shape']:15s} best {r['best']:6s} {best:8.1f}  exemplar {r['exemplar']:6s} "
+              f"{t_ex:8.1f}  cost model {t_cm:8.1f}", flush=True)
 
     def geo(key):
         return math.exp(np.mean([math.log(r[key] / r["best_us"]) for r in rows]))
     fixed_keys = list(rows[0]["fixed_us"])
     summary = {"histograms": len(rows), "geomean_vs_best": {
-        "exemplar": geo("exemplar_us"), "cost_model": geo("costmodel_us"),
+        "exemplar": geo("exemplar_us"), "exemplar_with_select_kernel": geo("exemplar_path_us"),
+        **({"exemplar_in_gemm": geo("exemplar_in_gemm_us")} if rows[0]["exemplar_in_gemm_us"] else {}),
+        "cost_model": geo("costmodel_us"),
         **{f"fixed_{k}": math.exp(np.mean([math.log(r["fixed_us"][k] / r["best_us"]) for r in rows]))
            for k in fixed_keys}}}
     # hysteresis: a walk of neighbouring histograms around two bases

@@ -330,3 +330,9 @@ def test_exemplar_calls_reject_bad_arguments(lib):
     assert L.mgemm_contiguous_tactic(*t) == 1                                              # tactic NULL
     assert L.mgemm_masked_tactic(mb.MG_BF16, FAKE, None, FAKE, None, FAKE, FAKE, 8, 64, 256, 256, None,
                                  None, None) == 1
+    m = [mb.MG_BF16, FAKE, None, FAKE, None, FAKE, FAKE, 8, 64, 256, 256]
+    assert L.mgemm_masked_exemplar(*m, None, 4, None, None, None) == 1                     # table NULL
+    assert L.mgemm_masked_exemplar(*m, FAKE, 0, None, None, None) == 1                     # n
+    assert L.mgemm_masked_exemplar(*m, FAKE, 2000, None, None, None) == 2                  # n > 1024
+    m[7] = 33
+    assert L.mgemm_masked_exemplar(*m, FAKE, 4, None, None, None) == 2                     # E > 32

@@ -110,6 +110,9 @@ def test_exemplar_tuner_guardrail():
         for i, (shape, param) in enumerate(te.SHAPES):
             c = te.histogram(shape, param, 64, U, seed=2000 + 37 * i + U)
             assert len(c) == 64 and sum(c) == U and min(c) >= 0
+    for held_out in (False, True):
+        for label, c in te.decode_histograms(16, 256, held_out):
+            assert len(c) == 16 and max(c) <= 256 and sum(1 for x in c if x == 0) >= 3
     for U in te.U_TUNE["masked"] + te.U_EVAL["masked"]:
         for i, (shape, param) in enumerate(te.SHAPES):
             c = te.histogram(shape, param, 16, U, seed=9000 + 53 * i + U, cap=256)

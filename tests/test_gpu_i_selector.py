@@ -206,3 +206,40 @@ def test_select_and_gemm_in_one_graph(lib, cuda):
         Dbits = gu.bf16_bits(D)
         assert np.array_equal(Dbits[written], gu.round_bf16_bits(R[written]))
         assert (Dbits[~written] == gu.SENTINEL_BITS).all()
+
+
+def test_masked_exemplar_in_gemm_matches_oracle_and_tactic_call(lib, cuda):
+    """mgemm_masked_exemplar: every CTA makes the select kernel's choice
+    (margin 0, no history) in its prologue; the choice equals the oracle's and
+    the product equals the tactic call's with that choice, bit for bit."""
+    rng = random.Random(33)
+    M, N, K = 96, 512, 256
+    for trial in range(24):
+        E = rng.choice([1, 3, 16, 32])
+        n = rng.choice([1, 5, 40, 1024])
+        entries = random_table(rng, n)
+        for x in entries:
+            x["tile_q"] = min(x["tile_q"], 240)
+        d_table = mb.exemplar_table_device(mb.exemplar_table(entries), cuda)
+        valid = [rng.choice([0, 0, 1, 5, 16, 33, 80, 96]) for _ in range(E)]
+        A = wl.integer_bf16((E, M, K), 50 + trial, cuda)
+        B = wl.integer_bf16((E, N, K), 80 + trial, cuda)
+        d_valid = torch.tensor(valid, dtype=torch.int32, device=cuda)
+        out = torch.full((3,), -7, dtype=torch.int32, device=cuda)
+        status = torch.zeros(1, dtype=torch.int32, device=cuda)
+        D1 = gu.sentinel_like((E, M, N), cuda)
+        mb.mgemm_masked_exemplar(A, B, D1, d_valid, d_table, n, tactic_out=out, status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        want = osel.choose(valid, entries)
+        assert out.cpu().tolist() == [entries[want]["tile_q"], entries[want]["blocks"], want], trial
+        D2 = gu.sentinel_like((E, M, N), cuda)
+        mb.mgemm_masked_tactic(A, B, D2, d_valid, out, status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        assert torch.equal(D1.view(torch.int16), D2.view(torch.int16)), trial
+        if trial < 4:
+            R, written = og.masked(gu.deq_bf16(A).reshape(E, M, K), gu.deq_bf16(B).reshape(E, N, K), valid)
+            Dbits = gu.bf16_bits(D1).reshape(E, M, N)
+            assert np.array_equal(Dbits[written], gu.round_bf16_bits(R[written]))
+            assert (Dbits[~written] == gu.SENTINEL_BITS).all()
