@@ -344,6 +344,18 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
 }
+// Arrivals that publish no memory: a release arrive waits until the
+// thread's earlier global stores are performed at the arrive's scope (for a
+// cluster-scope arrive, ~1800 cycles behind a warp's burst of output
+// stores), which a signal that only hands back TMEM columns the thread has
+// finished reading (tcgen05.wait::ld) does not need.
+__device__ __forceinline__ void mbar_arrive_relaxed(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
 // TMA tile load whose completion is signalled on an mbarrier that may live in
 // the peer CTA of the pair (cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map,

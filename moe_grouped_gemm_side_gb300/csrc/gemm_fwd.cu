@@ -1328,8 +1328,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          if constexpr (kPair) mbar_arrive_cluster(acc_empty0);
-          else mbar_arrive(&sh.acc_empty[0]);
+          if constexpr (kPair) mbar_arrive_cluster_relaxed(acc_empty0);
+          else mbar_arrive_relaxed(&sh.acc_empty[0]);
         }
 #pragma unroll
         for (int j = 0; j < kParked; ++j) {
@@ -1342,8 +1342,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          if constexpr (kPair) mbar_arrive_cluster(acc_empty0);
-          else mbar_arrive(&sh.acc_empty[0]);
+          if constexpr (kPair) mbar_arrive_cluster_relaxed(acc_empty0);
+          else mbar_arrive_relaxed(&sh.acc_empty[0]);
         }
       }
       acc_phase ^= 1u;
