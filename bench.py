@@ -57,8 +57,9 @@ CONFIGS = [
 ]
 FP8_OVER_BF16 = 2.0   # nominal dense fp8 : bf16 tensor throughput ratio
 METRIC = "effective TFLOPS (valid rows only)"
-L2_NOTE = ("L2 flushed between timed reps: 2 x l2CacheSize bytes written, then a ~0.2 ms GPU spin, "
-           "both outside the CUDA events")
+L2_NOTE = ("L2 flushed between timed reps: 2 x l2CacheSize bytes written, 2 x l2CacheSize bytes of another "
+           "buffer read (the written lines go back to HBM before the rep), then a ~0.2 ms GPU spin, all outside "
+           "the CUDA events")
 
 
 def _binding():
@@ -631,10 +632,13 @@ def cpu_baseline(w, budget_s):
 
 
 class L2Flush:
-    """Writes 2 x l2CacheSize bytes between timed repetitions, so every rep
-    reads its operands from HBM; then the GPU spins ~0.2 ms, so the host has
-    queued the next start event and launch before the GPU reaches them (a
-    short GEMM's host-side preparation otherwise lands inside its events)."""
+    """Between timed repetitions: writes 2 x l2CacheSize bytes, so every rep
+    reads its operands from HBM; then reads 2 x l2CacheSize bytes of a second
+    buffer, so the written lines are written back to HBM here rather than
+    while the next rep runs (the write-back of the flush's own dirty lines is
+    not the GEMM's cost); then the GPU spins ~0.2 ms, so the host has queued
+    the next start event and launch before the GPU reaches them (a short
+    GEMM's host-side preparation otherwise lands inside its events)."""
 
     SETTLE_CYCLES = 400_000
 
@@ -642,9 +646,12 @@ class L2Flush:
         l2 = torch.cuda.get_device_properties(dev).L2_cache_size
         self.bytes = 2 * int(l2)
         self.buf = torch.empty(self.bytes, dtype=torch.uint8, device=dev)
+        self.clean = torch.ones(self.bytes // 4, dtype=torch.int32, device=dev)
+        self.sink = torch.empty((), dtype=torch.int64, device=dev)
 
     def __call__(self):
         self.buf.fill_(1)
+        torch.sum(self.clean, dim=0, out=self.sink)
         torch.cuda._sleep(self.SETTLE_CYCLES)
 
 

@@ -110,15 +110,6 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, uin
   }
 }
 
-// Programmatic dependent launch: a grid launched with programmatic stream
-// serialization waits here until the grid before it has completed and its
-// memory is visible (a no-op for an ordinary launch); the grid before it lets
-// its dependents launch early with griddep_launch_dependents.
-__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void griddep_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
 // Drain wait used on the way out: ignores the abort flag, still bounded.
 __device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity, uint64_t deadline) {
   while (!mbar_try_wait_sleep(bar, parity, kWaitHintNs)) {

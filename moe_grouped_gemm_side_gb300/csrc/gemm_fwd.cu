@@ -19,7 +19,9 @@
 // without adding a CPU stall").  A weight block is 128 rows on one SM
 // (cta_group::1) or 256 rows on the two SMs of a cluster (kPair,
 // cta_group::2: each SM holds 128 weight rows and half of the token rows,
-// and the MMA reads the other half from the peer).
+// and the MMA reads the other half from the peer).  With kTokM the roles
+// swap: 128 token rows on M, the tile's 256 weight rows on N, one MMA per
+// K-step for both blocks, one issuing warp.
 //
 // Why bigger tiles.  Every MMA reads both operands from shared memory while
 // TMA writes the next stages into it; with one 128-row block a K-block stage
@@ -581,10 +583,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         p.tactic_out[2] = bi;
       }
     } else if (p.tactic != nullptr) {
-      // A tactic call may start while the kernel that writes the tactic is
-      // still running (programmatic dependent launch): the wait returns once
-      // that grid has completed and its writes are visible.
-      griddep_wait();
       const int32_t tq = p.tactic[0], tb = p.tactic[1];
       if (tq >= 16 && tq <= 256 && tq % 16 == 0 && (tb == 1 || tb == 2)) {
         q = tq;
@@ -1411,20 +1409,13 @@ cudaError_t launch(const FwdArgs& a, cudaStream_t s) {
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = s;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[1];
   unsigned n_attr = 0;
   if (kPair) {
     attr[n_attr].id = cudaLaunchAttributeClusterDimension;
     attr[n_attr].val.clusterDim.x = 2;
     attr[n_attr].val.clusterDim.y = 1;
     attr[n_attr].val.clusterDim.z = 1;
-    ++n_attr;
-  }
-  if (a.tactic != nullptr) {
-    // the prologue (TMEM, barriers, counts) overlaps the kernel that writes
-    // the tactic; the tactic itself is read after griddepcontrol.wait
-    attr[n_attr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[n_attr].val.programmaticStreamSerializationAllowed = 1;
     ++n_attr;
   }
   cfg.attrs = attr;

@@ -149,9 +149,6 @@ __global__ void __launch_bounds__(kPlanThreads)
   __shared__ int64_t best_d[32];
   __shared__ int32_t best_i[32];
   const int tid = threadIdx.x;
-  // a tactic GEMM launched after this kernel may start its prologue now; it
-  // reads the tactic only once this grid has completed
-  griddep_launch_dependents();
   int32_t P = 2;
   while (P < E) P <<= 1;
   for (int32_t i = tid; i < P; i += kPlanThreads) v[i] = i < E ? (int64_t)max(counts[i], 0) : 0;

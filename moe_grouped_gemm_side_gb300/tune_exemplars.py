@@ -107,6 +107,8 @@ class Bench:
         self.tactic = torch.zeros(3, dtype=torch.int32, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # larger than L2
+        self.clean = torch.ones(64 << 20, dtype=torch.int32, device=dev)      # 256 MB, read after the write
+        self.sink = torch.empty((), dtype=torch.int64, device=dev)
 
     def _time(self, fn, reps):
         for _ in range(2):
@@ -114,6 +116,9 @@ class Bench:
         ts = []
         for _ in range(reps):
             self.flush.zero_()
+            # reading another buffer writes the flushed lines back to HBM now,
+            # not during the timed call
+            torch.sum(self.clean, dim=0, out=self.sink)
             # the GPU spins ~0.2 ms so the launch below is queued before the
             # start event is reached (its host-side checks stay outside)
             torch.cuda._sleep(400_000)
