@@ -607,7 +607,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tiles[i] = s;
       }
       const int variant = kPair ? (kBlocks == 2 ? kFwdPairDual : kFwdPair) : (kBlocks == 2 ? kFwdDual : kFwdSingle);
-      q = pick_tile(p.fp8 != 0, tiles, variant, p.N, sel_kblocks(p.fp8 != 0, p.K), (int)gridDim.x);
+      if (p.masked && kBlocks == 2 && !kPair && !kTokM && p.epi == kEpiPlain && want_blocks == 0) {
+        // masked: tile and blocks per tile priced together
+        int pb = 2;
+        pick_tile_blocks(p.fp8 != 0, tiles, p.N, sel_kblocks(p.fp8 != 0, p.K), (int)gridDim.x, &q, &pb);
+        want_blocks = pb;
+      } else {
+        q = pick_tile(p.fp8 != 0, tiles, variant, p.N, sel_kblocks(p.fp8 != 0, p.K), (int)gridDim.x);
+      }
     }
     q = min(q, q_cap);
     // The two-block kernel runs one-block tiles when two-block tiles would

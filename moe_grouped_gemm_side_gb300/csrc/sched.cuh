@@ -129,4 +129,32 @@ MG_HD int pick_tile(bool fp8, const int64_t (&token_tiles)[kNumTileCand], int va
   return best_q;
 }
 
+// Masked form on the single-SM two-block kernel: the token tile and the
+// weight blocks per tile (one or two 128-row blocks) chosen together, every
+// (q, blocks) candidate priced as pick_tile prices a tile size: whole waves
+// of tiles over the SMs times the cost of one tile.  (Choosing q for
+// two-block tiles first and switching to one block when two-block tiles
+// would not fill two waves came out 7 % above the fastest candidate on the
+// tuning sweeps of the decode table, against 1.7 % for the joint choice.)
+// Ties go to the larger tile, then to two blocks.
+MG_HD void pick_tile_blocks(bool fp8, const int64_t (&token_tiles)[kNumTileCand], int64_t N, int64_t KB,
+                            int num_sms, int* q_out, int* blocks_out) {
+  int64_t best = -1;
+  int bq = tile_candidate(fp8, kNumTileCand - 1), bb = 2;
+  for (int i = 0; i < kNumTileCand; ++i) {
+    const int q = tile_candidate(fp8, i);
+    for (int nb = 1; nb <= 2; ++nb) {
+      const int64_t T = token_tiles[i] * (N / (128 * nb));
+      const int64_t cost = cdiv64(T, num_sms > 0 ? num_sms : 1) * tile_cost_cycles(fp8, q, KB, nb, q);
+      if (best < 0 || cost <= best) {
+        best = cost;
+        bq = q;
+        bb = nb;
+      }
+    }
+  }
+  *q_out = bq;
+  *blocks_out = bb;
+}
+
 }  // namespace mg

@@ -257,7 +257,7 @@ def evaluate(args):
                      "exemplar": f"{tq}x{blocks}", "exemplar_us": t_ex, "exemplar_path_us": t_path,
                      "exemplar_in_gemm_us": t_fused,
                      "costmodel_us": t_cm,
-                     "fixed_us": {k: times[k] for k in fixed},
+                     "fixed_us": {k: times[k] for k in fixed}, "times_us": times,
                      "eff_experts": (sum(counts) ** 2 / max(1, sum(c * c for c in counts)))})
         r = rows[-1]
         print(f"U={U:6d} {r['shape']:15s} best {r['best']:6s} {best:8.1f}  exemplar {r['exemplar']:6s} "

@@ -156,9 +156,11 @@ def test_empty_and_degenerate():
     assert p.pad_frac == 0.0 and p.eff_experts == 0.0 and p.tiles == []
     p = op.plan([1], 256)
     assert p.P == 256 and p.tiles == [(0, 0, 1)] and p.eff_experts == 1.0
+    # P past 2^31 (with a wide tile, so the tile list stays short)
     huge = [2 ** 31 - 1] * 3
-    p = op.plan(huge, 128)
-    assert p.P == 3 * 128 * math.ceil((2 ** 31 - 1) / 128)
+    p = op.plan(huge, 1 << 20)
+    assert p.P == 3 * (1 << 20) * math.ceil((2 ** 31 - 1) / (1 << 20)) and p.P > 2 ** 32
+    assert p.num_tiles == 3 * 2048 and p.U == 3 * (2 ** 31 - 1)
     with pytest.raises(ValueError):
         op.plan([1, -1], 8)
     with pytest.raises(ValueError):
