@@ -482,6 +482,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
 
+  // One SM: the issuing warps allocate their TMEM while warp 0 builds the
+  // schedule (allocation and schedule each took ~1500 and ~19000 cycles of
+  // the prologue, one after the other).
+  if constexpr (!kPair) {
+    if (warp == 1) tmem_alloc_keep_permit(&sh.tmem_base, !kTokM ? 256u : kTmemCols);
+    if (!kTokM && warp == kMma2Warp) tmem_alloc_keep_permit(&sh.tmem_base2, 256u);
+  }
+
   // ---- schedule (warp 0): row bases, token tile, tile prefix
   if (warp == 0) {
     if (p.masked) {
@@ -490,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int64_t carry = 0;
       for (int32_t b = 0; b < E; b += 32) {
         const int32_t e = b + lane;
-        const int64_t own = e < E ? (int64_t)p.align_q * cdiv64(cnt[e], p.align_q) : 0;
+        const int64_t own = e < E ? (int64_t)p.align_q * cdiv_u32((uint32_t)cnt[e], (uint32_t)p.align_q) : 0;
         int64_t v = own;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -601,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < kNumTileCand; ++i) {
         int64_t s = 0;
-        for (int32_t e = lane; e < E; e += 32) s += cdiv64(cnt[e], tile_candidate(p.fp8, i));
+        for (int32_t e = lane; e < E; e += 32) s += cdiv_u32((uint32_t)cnt[e], (uint32_t)tile_candidate(p.fp8, i));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
         tiles[i] = s;
@@ -627,7 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       nblk = want_blocks;
     } else if (kBlocks == 2 && p.epi == kEpiPlain) {  // a SwiGLU epilogue needs gate and up in one tile
       int64_t tt = 0;
-      for (int32_t e = lane; e < E; e += 32) tt += cdiv64(cnt[e], q);
+      for (int32_t e = lane; e < E; e += 32) tt += cdiv_u32((uint32_t)cnt[e], (uint32_t)q);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) tt += __shfl_xor_sync(0xffffffffu, tt, o);
       if (tt * (p.N / (2 * kBlockRows)) < 2 * (int64_t)n_units) nblk = 1;
@@ -637,7 +645,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int32_t b = 0; b < E; b += 32) {
       const int32_t e = b + lane;
       const int32_t c = e < E ? cnt[e] : 0;
-      const int32_t own = (int32_t)cdiv64(c, q) * NB;
+      const int32_t own = (int32_t)cdiv_u32((uint32_t)c, (uint32_t)q) * NB;
       if (c > 0) qmax = max(qmax, min(q, round_up16(c)));
       int32_t v = own;
 #pragma unroll
@@ -661,7 +669,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int32_t b = 0; b < E; b += 32) {
         const int32_t e = b + lane;
         const int32_t c = e < E ? cnt[e] : 0;
-        const int32_t nt = (int32_t)cdiv64(c, q);
+        const int32_t nt = (int32_t)cdiv_u32((uint32_t)c, (uint32_t)q);
         const int32_t nfull = c % q == 0 ? nt : nt - 1;
         int32_t v = nfull;
 #pragma unroll
@@ -678,7 +686,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int32_t b = 0; b < E; b += 32) {
           const int32_t e = b + lane;
           const int32_t c = e < E ? cnt[e] : 0;
-          const int32_t nt = (int32_t)cdiv64(c, q);
+          const int32_t nt = (int32_t)cdiv_u32((uint32_t)c, (uint32_t)q);
           const bool hit = c % q != 0 && round_up16(c - (nt - 1) * q) == w;
           const uint32_t m = __ballot_sync(0xffffffffu, hit);
           if (hit) ttab[pcarry + __popc(m & ((1u << lane) - 1u))] = (e << 16) | (nt - 1);
@@ -713,9 +721,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // words follow at 256-267.
   const bool two_issuers = !kTokM;
   if constexpr (!kPair) {
-    if (warp == 1) tmem_alloc_keep_permit(&sh.tmem_base, two_issuers ? 256u : kTmemCols);
-    if (two_issuers && warp == kMma2Warp) tmem_alloc_keep_permit(&sh.tmem_base2, 256u);
-    __syncthreads();
+    // (allocated before the schedule; both allocations are made by now)
     if (warp == 1) tmem_relinquish();
   } else {
     // pair allocations are made by one warp in each CTA; one at a time, so
