@@ -605,14 +605,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the narrower ring stages leave room for more of them).
     if (kTokM && q == 0) q = 128;  // the MMA computes 128 token rows whatever the tile
     if (q == 0) {
-      int64_t tiles[kNumTileCand];
+      // token tiles per candidate (32, 64, 128, then 240 or 256): shifts
+      // for the powers of two, one division for 240
+      int64_t tiles[kNumTileCand] = {0, 0, 0, 0};
+      static_assert(kNumTileCand == 4, "four tile candidates");
+      for (int32_t e = lane; e < E; e += 32) {
+        const uint32_t c = (uint32_t)cnt[e];
+        tiles[0] += (c + 31u) >> 5;
+        tiles[1] += (c + 63u) >> 6;
+        tiles[2] += (c + 127u) >> 7;
+        tiles[3] += p.fp8 ? cdiv_u32(c, 240u) : (c + 255u) >> 8;
+      }
 #pragma unroll
       for (int i = 0; i < kNumTileCand; ++i) {
-        int64_t s = 0;
-        for (int32_t e = lane; e < E; e += 32) s += cdiv_u32((uint32_t)cnt[e], (uint32_t)tile_candidate(p.fp8, i));
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        tiles[i] = s;
+        for (int o = 16; o > 0; o >>= 1) tiles[i] += __shfl_xor_sync(0xffffffffu, tiles[i], o);
       }
       const int variant = kPair ? (kBlocks == 2 ? kFwdPairDual : kFwdPair) : (kBlocks == 2 ? kFwdDual : kFwdSingle);
       if (p.masked && kBlocks == 2 && !kPair && !kTokM && p.epi == kEpiPlain && want_blocks == 0) {
@@ -682,15 +689,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         fcarry += __shfl_sync(0xffffffffu, v, 31);
       }
       int32_t pcarry = fcarry;
-      for (int32_t w = round_up16(q); w >= 16; w -= 16) {
-        for (int32_t b = 0; b < E; b += 32) {
-          const int32_t e = b + lane;
-          const int32_t c = e < E ? cnt[e] : 0;
-          const int32_t nt = (int32_t)cdiv_u32((uint32_t)c, (uint32_t)q);
-          const bool hit = c % q != 0 && round_up16(c - (nt - 1) * q) == w;
+      if (E <= 32) {
+        // one expert per lane: its trimmed last tile's width, found once
+        const int32_t c = (int32_t)lane < E ? cnt[lane] : 0;
+        const int32_t nt = (int32_t)cdiv_u32((uint32_t)c, (uint32_t)q);
+        const int32_t lw = (c % q != 0) ? round_up16(c - (nt - 1) * q) : 0;
+        for (int32_t w = round_up16(q); w >= 16; w -= 16) {
+          const bool hit = lw == w;
           const uint32_t m = __ballot_sync(0xffffffffu, hit);
-          if (hit) ttab[pcarry + __popc(m & ((1u << lane) - 1u))] = (e << 16) | (nt - 1);
+          if (hit) ttab[pcarry + __popc(m & ((1u << lane) - 1u))] = ((int32_t)lane << 16) | (nt - 1);
           pcarry += __popc(m);
+        }
+      } else {
+        for (int32_t w = round_up16(q); w >= 16; w -= 16) {
+          for (int32_t b = 0; b < E; b += 32) {
+            const int32_t e = b + lane;
+            const int32_t c = e < E ? cnt[e] : 0;
+            const int32_t nt = (int32_t)cdiv_u32((uint32_t)c, (uint32_t)q);
+            const bool hit = c % q != 0 && round_up16(c - (nt - 1) * q) == w;
+            const uint32_t m = __ballot_sync(0xffffffffu, hit);
+            if (hit) ttab[pcarry + __popc(m & ((1u << lane) - 1u))] = (e << 16) | (nt - 1);
+            pcarry += __popc(m);
+          }
         }
       }
     }
