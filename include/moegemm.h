@@ -411,8 +411,11 @@ int64_t mg_get_wait_limit_ns(void);
  *   4: SM pair, two blocks (512 rows; needs N % 512 == 0);
  *   5: single SM, tokens on M, 256 weight rows (needs N % 256 == 0).
  * A family whose tile does not divide N falls back to the next narrower one
- * (4 -> 3 -> 1, 2 -> 1, 5 -> 1, 0 -> 1).  Results are identical up to fp32
- * summation order.
+ * (4 -> 3 -> 1, 2 -> 1, 5 -> 1, 0 -> 1).  The two-block families run
+ * one-block tiles where the device finds them cheaper from the counts
+ * (contiguous form: when two-block tiles would not fill two waves of
+ * workers; masked form: priced together with the token tile).  Results are
+ * identical up to fp32 summation order.
  * Process-wide.  Returns MG_ERR_INVALID_ARG for other values.
  * ------------------------------------------------------------------------ */
 mg_status mg_set_kernel_policy(int32_t policy);
