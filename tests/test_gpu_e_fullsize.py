@@ -90,10 +90,16 @@ def test_prefill_fp8_gemm2_every_expert_all_rows(lib, cuda):
 
 def _row_sample(t, q, rng, extra=8):
     """Rows of an expert to check: its first rows, the rows of its last
-    token tile (trimmed to a multiple of 16 by the kernel, capped at 48),
-    and a few random rows."""
-    last0 = (t // q) * q if t % q else max(0, t - q)
+    token tile (capped at 48) and the rows on either side of every other
+    tile boundary, and a few random rows.  The kernel splits an expert's
+    ceil(t / q) token tiles evenly (widths rounded up to 16, the last tile
+    trimmed)."""
+    n = -(-t // q)
+    w = -(-(-(-t // n)) // 16) * 16
+    last0 = (n - 1) * w
     rows = set(range(min(t, 8))) | set(range(last0, min(t, last0 + 48)))
+    for j in range(1, n):
+        rows |= {j * w - 1, j * w}
     rows |= set(int(r) for r in rng.integers(0, t, size=min(extra, t)))
     return np.array(sorted(rows))
 
@@ -102,7 +108,8 @@ def _row_sample(t, q, rng, extra=8):
 def test_prefill_fp8_every_expert_row_sample(lib, cuda, gemm_index):
     """Skewed FP8 prefill, both GEMMs: every expert, on a row sample that
     holds the rows of its last token tile at the tile the device chose (the
-    one the kernel trims), the first rows and random rows; the per-expert
+    one the kernel trims), the rows around its tile boundaries, the first
+    rows and random rows; the per-expert
     Frobenius rule applies to the sampled rows, all columns."""
     name = "prefill_fp8_e64_t32768_n4096_k7168"
     counts, p, ops, Dbits = _contiguous_full(name, cuda, gemm_index)
