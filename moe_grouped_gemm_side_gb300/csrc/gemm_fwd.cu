@@ -632,7 +632,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (p.masked && kBlocks == 2 && !kPair && !kTokM && p.epi == kEpiPlain && want_blocks == 0) {
         // masked: tile and blocks per tile priced together
         int pb = 2;
-        pick_tile_blocks(p.fp8 != 0, tiles, p.N, sel_kblocks(p.fp8 != 0, p.K), (int)gridDim.x, &q, &pb);
+        // the ring's bytes and per-stage scale bytes as laid out below
+        const int64_t ring = kSmemBytes - 2048 - (int64_t)(reinterpret_cast<uintptr_t>(sf_area) -
+                                                          reinterpret_cast<uintptr_t>(smem));
+        const int64_t sfb = p.fp8 ? kSfStage + (kW4 ? kWsfArea : 0) : 0;
+        pick_tile_blocks(p.fp8 != 0, kW4, tiles, p.N, sel_kblocks(p.fp8 != 0, p.K), (int)gridDim.x, ring, sfb, &q,
+                         &pb);
         want_blocks = pb;
       } else {
         q = pick_tile(p.fp8 != 0, tiles, variant, p.N, sel_kblocks(p.fp8 != 0, p.K), (int)gridDim.x);

@@ -86,13 +86,20 @@ constexpr int64_t kSelMmaSlopeX10Bf16 = 21, kSelMmaSlopeX10Fp8 = 27;  // cycles 
 constexpr int64_t kSelMmaFloorBf16 = 350, kSelMmaFloorFp8 = 600;      // cycles per K-block and block
 constexpr int64_t kSelLoadNum = 8, kSelLoadDen = 5;  // cycles per 128-byte row (1.6)
 constexpr int64_t kSelTileOverhead = 2500;        // per tile
+// Round trip of a stage's loads when every SM streams weights from DRAM
+// (masked decode batches), in SM cycles: a ring of S stages cannot turn a
+// stage over faster than this over S.  Fitted to in-kernel clock stamps of
+// the 16-expert decode with E2M1 weights (five 40 KB stages at ~814
+// cycles, a third of them waiting for data).
+constexpr int64_t kSelLoadRoundTrip = 4000;
 
-MG_HD int64_t tile_cost_cycles(bool fp8, int q, int64_t KB, int w_blocks, int b_rows) {
+// stage_floor: a lower bound on the cycles of one stage (0: none).
+MG_HD int64_t tile_cost_cycles(bool fp8, int q, int64_t KB, int w_blocks, int b_rows, int64_t stage_floor = 0) {
   const int64_t per_block = fp8 ? max64(kSelMmaSlopeX10Fp8 * q / 10, kSelMmaFloorFp8)
                                 : max64(kSelMmaSlopeX10Bf16 * q / 10, kSelMmaFloorBf16);
   const int64_t mma = per_block * w_blocks;
   const int64_t load = (128 * (int64_t)w_blocks + b_rows) * kSelLoadNum / kSelLoadDen;
-  return KB * max64(mma, load) + kSelTileOverhead;
+  return KB * max64(max64(mma, load), stage_floor) + kSelTileOverhead;
 }
 
 // Number of 128-byte K blocks of one operand row: the unit tile_cost_cycles
@@ -146,16 +153,30 @@ MG_HD int pick_tile(bool fp8, const int64_t (&token_tiles)[kNumTileCand], int va
 // two-block tiles first and switching to one block when two-block tiles
 // would not fill two waves came out 7 % above the fastest candidate on the
 // tuning sweeps of the decode table, against 1.7 % for the joint choice.)
+// E2M1 weights (w4) fill 16 KB of shared memory per block and stage for 8 KB
+// of DRAM data, so the ring holds half the weight bytes in flight and the
+// decode waits on loads: their launches take two-block tiles only, and a
+// stage costs at least the load round trip over the stages the ring holds
+// (ring_bytes / (128-byte rows of both blocks and the tile, plus sf_bytes of
+// scale data per stage)).  Replayed on the measured tactic sweeps of the
+// decode table's 68 held-out histograms with E2M1 weights, this rule lands
+// at 1.012 of the fastest tactic against 1.043 for the joint rule (the
+// 16-expert decode: 64 x 2 tiles, 0.092 ms, rather than 128 x 1, 0.104).
+// With E4M3 weights the floor made the choice worse (measured 1.038 ->
+// 1.076), so it stays off there.
 // Ties go to the larger tile, then to two blocks.
-MG_HD void pick_tile_blocks(bool fp8, const int64_t (&token_tiles)[kNumTileCand], int64_t N, int64_t KB,
-                            int num_sms, int* q_out, int* blocks_out) {
+MG_HD void pick_tile_blocks(bool fp8, bool w4, const int64_t (&token_tiles)[kNumTileCand], int64_t N, int64_t KB,
+                            int num_sms, int64_t ring_bytes, int64_t sf_bytes, int* q_out, int* blocks_out) {
   int64_t best = -1;
   int bq = tile_candidate(fp8, kNumTileCand - 1), bb = 2;
   for (int i = 0; i < kNumTileCand; ++i) {
     const int q = tile_candidate(fp8, i);
-    for (int nb = 1; nb <= 2; ++nb) {
+    for (int nb = w4 ? 2 : 1; nb <= 2; ++nb) {
       const int64_t T = token_tiles[i] * (N / (128 * nb));
-      const int64_t cost = cdiv_fast(T, num_sms > 0 ? num_sms : 1) * tile_cost_cycles(fp8, q, KB, nb, q);
+      const int64_t stage = 128 * (128 * (int64_t)nb + q) + sf_bytes;
+      const int64_t S = (w4 && ring_bytes > 0) ? max64(1, ring_bytes / stage) : 0;
+      const int64_t floor = S > 0 ? kSelLoadRoundTrip / (S < 16 ? S : 16) : 0;
+      const int64_t cost = cdiv_fast(T, num_sms > 0 ? num_sms : 1) * tile_cost_cycles(fp8, q, KB, nb, q, floor);
       if (best < 0 || cost <= best) {
         best = cost;
         bq = q;
