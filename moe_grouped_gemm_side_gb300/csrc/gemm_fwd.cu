@@ -90,7 +90,18 @@ constexpr int kSfW1 = kSfStageBytes;             // offset of block-1 weight wor
 // scales of row i + 32 j), the layout tcgen05.cp.32x128b.warpx4 expects.
 constexpr int kWsfBytes = kCtaRows * 16;
 constexpr int kWsfAtom = 32 * 16;
-constexpr int kWsfArea = 2 * kWsfBytes + 2 * kWsfAtom;
+// The boxes arrive once per group of four K-blocks, into a ring of
+// kW4Groups group slots (both blocks' boxes per slot) ahead of the stage
+// ring; every stage keeps only its two atoms.  (A box in every stage took
+// 8 KB of scale data per stage: one stage fewer in the ring, and the decode
+// waited on its loads.)  The scale warp releases a slot (sf_grp) when it
+// starts the next group, and the producer reloads it only after that.  Two
+// slots hold 8 KB where the boxes took 4 KB in every stage: two-block tiles
+// of 128 tokens keep four stages in the ring instead of three.
+constexpr int kW4Groups = 2;
+constexpr int kW4GroupBytes = 2 * kWsfBytes;
+constexpr int kW4Area = kW4Groups * kW4GroupBytes;
+constexpr int kW4StageBytes = 2 * kWsfAtom;
 static_assert(kSfStage % 1024 == 0 && kWsfBytes % 1024 == 0 && kWsfAtom % 16 == 0,
               "TMA and tcgen05.cp sources stay aligned");
 constexpr int kGroupTiles = 8;                   // token tiles per raster group
@@ -471,7 +482,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // initialised once the block count of the launch is known)
     for (int i = 0; i < 2; ++i) mbar_init(&sh.amax_bar[i], 4 * 32);
     for (int i = 0; i < kGRing; ++i) {
-      mbar_init(&sh.sf_grp[i], 2);
+      // pairs: both CTAs' scale warps publish a group; FP4 weights on one SM:
+      // the scale warp releases a weight-scale group slot
+      mbar_init(&sh.sf_grp[i], kPair ? 2 : 1);
       mbar_init(&sh.g_full[i], 1);
     }
     sh.abort_flag = 0;
@@ -633,11 +646,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // masked: tile and blocks per tile priced together
         int pb = 2;
         // the ring's bytes and per-stage scale bytes as laid out below
-        const int64_t ring = kSmemBytes - 2048 - (int64_t)(reinterpret_cast<uintptr_t>(sf_area) -
-                                                          reinterpret_cast<uintptr_t>(smem));
-        const int64_t sfb = p.fp8 ? kSfStage + (kW4 ? kWsfArea : 0) : 0;
-        pick_tile_blocks(p.fp8 != 0, kW4, tiles, p.N, sel_kblocks(p.fp8 != 0, p.K), (int)gridDim.x, ring, sfb, &q,
-                         &pb);
+        const int64_t ring = kSmemBytes - 2048 - (kW4 ? kW4Area : 0) -
+                             (int64_t)(reinterpret_cast<uintptr_t>(sf_area) - reinterpret_cast<uintptr_t>(smem));
+        const int64_t sfb = p.fp8 ? kSfStage + (kW4 ? kW4StageBytes : 0) : 0;
+        pick_tile_blocks(p.fp8 != 0, kW4, tiles, p.N, sel_kblocks(p.fp8 != 0, p.K), (int)gridDim.x, ring, sfb,
+                         kMaxStages, &q, &pb);
         want_blocks = pb;
       } else {
         q = pick_tile(p.fp8 != 0, tiles, variant, p.N, sel_kblocks(p.fp8 != 0, p.K), (int)gridDim.x);
@@ -790,9 +803,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       nblk * kWTileBytes + (kTokM ? 128 : (kPair ? sh.qn_max / 2 : sh.qn_max)) * kRowBytes;
   // scale data: per stage on one SM; a ring of groups for a pair
   const bool gring = kPair && p.fp8;
-  const int32_t sf_bytes = (p.fp8 && !kPair) ? kSfStage + (kW4 ? kWsfArea : 0) : 0;
-  const int32_t grp_area = gring ? kGRing * kSfStage : 0;
+  const int32_t sf_bytes = (p.fp8 && !kPair) ? kSfStage + (kW4 ? kW4StageBytes : 0) : 0;
+  // a pair's ring of scale groups, or (FP4 weights) the weight-scale group ring
+  const int32_t grp_area = gring ? kGRing * kSfStage : (kW4 ? kW4Area : 0);
   uint8_t* gbuf = sf_area;
+  uint8_t* sfst = sf_area + grp_area;  // one SM: the stages' scale areas
   const int32_t avail = kSmemBytes - 1024 - (int32_t)(reinterpret_cast<uintptr_t>(sf_area) -
                                                      reinterpret_cast<uintptr_t>(smem)) - 1024 - grp_area;
   int32_t S = avail / (stage_bytes + sf_bytes);
@@ -819,6 +834,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t stage = 0, phase = 0;
       int64_t issued = 0;
       int64_t gload = 0;  // pairs, fp8: scale groups loaded into the ring
+      int64_t w4load = 0;  // FP4 weights: weight-scale groups loaded
       auto load_group = [&](const Tile& gt, int32_t g) {
         const uint32_t slot = (uint32_t)(gload % kGRing);
         mbar_arrive_expect_tx(&sh.g_full[slot], (uint32_t)kSfRaw);
@@ -845,6 +861,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
+          if (kW4 && group && w4load >= kW4Groups) {
+            // the scale warp has moved past the group this slot held
+            const uint32_t slot = (uint32_t)(w4load % kW4Groups);
+            if (!wait_bounded(&sh.sf_grp[slot], (uint32_t)(((w4load / kW4Groups) - 1) & 1), deadline, &sh.abort_flag,
+                              p.status)) {
+              ok = false;
+              break;
+            }
+            fence_proxy_async_smem();
+          }
           uint8_t* sw = ring + (size_t)stage * stage_bytes;
           uint8_t* sa = sw + nblk * kWTileBytes;
           if (leader) {
@@ -856,16 +882,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           // first: the 1 KB lands well before the operands, so warp 6 builds
           // the scale words while the operands are still in flight.
           if (p.fp8 && !gring) {
-            uint8_t* sfs = sf_area + (size_t)stage * sf_bytes;
-            // FP4 weights: every stage loads each block's scale box of its
-            // group of four K-blocks (16 bytes per row: the TMA minimum)
-            const uint32_t wsf_tx = kW4 ? (uint32_t)(nblk * kWsfBytes) : 0u;
-            mbar_arrive_expect_tx(&sh.sf_full[stage], (group ? (uint32_t)kSfRaw : 0u) + wsf_tx);
+            uint8_t* sfs = sfst + (size_t)stage * sf_bytes;
+            mbar_arrive_expect_tx(&sh.sf_full[stage], group ? (uint32_t)kSfRaw : 0u);
             if (group) tma_load_3d(sfs, &tmSF, &sh.sf_full[stage], tl.sf_x, kb, tl.sf_z);
-            if (kW4)
+            if (kW4 && group) {
+              // FP4 weights: each block's scale box of the group of four
+              // K-blocks (16 bytes per row: the TMA minimum), once per group
+              const uint32_t slot = (uint32_t)(w4load % kW4Groups);
+              mbar_arrive_expect_tx(&sh.g_full[slot], (uint32_t)(nblk * kWsfBytes));
               for (int32_t b = 0; b < nblk; ++b)
-                tma_load_2d(sfs + kSfStage + b * kWsfBytes, &tmSFW, &sh.sf_full[stage], (kb & ~3) * 4,
-                            wy + b * kBlockRows);
+                tma_load_2d(gbuf + (size_t)slot * kW4GroupBytes + b * kWsfBytes, &tmSFW, &sh.g_full[slot],
+                            (kb & ~3) * 4, wy + b * kBlockRows);
+              ++w4load;
+            }
           }
           const int32_t kx = kb * (p.fp8 ? 128 : 64);
           if constexpr (kPair) {
@@ -919,6 +948,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int64_t i = gload > kGRing ? gload - kGRing : 0; i < gload; ++i)
         wait_drain(&sh.g_full[i % kGRing], (uint32_t)((i / kGRing) & 1), dl);
+      for (int64_t i = w4load > kW4Groups ? w4load - kW4Groups : 0; i < w4load; ++i)
+        wait_drain(&sh.g_full[i % kW4Groups], (uint32_t)((i / kW4Groups) & 1), dl);
       if (kPair && !ok) {
         // give the second CTA's operand copies still in flight time to land
         const uint64_t until = globaltimer_ns() + 100000ull;
@@ -972,12 +1003,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             // stage's atom (B scale id)
             const uint32_t idesc = p.fp8 ? (idesc0 | (sid << 29) | (kW4 ? 0u : (sid << 4))) : idesc0;
             if (kW4) {
-              const uint32_t atoms = smem_u32(sf_area + (size_t)stage * sf_bytes + kSfStage + 2 * kWsfBytes);
+              const uint32_t atoms = smem_u32(sfst + (size_t)stage * sf_bytes + kSfStage);
               tmem_cp_32x128b_x4_e(e0, sf_w, desc_sf_32x16(atoms));
               tmem_cp_32x128b_x4_e(e0, sf_w + 4, desc_sf_32x16(atoms + kWsfAtom));
             }
             if (p.fp8 && sid == 0) {
-              const uint32_t sfs = smem_u32(sf_area + (size_t)stage * sf_bytes);
+              const uint32_t sfs = smem_u32(sfst + (size_t)stage * sf_bytes);
               tmem_cp_32x128b_x4_e(e0, sf_tok, desc_sf_32x16(sfs + kSfRaw + 512));
               if (!kW4) {
                 tmem_cp_32x128b_x4_e(e0, sf_w, desc_sf_32x16(sfs + kSfRaw));
@@ -1045,7 +1076,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t idesc = p.fp8 ? (idesc0 | (sid << 4) | (kW4 ? 0u : (sid << 29))) : idesc0;
           if constexpr (!kPair) {
             if (kW4) {
-              const uint32_t atoms = smem_u32(sf_area + (size_t)stage * sf_bytes + kSfStage + 2 * kWsfBytes);
+              const uint32_t atoms = smem_u32(sfst + (size_t)stage * sf_bytes + kSfStage);
               for (int b = b_lo; b < b_hi; ++b)
                 tmem_cp_32x128b_x4_e(e0, my_sfa + 4 * (b - b_lo), desc_sf_32x16(atoms + b * kWsfAtom));
             }
@@ -1064,7 +1095,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               tmem_cp_32x128b_x4_pair_e(e0, my_sfb, desc_sf_32x16(sfs + kSfRaw + 512));
               if (qn > 128) tmem_cp_32x128b_x4_pair_e(e0, my_sfb + 4, desc_sf_32x16(sfs + kSfRaw + 1024));
             } else {
-              const uint32_t sfs = smem_u32(sf_area + (size_t)stage * sf_bytes);
+              const uint32_t sfs = smem_u32(sfst + (size_t)stage * sf_bytes);
               if (!kW4) {
                 // weight words of block b: at kSfRaw (block 0) or kSfW1 (block 1)
                 for (int b = b_lo; b < b_hi; ++b)
@@ -1141,6 +1172,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       const uint32_t grp0 = mapa_shared(smem_u32(&sh.sf_grp[0]), 0);
       uint32_t wgrp = 0;  // groups of words published
+      int64_t w4use = 0;    // FP4 weights: weight-scale groups read
+      uint32_t w4slot = 0;
       // weight scales of a tile's blocks: lane l holds K-blocks l + 32 i;
       // the next tile's are fetched while the current tile streams
       with_blocks([&](auto bc) {
@@ -1194,7 +1227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          uint8_t* sfs = sf_area + (size_t)stage * sf_bytes;
+          uint8_t* sfs = sfst + (size_t)stage * sf_bytes;
           if ((kb % kSfGroup) == 0) {
             // lane l, column c of a word block holds the word of row c*32 + l
             // (FP4 weights: only the token words are built here)
@@ -1206,14 +1239,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (kW4) {
+            if ((kb % kSfGroup) == 0) {
+              // release the previous group's slot, then take the group's boxes
+              __syncwarp();
+              if (w4use > 0 && lane == 0) mbar_arrive(&sh.sf_grp[w4slot]);
+              w4slot = (uint32_t)(w4use % kW4Groups);
+              if (!warp_wait(&sh.g_full[w4slot], (uint32_t)((w4use / kW4Groups) & 1), deadline, &sh.abort_flag,
+                             p.status)) {
+                ok = false;
+                break;
+              }
+              ++w4use;
+            }
             // this K-block's word of rows lane + 32 j, from the group's box
 #pragma unroll
             for (int b = 0; b < kB; ++b) {
-              const uint8_t* box = sfs + kSfStage + b * kWsfBytes + 4 * (kb & 3);
+              const uint8_t* box = gbuf + (size_t)w4slot * kW4GroupBytes + b * kWsfBytes + 4 * (kb & 3);
               uint32_t w[4];
 #pragma unroll
               for (int j = 0; j < 4; ++j) w[j] = *reinterpret_cast<const uint32_t*>(box + 16 * (lane + 32 * j));
-              *reinterpret_cast<uint4*>(sfs + kSfStage + 2 * kWsfBytes + b * kWsfAtom + lane * 16) =
+              *reinterpret_cast<uint4*>(sfs + kSfStage + b * kWsfAtom + lane * 16) =
                   make_uint4(w[0], w[1], w[2], w[3]);
             }
           }

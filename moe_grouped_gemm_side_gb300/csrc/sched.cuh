@@ -166,7 +166,8 @@ MG_HD int pick_tile(bool fp8, const int64_t (&token_tiles)[kNumTileCand], int va
 // 1.076), so it stays off there.
 // Ties go to the larger tile, then to two blocks.
 MG_HD void pick_tile_blocks(bool fp8, bool w4, const int64_t (&token_tiles)[kNumTileCand], int64_t N, int64_t KB,
-                            int num_sms, int64_t ring_bytes, int64_t sf_bytes, int* q_out, int* blocks_out) {
+                            int num_sms, int64_t ring_bytes, int64_t sf_bytes, int max_stages, int* q_out,
+                            int* blocks_out) {
   int64_t best = -1;
   int bq = tile_candidate(fp8, kNumTileCand - 1), bb = 2;
   for (int i = 0; i < kNumTileCand; ++i) {
@@ -175,7 +176,7 @@ MG_HD void pick_tile_blocks(bool fp8, bool w4, const int64_t (&token_tiles)[kNum
       const int64_t T = token_tiles[i] * (N / (128 * nb));
       const int64_t stage = 128 * (128 * (int64_t)nb + q) + sf_bytes;
       const int64_t S = (w4 && ring_bytes > 0) ? max64(1, ring_bytes / stage) : 0;
-      const int64_t floor = S > 0 ? kSelLoadRoundTrip / (S < 16 ? S : 16) : 0;
+      const int64_t floor = S > 0 ? kSelLoadRoundTrip / (S < max_stages ? S : max_stages) : 0;
       const int64_t cost = cdiv_fast(T, num_sms > 0 ? num_sms : 1) * tile_cost_cycles(fp8, q, KB, nb, q, floor);
       if (best < 0 || cost <= best) {
         best = cost;

@@ -52,10 +52,11 @@ def contiguous_case(counts, N, K, align_q, tile_q=0, seed=5, integer=True, dev="
     return A, SFA, B, SFB, R, written, rows_cap
 
 
-@pytest.mark.parametrize("tile_q", [0, 16, 64, 128, 240])
-def test_contiguous_integer_exact(lib, cuda, tile_q):
+@pytest.mark.parametrize("tile_q,K", [(0, 1024), (16, 1024), (64, 1024), (128, 1024), (240, 1024), (0, 1536),
+                                      (64, 512)])
+def test_contiguous_integer_exact(lib, cuda, tile_q, K):
     counts = [37, 0, 300, 1, 16, 129]
-    N, K = 768, 1024
+    N = 768
     A, SFA, B, SFB, R, written, rows_cap = contiguous_case(counts, N, K, 16, tile_q)
     D = gu.sentinel_like((rows_cap, N), cuda)
     status = torch.zeros(1, dtype=torch.int32, device=cuda)
@@ -129,8 +130,12 @@ def test_contiguous_float_operands(lib, cuda, seed):
     assert (Dbits[~written] == gu.SENTINEL_BITS).all()
 
 
-def test_masked_integer_exact(lib, cuda):
-    E, M, N, K = 6, 96, 512, 1024
+@pytest.mark.parametrize("K", [1024, 512, 2560])
+def test_masked_integer_exact(lib, cuda, K):
+    """(E2M1 weights need K % 512 == 0: whole 16-byte weight-scale rows.)
+    K = 512 runs one group of four K-blocks per tile, so the weight-scale
+    group ring turns over at every tile."""
+    E, M, N = 6, 96, 512
     valid = [96, 0, 17, 1, 64, 50]
     A = gu.integer_e4m3((E, M, K), 21, cuda)
     SFA = gu.rand_scales((E, K // 128, M), 22, cuda, 126, 128)
