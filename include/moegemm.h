@@ -311,8 +311,11 @@ mg_status mgemm_masked(mg_dtype dt, const void* A, const uint8_t* SFA,
  * rows = rows_cap (contiguous) or E*M_max (masked).  All other arguments,
  * requirements and device errors are those of mgemm_contiguous /
  * mgemm_masked.  N must be a multiple of 256 (else MG_ERR_UNSUPPORTED).
- * These calls always run the single-SM two-block kernel (tile = one gate
- * block and its up block), whatever mg_set_kernel_policy chose.
+ * mgemm_contiguous_swiglu runs CTA pairs (a tile: two feature blocks, each
+ * SM one gate block and its up block) where mgemm_contiguous would run the
+ * pair two-block family (N % 512 == 0, E4M3 or bf16 weights, default or
+ * pair-dual policy); otherwise, and for mgemm_masked_swiglu always, the
+ * single-SM two-block kernel (tile = one gate block and its up block).
  * ------------------------------------------------------------------------ */
 typedef enum {
   MG_SWIGLU_BF16 = 1,

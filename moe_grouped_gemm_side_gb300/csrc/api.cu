@@ -255,8 +255,8 @@ mg_status prep_masked(FwdArgs& a, mg_dtype dt, const void* A, const uint8_t* SFA
   return encode_operands(a, A, SFA, B, (int64_t)E * M_max, M_max, E, 4u);
 }
 
-// The SwiGLU epilogue pairs the two 128-row weight blocks of a single-SM
-// tile (gate, then up), so N must hold whole 256-row gate/up pairs.
+// The SwiGLU epilogue pairs a gate block with its up block in every SM's
+// two-block tile, so N must hold whole 256-row gate/up pairs.
 mg_status check_swiglu(mg_swiglu_out out, int32_t N, const uint8_t* SFY) {
   if (out != MG_SWIGLU_BF16 && out != MG_SWIGLU_FP8_E4M3_UE8M0) return MG_ERR_INVALID_ARG;
   if (N <= 0) return MG_ERR_INVALID_ARG;
@@ -393,7 +393,10 @@ mg_status mgemm_contiguous_swiglu(mg_dtype dt, mg_swiglu_out out, const void* A,
   st = prep_contiguous(a, dt, A, SFA, B, SFB, Y, d_counts, E, rows_cap, N, K, align_q, tile_q, d_status);
   if (st != MG_OK) return st;
   set_swiglu(a, out, SFY, rows_cap);
-  return from_cuda(launch_fwd(a, static_cast<cudaStream_t>(stream), kFwdDual));
+  // two-block tiles only: CTA pairs (two gate/up pairs per tile) where the
+  // plain call would run them, else one SM
+  const int v = fwd_variant(N, a.w4, false);
+  return from_cuda(launch_fwd(a, static_cast<cudaStream_t>(stream), v == kFwdPairDual ? kFwdPairDual : kFwdDual));
 }
 
 mg_status mgemm_masked_swiglu(mg_dtype dt, mg_swiglu_out out, const void* A, const uint8_t* SFA,

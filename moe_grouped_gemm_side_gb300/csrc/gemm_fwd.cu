@@ -288,26 +288,28 @@ __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// SwiGLU epilogue of a two-block tile on one SM ("flops/deepgemm-grouped-
-// masked-moe-gemm", "Workarounds": the expert's SwiGLU runs between the two
-// grouped GEMMs, and the FP8 path hands the second GEMM per-128 UE8M0-scaled
-// E4M3 activations).  GEMM1's weight rows are interleaved in 128-row blocks
-// (gate rows of features 128j..128j+127, then their up rows), so block 0 of
-// tile nb holds the gate and block 1 the up values of features
-// 128nb..128nb+127 and the thread owning TMEM lane l has both halves of one
-// feature:  y = SiLU(g) * u = g / (1 + e^-g) * u  in fp32.  The two warps of
-// a lane quadrant take alternate 16-token chunks, as in the plain epilogue.
+// SwiGLU epilogue of a two-block tile ("flops/deepgemm-grouped-masked-moe-
+// gemm", "Workarounds": the expert's SwiGLU runs between the two grouped
+// GEMMs, and the FP8 path hands the second GEMM per-128 UE8M0-scaled E4M3
+// activations).  GEMM1's weight rows are interleaved in 128-row blocks (gate
+// rows of features 128j..128j+127, then their up rows), and each SM loads
+// the gate block of its feature group fgrp as its block 0 and the up block
+// as its block 1 (one SM: fgrp = tile nb; a CTA pair: fgrp = 2 nb + rank,
+// the pair's M = 256 rows being two SMs' gate blocks, then their up blocks),
+// so the thread owning TMEM lane l has both halves of one feature:
+// y = SiLU(g) * u = g / (1 + e^-g) * u  in fp32.  The two warps of a lane
+// quadrant take alternate 16-token chunks, as in the plain epilogue.
 __device__ __forceinline__ float swiglu_f32(uint32_t g, uint32_t u) {
   const float gf = __uint_as_float(g);
   return __fdividef(gf, 1.0f + __expf(-gf)) * __uint_as_float(u);
 }
 
 // To bf16: lane pairs exchange so each store writes two features.
-__device__ __forceinline__ void swiglu_bf16_tile(const Params& p, const Tile& tl, uint32_t taddr,
+__device__ __forceinline__ void swiglu_bf16_tile(const Params& p, const Tile& tl, int32_t fgrp, uint32_t taddr,
                                                  uint32_t taddr_up, uint32_t quad, int32_t half,
                                                  uint32_t lane) {
   const int32_t I = p.N >> 1;
-  const int32_t f = tl.nb * kCtaRows + (int32_t)(quad * 32u + lane);  // this thread's feature
+  const int32_t f = fgrp * kCtaRows + (int32_t)(quad * 32u + lane);  // this thread's feature
   const bool odd = (lane & 1u) != 0;
   __nv_bfloat16* ypair = static_cast<__nv_bfloat16*>(p.D) + (int64_t)tl.row0 * I + (f & ~1);
   for (int32_t c0 = 16 * half; c0 < tl.qn; c0 += 32) {
@@ -345,12 +347,12 @@ __device__ __forceinline__ void swiglu_bf16_tile(const Params& p, const Tile& tl
 // tile's pass 1 cannot start before every epilogue warp has released this
 // tile's accumulator, so one buffer of maxima suffices.  Returns false if
 // the wait gave up.
-__device__ __forceinline__ bool swiglu_fp8_tile(const Params& p, Shared& sh, const Tile& tl,
+__device__ __forceinline__ bool swiglu_fp8_tile(const Params& p, Shared& sh, const Tile& tl, int32_t fgrp,
                                                 uint32_t taddr, uint32_t taddr_up, uint32_t quad,
                                                 int32_t half, uint32_t lane, uint32_t tile_par,
                                                 uint64_t deadline) {
   const int32_t I = p.N >> 1;
-  const int32_t f = tl.nb * kCtaRows + (int32_t)(quad * 32u + lane);
+  const int32_t f = fgrp * kCtaRows + (int32_t)(quad * 32u + lane);
   const bool odd = (lane & 1u) != 0;
   const int32_t t = (int32_t)(lane >> 1);
   for (int32_t c0 = 16 * half; c0 < tl.qn; c0 += 32) {
@@ -402,7 +404,7 @@ __device__ __forceinline__ bool swiglu_fp8_tile(const Params& p, Shared& sh, con
     // 2^(127-s): a normal float for s <= 253, the subnormal 2^-127 for s = 254
     const float inv = sc < 254 ? __uint_as_float((uint32_t)(254 - sc) << 23) : __uint_as_float(0x00400000u);
     if (quad == 0 && !odd && tok < tl.rows)
-      p.sfy[((int64_t)tl.sf_z * (I / kCtaRows) + tl.nb) * p.sfy_ld + tl.sf_x + tok] = (uint8_t)sc;
+      p.sfy[((int64_t)tl.sf_z * (I / kCtaRows) + fgrp) * p.sfy_ld + tl.sf_x + tok] = (uint8_t)sc;
     // codes of tokens 4w..4w+3 of this lane's feature, one word per w
     uint32_t wd[4];
 #pragma unroll
@@ -789,6 +791,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int32_t bal = sh.bal;
   const int32_t NB = p.N / (nblk * kBlockRows);  // tiles per token tile
   const int32_t tile_rows = nblk * kBlockRows;
+  // Weight rows of this SM's blocks: tile_rows * nb + rank * wrank + b * wstep.
+  // A pair with a SwiGLU epilogue takes each SM's gate block and its up
+  // block (128 rows apart in GEMM1's interleaved layout) rather than each
+  // SM's half of two 256-row blocks.
+  const bool swiglu_pair = kPair && p.epi != kEpiPlain;
+  const int32_t wrank = swiglu_pair ? 2 * kCtaRows : kCtaRows;
+  const int32_t wstep = swiglu_pair ? kCtaRows : kBlockRows;
   // Runs body with the launch's block count as a compile-time constant.
   auto with_blocks = [&](auto&& body) {
     if constexpr (kBlocks == 2) {
@@ -849,7 +858,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int32_t t = unit, ti = 0; ok && t < total; t += n_units, ++ti) {
         const Tile tl = nxt;
         const int32_t qc = kPair ? tl.qn >> 1 : tl.qn;   // token rows staged here
-        const int32_t wy = tl.e * p.N + tl.nb * tile_rows + (int32_t)rank * kCtaRows;
+        const int32_t wy = tl.e * p.N + tl.nb * tile_rows + (int32_t)rank * wrank;
         const int32_t ty = tl.row0 + (int32_t)rank * qc;
         // A packed E2M1 box counts its 8 KB of global data toward the barrier,
         // although it fills 16 KB of shared memory
@@ -902,7 +911,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t bar = mapa_shared(smem_u32(&sh.full[stage]), 0);
 #pragma unroll
             for (int b = 0; b < kBlocks; ++b)
-              if (b < nblk) tma_load_2d_pair(sw + b * kWTileBytes, &tmW, bar, kx, wy + b * kBlockRows);
+              if (b < nblk) tma_load_2d_pair(sw + b * kWTileBytes, &tmW, bar, kx, wy + b * wstep);
             for (int32_t r = 0; r < qc;) {
               const int32_t left = qc - r;
               const CUtensorMap* m = left >= 64 ? &tmA64 : (left >= 16 ? &tmA16 : &tmA8);
@@ -1183,7 +1192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Tile tl = decode_tile(t, tpre, cnt, rowbase, E, NB, q, p.masked, ttab, bal, total, n_units, p.fp8);
 #pragma unroll
         for (int b = 0; b < kB; ++b) {
-          const int32_t nb128 = (tl.nb * tile_rows + b * kBlockRows) / kCtaRows + (int32_t)rank;
+          const int32_t nb128 = (tl.nb * tile_rows + (int32_t)rank * wrank + b * wstep) / kCtaRows;
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int32_t kb = (int32_t)lane + 32 * i;
@@ -1299,7 +1308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       [[maybe_unused]] const uint32_t taddr1 = tacc1 + ((quad * 32u) << 16);
       bool released = false;  // this warp's arrival on acc_empty is made
       bool swiglu = false;
-      if constexpr (kB == 2 && !kPair && !kTokM) swiglu = p.epi != kEpiPlain;
+      if constexpr (kB == 2 && !kTokM) swiglu = p.epi != kEpiPlain;
       if (kTokM && third == 2) {
         // (not needed by this epilogue)
       } else if constexpr (kTokM) {
@@ -1336,8 +1345,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (third == 2) {
           // (not needed by this epilogue)
         } else if (p.epi == kEpiSwigluBf16) {
-          swiglu_bf16_tile(p, tl, taddr, taddr1, quad, half, lane);
-        } else if (!swiglu_fp8_tile(p, sh, tl, taddr, taddr1, quad, half, lane, tile_par, deadline)) {
+          swiglu_bf16_tile(p, tl, kPair ? 2 * tl.nb + (int32_t)rank : tl.nb, taddr, taddr1, quad, half, lane);
+        } else if (!swiglu_fp8_tile(p, sh, tl, kPair ? 2 * tl.nb + (int32_t)rank : tl.nb, taddr, taddr1, quad,
+                                    half, lane, tile_par, deadline)) {
           break;
         }
         tile_par ^= 1u;
@@ -1468,8 +1478,8 @@ cudaError_t launch(const FwdArgs& a, cudaStream_t s) {
     if (err != cudaSuccess) return err;
     attr_done[dev] = true;
   }
-  // the SwiGLU epilogue pairs the two blocks of a single-SM tile
-  if (a.epi != kEpiPlain && (kBlocks != 2 || kPair || kTokM)) return cudaErrorInvalidValue;
+  // the SwiGLU epilogue pairs the gate and up blocks of a two-block tile
+  if (a.epi != kEpiPlain && (kBlocks != 2 || kTokM)) return cudaErrorInvalidValue;
   if (a.w4 != kW4) return cudaErrorInvalidValue;
   Params p;
   p.counts = a.counts;

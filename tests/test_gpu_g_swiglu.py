@@ -216,13 +216,24 @@ def test_all_zero_block_gets_the_unit_scale(lib, cuda):
     assert (Y.cpu().numpy()[rows1, 128:256] & 0x7F == 0).all()
 
 
-def test_empty_and_policy_independent(lib, cuda):
+def test_empty(lib, cuda):
     res = run_contiguous_swiglu([0, 0, 0], 256, 256, "fp8", "fp8", 16)
     assert_contiguous(*res, "fp8")
+    res = run_contiguous_swiglu([0, 0], 1024, 512, "bf16", "bf16", 16)
+    assert_contiguous(*res, "bf16")
+
+
+@pytest.mark.parametrize("policy", ["auto", "single", "dual", "pair", "pair_dual", "tokm"])
+@pytest.mark.parametrize("dtype,out", [("fp8", "fp8"), ("bf16", "bf16")])
+def test_every_policy(lib, cuda, policy, dtype, out):
+    """Every family choice runs a two-block kernel: CTA pairs (each SM one
+    gate block and its up block) for auto and pair-dual with N % 512 == 0,
+    one SM otherwise; N = 1024 and 768 cover both."""
     try:
-        mb.set_kernel_policy(mb.POLICY_PAIR_DUAL)      # the SwiGLU calls ignore the family choice
-        res = run_contiguous_swiglu([5, 70], 512, 256, "fp8", "bf16", 16)
-        assert_contiguous(*res, "bf16")
+        mb.set_kernel_policy(mb.POLICIES[policy])
+        for N in (1024, 768):
+            res = run_contiguous_swiglu([5, 70, 0, 300], N, 256 if dtype == "bf16" else 512, dtype, out, 16)
+            assert_contiguous(*res, out)
     finally:
         mb.set_kernel_policy(mb.POLICY_AUTO)
 
