@@ -417,8 +417,8 @@ int64_t mg_get_wait_limit_ns(void);
  * (4 -> 3 -> 1, 2 -> 1, 5 -> 1, 0 -> 1).  The two-block families run
  * one-block tiles where the device finds them cheaper from the counts
  * (contiguous form: when two-block tiles would not fill two waves of
- * workers; masked form: priced together with the token tile).  Results are
- * identical up to fp32 summation order.
+ * workers; masked form: priced together with the token tile, E2M1 weights
+ * always two blocks).  Results are identical up to fp32 summation order.
  * Process-wide.  Returns MG_ERR_INVALID_ARG for other values.
  * ------------------------------------------------------------------------ */
 mg_status mg_set_kernel_policy(int32_t policy);
