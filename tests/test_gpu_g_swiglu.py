@@ -178,10 +178,12 @@ def assert_contiguous(Y, SFY, written, y, g, u, out, exact=True):
 @pytest.mark.parametrize("dtype", ["bf16", "fp8"])
 @pytest.mark.parametrize("out", ["bf16", "fp8"])
 @pytest.mark.parametrize("tile_q", [0, 16, 64, 240])
-def test_contiguous_integer(lib, cuda, dtype, out, tile_q):
+@pytest.mark.parametrize("N", [768, 1024])
+def test_contiguous_integer(lib, cuda, dtype, out, tile_q, N):
+    """N = 768 runs one SM per tile, N = 1024 CTA pairs."""
     counts = [37, 0, 300, 1, 16, 129]
     K = 256 if dtype == "bf16" else 512
-    res = run_contiguous_swiglu(counts, 768, K, dtype, out, 16, tile_q)
+    res = run_contiguous_swiglu(counts, N, K, dtype, out, 16, tile_q)
     assert_contiguous(*res, out)
 
 
