@@ -651,8 +651,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t ring = kSmemBytes - 2048 - (kW4 ? kW4Area : 0) -
                              (int64_t)(reinterpret_cast<uintptr_t>(sf_area) - reinterpret_cast<uintptr_t>(smem));
         const int64_t sfb = p.fp8 ? kSfStage + (kW4 ? kW4StageBytes : 0) : 0;
-        pick_tile_blocks(p.fp8 != 0, kW4, tiles, p.N, sel_kblocks(p.fp8 != 0, p.K), (int)gridDim.x, ring, sfb,
-                         kMaxStages, &q, &pb);
+        pick_tile_blocks_warp(p.fp8 != 0, kW4, tiles, p.N, sel_kblocks(p.fp8 != 0, p.K), (int)gridDim.x, ring, sfb,
+                              kMaxStages, &q, &pb);
         want_blocks = pb;
       } else {
         q = pick_tile(p.fp8 != 0, tiles, variant, p.N, sel_kblocks(p.fp8 != 0, p.K), (int)gridDim.x);

@@ -197,4 +197,40 @@ MG_HD void pick_tile_blocks(bool fp8, bool w4, const int64_t (&token_tiles)[kNum
   *blocks_out = bb;
 }
 
+#ifdef __CUDACC__
+// pick_tile_blocks with one candidate per lane (lane 2i + nb - 1 prices tile
+// candidate i with nb blocks) and a warp reduction to the cheapest, ties to
+// the higher lane, i.e. the same order of preference as the loop above.
+// Called by all 32 lanes of a warp; every lane gets the choice.  (In a GEMM
+// prologue whose instructions come from DRAM, eight candidates priced one
+// after another cost the 16-expert decode ~1.6 us.)
+__device__ __forceinline__ void pick_tile_blocks_warp(bool fp8, bool w4, const int64_t (&token_tiles)[kNumTileCand],
+                                                      int64_t N, int64_t KB, int num_sms, int64_t ring_bytes,
+                                                      int64_t sf_bytes, int max_stages, int* q_out, int* blocks_out) {
+  const int lane = (int)(threadIdx.x & 31u);
+  const int i = (lane >> 1) & (kNumTileCand - 1), nb = (lane & 1) + 1;
+  const bool valid = lane < 2 * kNumTileCand && (!w4 || nb == 2);
+  const int q = tile_candidate(fp8, i);
+  const int64_t tiles = i == 0 ? token_tiles[0] : i == 1 ? token_tiles[1] : i == 2 ? token_tiles[2] : token_tiles[3];
+  const int64_t T = tiles * (N / (128 * nb));
+  const int64_t stage = 128 * (128 * (int64_t)nb + q) + sf_bytes;
+  const int64_t S = (w4 && ring_bytes > 0) ? max64(1, ring_bytes / stage) : 0;
+  const int64_t floor = S > 0 ? kSelLoadRoundTrip / (S < max_stages ? S : max_stages) : 0;
+  int64_t cost = valid ? cdiv_fast(T, num_sms > 0 ? num_sms : 1) * tile_cost_cycles(fp8, q, KB, nb, q, floor)
+                       : INT64_MAX;
+  int best = lane;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const int64_t oc = __shfl_xor_sync(0xffffffffu, cost, o);
+    const int ol = __shfl_xor_sync(0xffffffffu, best, o);
+    if (oc < cost || (oc == cost && ol > best)) {
+      cost = oc;
+      best = ol;
+    }
+  }
+  *q_out = tile_candidate(fp8, (best >> 1) & (kNumTileCand - 1));
+  *blocks_out = (best & 1) + 1;
+}
+#endif
+
 }  // namespace mg
